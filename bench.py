@@ -1,0 +1,357 @@
+"""Benchmark of the composite multi-LoRA delta on GB300.
+
+One step = one pass of the whole hot path over one batch: build the
+adapter-ordered mapping from the batch's per-token pair lists, then apply the
+fused delta y += sum alpha (x A[:, :k]) B[:k, :] through the C ABI.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Prints one JSON line.  `value` is tokens/s over the timed steps with every
+input resident in HBM; the steps run from a captured CUDA graph and rotate
+over R independent replicas (pool, x, y, pair lists, mapping) whose total size
+exceeds twice the L2, so every step reads cold data from HBM.  `e2e` times the
+same step through lora_delta_apply_host from pinned host buffers, with the
+host->device copies of the step's inputs and the device->host copy of y
+inside the timed region.  `roofline` measures lora_delta_apply alone (same
+rotation) against the measured HBM copy bandwidth.  `--impl reference` times
+the fp64 CPU oracle on the host cores instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "composite-LoRA delta tokens/s and achieved HBM GB/s vs GB300 peak, per config"
+CONFIG_NAMES = {
+    "distinct": "distinct decode, q_proj 4096x4096, r=8, T=32, 3 unshared adapters/token, pool 96",
+    "zipf": "Zipf(1.5) decode, gate_proj 4096->14336, r=8, T=64, 2-4 adapters/token, pool 128",
+    "prefill": "sparse MoE-LoRA prefill, 4096x4096, r=16, 16 requests lognormal lengths, top-2 of 8, pool 64",
+    "sweep1": "rank sweep k_i~U{1..64}, k/v_proj 4096->1024, r_max=64, pool 1000, T=1",
+    "sweep8": "rank sweep k_i~U{1..64}, k/v_proj 4096->1024, r_max=64, pool 1000, T=8",
+    "sweep64": "rank sweep k_i~U{1..64}, k/v_proj 4096->1024, r_max=64, pool 1000, T=64",
+    "sweep256": "rank sweep k_i~U{1..64}, k/v_proj 4096->1024, r_max=64, pool 1000, T=256",
+}
+KERNEL_SOURCES = ["shrink.cu", "expand.cu", "mapping.cu", "api.cu", "internal.h", "ptx.cuh"]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def sources_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        fp = os.path.join(ROOT, "tenant_composite_lora_gb300", "csrc", f)
+        if os.path.exists(fp):
+            h.update(open(fp, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: str):
+    """dram bytes per lora_delta_apply from a committed ncu summary, valid
+    only while the kernel sources are unchanged."""
+    fp = os.path.join(ROOT, "profiles", f"traffic_{config}.txt")
+    if not os.path.exists(fp):
+        return None
+    kv = {}
+    for line in open(fp):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("sources_sha256_16") != sources_digest():
+        return None
+    try:
+        return int(kv["dram_bytes_per_apply"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n):
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1, None
+    import torch.distributed as dist
+    dist.init_process_group("nccl" if os.environ.get("TCL_BENCH_BACKEND") != "gloo" else "gloo")
+    return dist.get_rank(), dist.get_world_size(), dist
+
+
+def bench_ours(args, rank, world, dist):
+    import torch
+    import tenant_composite_lora_gb300 as tcl
+    from tenant_composite_lora_gb300 import native
+    import workloads as W
+    from workloads.device import bf16_tensor, bf16_to_numpy_bits
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.Stream(device=dev)
+    wl = W.make(args.config)
+    ab = W.algorithmic_bytes(wl)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    R = max(2, int(np.ceil(2.0 * l2 / max(ab["total"], 1))))
+    R = min(R, args.max_replicas)
+
+    with torch.cuda.stream(stream):
+        # replicas: pools registered from the same factors, separate buffers
+        A_t = [bf16_tensor(wl.A[a], dev) for a in range(wl.capacity)]
+        B_t = [bf16_tensor(wl.B[a], dev) for a in range(wl.capacity)]
+        reps = []
+        for r in range(R):
+            pool = tcl.LoraPool(wl.d_in, wl.d_out, wl.r_max, wl.capacity)
+            for a in range(wl.capacity):
+                pool.register(a, A_t[a], B_t[a], int(wl.ranks[a]))
+            mp = tcl.LoraMapping(wl.T, wl.P, wl.capacity)
+            rep = dict(pool=pool, mapping=mp,
+                       off=torch.from_numpy(wl.offsets).to(dev), ids=torch.from_numpy(wl.ids).to(dev),
+                       alpha=torch.from_numpy(wl.alpha).to(dev), x=bf16_tensor(wl.x, dev),
+                       y0=bf16_tensor(wl.y, dev), y=bf16_tensor(wl.y, dev))
+            reps.append(rep)
+        del A_t, B_t
+        torch.cuda.synchronize()
+
+        def step(rep):
+            native.lora_build_mapping(rep["mapping"].handle, rep["off"], rep["ids"], rep["alpha"],
+                                      wl.T, wl.P, stream)
+            native.lora_delta_apply(rep["x"], rep["y"], rep["pool"].handle, None, rep["mapping"].handle, stream)
+
+        def apply_only(rep):
+            native.lora_delta_apply(rep["x"], rep["y"], rep["pool"].handle, None, rep["mapping"].handle, stream)
+
+        # correctness spot check of replica 0 (one step from y0)
+        reps[0]["y"].copy_(reps[0]["y0"])
+        step(reps[0])
+        stream.synchronize()
+        st = native.lora_mapping_status(reps[0]["mapping"].handle, stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st}")
+
+        # graphs: one pass over all replicas
+        def capture(fn):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for rep in reps:
+                    fn(rep)
+            return g
+
+        for rep in reps:  # build every mapping once before the apply-only graph
+            native.lora_build_mapping(rep["mapping"].handle, rep["off"], rep["ids"], rep["alpha"],
+                                      wl.T, wl.P, stream)
+        g_step = capture(step)
+        g_apply = capture(apply_only)
+        stream.synchronize()
+
+        def timed(graph, passes):
+            for _ in range(max(1, args.warmup)):
+                graph.replay()
+            stream.synchronize()
+            if dist is not None:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(passes):
+                graph.replay()
+            e1.record(stream)
+            e1.synchronize()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            if dist is not None:
+                t = torch.tensor([ms], dtype=torch.float64, device=dev)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                ms = float(t.item())
+            return ms
+
+        passes = max(1, int(np.ceil(args.steps / R)))
+        clk = ClockSampler(local)
+        ms_step_total = timed(g_step, passes)
+        clocks = clk.stop()
+        steps_done = passes * R
+        ms_per_step = ms_step_total / steps_done
+        ms_apply = timed(g_apply, passes) / steps_done
+
+        # end to end through the host entry point (pinned buffers, copies timed)
+        x_h = torch.from_numpy(wl.x.view(np.int16).copy()).pin_memory()
+        y_h = torch.from_numpy(wl.y.view(np.int16).copy()).pin_memory()
+        off_h = torch.from_numpy(wl.offsets).pin_memory()
+        ids_h = torch.from_numpy(wl.ids).pin_memory()
+        al_h = torch.from_numpy(wl.alpha).pin_memory()
+        rep = reps[0]
+        for _ in range(max(1, args.warmup)):
+            native.lora_delta_apply_host(x_h, y_h, off_h, ids_h, al_h, wl.T, wl.P, rep["pool"].handle, None,
+                                         rep["mapping"].handle, stream)
+        stream.synchronize()
+        e2e_steps = max(args.steps, 10)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            native.lora_delta_apply_host(x_h, y_h, off_h, ids_h, al_h, wl.T, wl.P, rep["pool"].handle, None,
+                                         rep["mapping"].handle, stream)
+        e1.record(stream)
+        e1.synchronize()
+        ms_e2e = e0.elapsed_time(e1) / e2e_steps
+        h2d = wl.x.nbytes + wl.y.nbytes + wl.offsets.nbytes + wl.ids.nbytes + wl.alpha.nbytes
+        d2h = wl.y.nbytes
+
+    peak, peak_kind = peaks()
+    achieved = ab["total"] / (ms_apply * 1e-3) / 1e9
+    value = world * wl.T / (ms_per_step * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps_done,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy draws shaped like the pages' workloads)",
+        "config": {
+            "workload": args.config, "desc": CONFIG_NAMES.get(args.config, args.config),
+            "T": wl.T, "P": wl.P, "d_in": wl.d_in, "d_out": wl.d_out, "r_max": wl.r_max,
+            "pool": wl.capacity, "distinct_adapters": ab["U"], "sum_k": ab["sum_k"],
+            "step": "lora_build_mapping + lora_delta_apply",
+            "l2_protocol": f"inputs larger than L2: {R} rotating replicas, {R * ab['total'] / 1e6:.0f} MB "
+                           f"touched per pass vs {l2 / 1e6:.0f} MB L2",
+            "parallelism": "replicas only" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "lora_delta_apply (shrink + expand, PDL-overlapped)",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+            "algorithmic_bytes": ab["total"], "apply_us": round(ms_apply * 1e3, 3),
+            "traffic": ncu_traffic(args.config),
+        },
+        "e2e": {"value": round(world * wl.T / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 6),
+                "api": "lora_delta_apply_host"},
+        "gpu_launches": 3 * steps_done,
+        "clocks": clocks,
+    }
+    return line, wl
+
+
+def oracle_baseline(wl, budget_s: float):
+    import oracle
+    th = oracle.max_threads()
+    t0 = time.perf_counter()
+    n = 0
+    tokens = 0
+    # whole batches while the budget lasts (at least one)
+    while True:
+        oracle.apply_workload(wl, threads=th, want_acc=False)
+        n += 1
+        tokens += wl.T
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens / dt, 3), "unit": "tokens/s", "cores": th, "kind": "oracle",
+            "sample": f"{n} full batch(es) of the workload ({tokens} tokens, fp64, OpenMP over tokens)",
+            "seconds": round(dt, 2)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="distinct", choices=sorted(CONFIG_NAMES))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--max-replicas", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank, world, dist = dist_setup(args.gpus)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import workloads as W
+        wl = W.make(args.config)
+        cb = oracle_baseline(wl, args.cpu_seconds)
+        line = {"metric": METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": 1, "steps": 1,
+                "warmup": 0, "ms_per_step": round(1e3 * wl.T / cb["value"], 3), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": args.config, "desc": CONFIG_NAMES[args.config]},
+                "impl": "reference", "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    line, wl = bench_ours(args, rank, world, dist)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_baseline(wl, args.cpu_seconds)
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,230 @@
+/*
+ * lora.h -- C ABI of the GB300 composite multi-LoRA delta library
+ * (libtclora.so).
+ *
+ * The library computes, for every token t of a mixed batch,
+ *
+ *     y_t  +=  sum over the pairs (i, alpha) of token t of  alpha * (x_t A_i[:, :k_i]) B_i[:k_i, :]
+ *
+ * with A_i in R^{d_in x r_max}, B_i in R^{r_max x d_out} held in a device
+ * pool, k_i <= r_max the retained rank of adapter i, bf16 operands, fp32
+ * accumulation and one round-to-nearest-even to bf16 of the result.
+ *
+ * Where the operation comes from:
+ *  - the composite update dW = sum_i alpha_i B_i A_i^T, with weights fixed per
+ *    request (LoRA-Soup style) or computed per token (MoE-LoRA style), served
+ *    on one path: DyMerge-LoRA summary page, "Core idea" (paper Sec. 3.1, M1);
+ *  - post-merge fusion: only the base factors are cached and all token-LoRA
+ *    pairs of a batch are fused in one pass at kernel time, with the pairs
+ *    reordered by LoRA id in a mapping stage: same page, "One-minute summary"
+ *    and "Core idea" (paper Sec. 4.3, Algorithm 2, Figure 8);
+ *  - one LoRA on one projection, W' = W + A B: ELORA summary page, Sec. 1.2
+ *    (Eq. 1) and Sec. 1.3 (Eq. 2);
+ *  - the retained-rank contract (a sorted factor prefix plus an effective
+ *    rank k_m per module carried as device metadata) and the shrink /
+ *    RowExpand split with phase-, rank- and shape-aware dispatch: LoRAForge
+ *    summary page, "Key contributions" and "Approach" (1), (4), (5).
+ *
+ * Conventions (all entry points):
+ *  - Row form: y (T x d_out) += x (T x d_in) . A (d_in x k) . B (k x d_out).
+ *  - All device arrays are row-major and C-contiguous.  bf16 arrays are passed
+ *    as void* holding IEEE bfloat16 bit patterns.  Device pointers must be
+ *    16-byte aligned (any cudaMalloc'd base is).
+ *  - lora_stream_t is a cudaStream_t (NULL = the legacy default stream).
+ *    Every call is stream-ordered and asynchronous unless stated otherwise;
+ *    the caller keeps every buffer it passes alive until the stream reaches
+ *    the call.
+ *  - Errors that the host can see (NULL pointers, sizes out of range, a
+ *    mismatched object) return a status and launch nothing.  Errors that only
+ *    the device can see (an adapter id outside the pool, an unregistered
+ *    slot, a retained rank above r_max, malformed CSR offsets) make the
+ *    offending pairs contribute nothing and set bits in the mapping's device
+ *    status word, read with lora_mapping_status().  No kernel traps.
+ *  - Objects are tied to the CUDA device that was current when they were
+ *    created; call with that device current.
+ */
+#ifndef TCLORA_LORA_H
+#define TCLORA_LORA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_ERR_INVALID_ARG = 1,
+    LORA_ERR_OUT_OF_MEMORY = 2,
+    LORA_ERR_CUDA = 3,
+    LORA_ERR_BAD_ADAPTER = 4,
+    LORA_ERR_NOT_SUPPORTED = 5
+} lora_status;
+
+/* Bits of the mapping's device status word (lora_mapping_status). */
+#define LORA_DEV_BAD_ID 1       /* a pair's adapter id is outside [0, capacity) */
+#define LORA_DEV_BAD_OFFSETS 2  /* CSR offsets not a row pointer for P pairs    */
+#define LORA_DEV_UNREGISTERED 4 /* a pair names a slot never registered          */
+#define LORA_DEV_BAD_RANK 8     /* a retained rank outside [0, r_max]            */
+#define LORA_DEV_TIMEOUT 16     /* a bounded on-chip wait gave up                */
+
+/* Limits of this implementation. */
+#define LORA_MAX_RANK 64          /* r_max                                    */
+#define LORA_MAX_CAPACITY 49152   /* adapters per pool / mapping key range    */
+#define LORA_MAX_PAIRS (1 << 24)
+#define LORA_MAX_TOKENS (1 << 24)
+#define LORA_DIM_MULTIPLE 64      /* d_in and d_out must be multiples of this */
+
+/* Execution paths of lora_delta_apply_path (LoRAForge page, "Approach" (5):
+ * the path is fixed per phase, rank and shape). */
+typedef enum {
+    LORA_PATH_AUTO = 0,    /* the dispatch table chooses                       */
+    LORA_PATH_SPLIT = 1,   /* segment shrink, then token-block RowExpand (PDL) */
+    LORA_PATH_FUSED = 2,   /* one-launch decode kernel (small T)               */
+    LORA_PATH_MMA = 3      /* tensor-core prefill (many tokens per adapter)    */
+} lora_path;
+
+typedef void *lora_stream_t;
+typedef struct lora_pool lora_pool;       /* opaque, library-owned device storage   */
+typedef struct lora_mapping lora_mapping; /* opaque, library-owned device workspace */
+
+/*
+ * lora_pool_create: a device pool of `capacity` adapter slots, each holding
+ * A_i (d_in x r_max) and B_i (r_max x d_out) in bf16 and a retained rank.
+ * Storage is zeroed and every slot starts unregistered.  Synchronous.
+ *   d_in, d_out : multiples of LORA_DIM_MULTIPLE, >= 64
+ *   r_max       : 1..LORA_MAX_RANK
+ *   capacity    : 1..LORA_MAX_CAPACITY
+ *   out         : receives the pool; release with lora_pool_destroy.
+ * Returns LORA_ERR_INVALID_ARG / LORA_ERR_NOT_SUPPORTED on bad sizes,
+ * LORA_ERR_OUT_OF_MEMORY if the device allocation fails.
+ * (DyMerge-LoRA page, "Core idea": only the base {A_i, B_i} are cached on the
+ * GPU; ELORA page, Sec. 1.2.3: adapters are stored sliced along the rank.)
+ */
+lora_status lora_pool_create(int d_in, int d_out, int r_max, int capacity, lora_pool **out);
+
+/*
+ * lora_pool_register: copy adapter `slot`'s factors into the pool and set its
+ * retained rank k (LoRAForge page, "Approach" (1): the factors are a sorted
+ * prefix, k_m directions are live, padding beyond k_m is inert).
+ *   A_dev : device bf16 [d_in][r_max] (A_i in R^{d_in x r})
+ *   B_dev : device bf16 [r_max][d_out]
+ *   k     : 0..r_max; rows/columns at index >= k are never read by the delta
+ * The pool stores A transposed (r_max x d_in) so that the first k rows of
+ * both factors are contiguous.  Stream-ordered; the caller keeps ownership of
+ * A_dev and B_dev, which must stay valid until the stream reaches the call.
+ * Re-registering a slot replaces it (order it after any delta still reading it).
+ */
+lora_status lora_pool_register(lora_pool *pool, int slot, const void *A_dev, const void *B_dev,
+                               int k, lora_stream_t stream);
+
+/* lora_pool_unregister: mark `slot` unregistered (stream-ordered). */
+lora_status lora_pool_unregister(lora_pool *pool, int slot, lora_stream_t stream);
+
+/* lora_pool_destroy: synchronise the device and free the pool.  NULL is a no-op. */
+lora_status lora_pool_destroy(lora_pool *pool);
+
+/*
+ * lora_mapping_create: device workspace for batches of up to max_tokens
+ * tokens and max_pairs (token, adapter) pairs over adapter ids in
+ * [0, capacity).  Holds the adapter-ordered tuples, their inverse
+ * permutation, the segments, the shrink output z (max_pairs x LORA_MAX_RANK
+ * fp32) and the device status word.  Synchronous.
+ */
+lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lora_mapping **out);
+
+/*
+ * lora_build_mapping: the mapping stage of the fused kernel (DyMerge-LoRA
+ * page, "Core idea" and "Reading map": tuples (i, j, k, w) built per batch,
+ * reordered by LoRA id so that one CTA processes one adapter's tokens
+ * together; paper Sec. 4.3, Algorithm 2, Figure 8).
+ *   offsets_dev : int32 [T+1], CSR row pointer of each token's pair list
+ *   ids_dev     : int32 [P], adapter id of pair p (CSR order)
+ *   alpha_dev   : fp32 [P], weight of pair p
+ *   T, P        : 0 <= T <= max_tokens, 0 <= P <= max_pairs
+ * Result (device, inside the mapping): tuples (token, adapter, alpha, src=p)
+ * ordered by (adapter, p) -- a stable sort on adapter id --, the inverse
+ * permutation pos[p] (-1 for a pair left out), the distinct adapters in
+ * ascending order with their segment starts.  Pairs with an id outside
+ * [0, capacity) are left out and set LORA_DEV_BAD_ID; malformed offsets give
+ * an empty mapping and set LORA_DEV_BAD_OFFSETS.  Clears the status word.
+ * One mapping serves every lora_delta_apply on the same batch (all
+ * projections and layers).  The input arrays need to stay valid only until
+ * the stream reaches this call.
+ */
+lora_status lora_build_mapping(lora_mapping *m, const int32_t *offsets_dev, const int32_t *ids_dev,
+                               const float *alpha_dev, int T, int P, lora_stream_t stream);
+
+/*
+ * lora_delta_apply: y += sum over each token's pairs of alpha (x A[:, :k]) B[:k, :]
+ * (the composite delta above), in place, fused over all pairs of the batch.
+ *   x_dev     : device bf16 [T][d_in]  (T of the last lora_build_mapping)
+ *   y_dev     : device bf16 [T][d_out], read and written; must not alias x
+ *   pool      : adapters; its capacity must equal the mapping's
+ *   ranks_dev : device int32 [capacity] retained rank per slot, or NULL to use
+ *               the ranks given at registration.  A value outside [0, r_max]
+ *               sets LORA_DEV_BAD_RANK and that adapter contributes nothing.
+ *   m         : a mapping built for this batch
+ * Accumulates in fp32 and rounds once to bf16 (nearest even).  Chooses its
+ * kernels with the dispatch table of lora_dispatch_choose.  Stream-ordered,
+ * no host synchronisation, no allocation: safe to capture in a CUDA graph.
+ */
+lora_status lora_delta_apply(const void *x_dev, void *y_dev, const lora_pool *pool,
+                             const int32_t *ranks_dev, const lora_mapping *m, lora_stream_t stream);
+
+/* lora_delta_apply_path: lora_delta_apply with the execution path forced
+ * (LORA_PATH_AUTO = the dispatch table).  Returns LORA_ERR_NOT_SUPPORTED if the
+ * path cannot run this shape. */
+lora_status lora_delta_apply_path(const void *x_dev, void *y_dev, const lora_pool *pool,
+                                  const int32_t *ranks_dev, const lora_mapping *m, int path,
+                                  lora_stream_t stream);
+
+/*
+ * lora_dispatch_choose: the dispatch table, host only (no device work).
+ * Returns the lora_path that lora_delta_apply takes for T tokens, P pairs,
+ * the given r_max, d_in and d_out.  (LoRAForge page, "Approach" (5).)
+ */
+int lora_dispatch_choose(int T, int P, int r_max, int d_in, int d_out);
+
+/*
+ * lora_delta_apply_host: one whole step from HOST buffers (pinned memory
+ * recommended): copy offsets, ids, alpha, x and y to the device, build the
+ * mapping, apply the delta and copy y back into y_host.  Device staging is
+ * allocated inside the mapping on the first call for a given (d_in, d_out)
+ * and reused after.  Stream-ordered: y_host is valid after the stream
+ * synchronises.  Same element layouts as the device calls.
+ */
+lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_t *offsets_host,
+                                  const int32_t *ids_host, const float *alpha_host, int T, int P,
+                                  const lora_pool *pool, const int32_t *ranks_dev, lora_mapping *m,
+                                  lora_stream_t stream);
+
+/* lora_mapping_status: synchronise `stream` and return the device status word
+ * (LORA_DEV_* bits) accumulated since the last lora_build_mapping. */
+lora_status lora_mapping_status(const lora_mapping *m, lora_stream_t stream, int *device_error);
+
+/*
+ * lora_mapping_export: synchronise `stream` and copy the mapping into HOST
+ * buffers (for checking it; any pointer may be NULL to skip that array):
+ *   tok, adapter, alpha, src : [P_valid]   the ordered tuples
+ *   pos                      : [P]         inverse permutation (-1 = left out)
+ *   seg_adapter : [U], seg_start : [U+1]
+ *   counts : int32 [3] = { U, P_valid, status word }
+ */
+lora_status lora_mapping_export(const lora_mapping *m, lora_stream_t stream, int32_t *tok,
+                                int32_t *adapter, float *alpha, int32_t *src, int32_t *pos,
+                                int32_t *seg_adapter, int32_t *seg_start, int32_t *counts);
+
+/* lora_mapping_destroy: synchronise the device and free the mapping. */
+lora_status lora_mapping_destroy(lora_mapping *m);
+
+/* lora_status_string: a static description of a status code. */
+const char *lora_status_string(lora_status s);
+
+/* lora_version: the library version string. */
+const char *lora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TCLORA_LORA_H */

@@ -1,0 +1,479 @@
+// The C ABI declared in include/lora.h: objects, argument checks, dispatch.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "internal.h"
+
+struct lora_pool {
+    int d_in, d_out, r_max, capacity, device;
+    __nv_bfloat16 *At;  // [capacity][r_max][d_in]
+    __nv_bfloat16 *B;   // [capacity][r_max][d_out]
+    int32_t *reg_rank;  // [capacity]
+};
+
+struct lora_mapping {
+    int max_tokens, max_pairs, capacity, device;
+    int T, P;
+    bool built;
+    tcl::MapDev dev;
+    // staging of lora_delta_apply_host
+    void *sx, *sy;
+    int32_t *soff, *sids;
+    float *salpha;
+    int s_d_in, s_d_out;
+};
+
+namespace tcl {
+
+namespace {
+
+__global__ void k_transpose_bf16(const __nv_bfloat16 *__restrict__ src, __nv_bfloat16 *__restrict__ dst, int rows,
+                                 int cols)
+{
+    // dst[c][r] = src[r][c], 32 x 32 tiles through shared memory
+    __shared__ __nv_bfloat16 tile[32][33];
+    const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int r = r0 + i, c = c0 + threadIdx.x;
+        if (r < rows && c < cols)
+            tile[i][threadIdx.x] = src[(size_t)r * cols + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int c = c0 + i, r = r0 + threadIdx.x;
+        if (r < rows && c < cols)
+            dst[(size_t)c * rows + r] = tile[threadIdx.x][i];
+    }
+}
+
+__global__ void k_set_int(int32_t *p, int v) { *p = v; }
+
+int g_sm_count = 0;
+int g_sm_dev = -1;
+
+}  // namespace
+
+cudaError_t launch_transpose_bf16(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int rows, int cols,
+                                  cudaStream_t st)
+{
+    dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
+    k_transpose_bf16<<<grid, block, 0, st>>>(src, dst, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_set_int(int32_t *p, int v, cudaStream_t st)
+{
+    k_set_int<<<1, 1, 0, st>>>(p, v);
+    return cudaGetLastError();
+}
+
+int sm_count()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev != g_sm_dev) {
+        cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev);
+        g_sm_dev = dev;
+    }
+    return g_sm_count > 0 ? g_sm_count : 1;
+}
+
+}  // namespace tcl
+
+using namespace tcl;
+
+namespace {
+
+lora_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess)
+        return LORA_OK;
+    if (e == cudaErrorMemoryAllocation)
+        return LORA_ERR_OUT_OF_MEMORY;
+    return LORA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PoolDev pool_dev(const lora_pool *p)
+{
+    PoolDev d;
+    d.At = p->At;
+    d.B = p->B;
+    d.reg_rank = p->reg_rank;
+    d.d_in = p->d_in;
+    d.d_out = p->d_out;
+    d.r_max = p->r_max;
+    d.capacity = p->capacity;
+    return d;
+}
+
+template <typename T>
+cudaError_t dalloc(T **p, size_t count)
+{
+    return cudaMalloc(reinterpret_cast<void **>(p), (count > 0 ? count : 1) * sizeof(T));
+}
+
+void free_mapping(lora_mapping *m)
+{
+    MapDev &d = m->dev;
+    void *ptrs[] = {d.tok, d.adapter, d.src, d.pos, d.alpha, d.seg_adapter, d.seg_start, d.tile,
+                    d.tmp_tok, d.hdr, d.z, m->sx, m->sy, m->soff, m->sids, m->salpha};
+    for (void *p : ptrs)
+        if (p)
+            cudaFree(p);
+    std::free(m);
+}
+
+// Dispatch table (LoRAForge page, "Approach" (5): native path or a special
+// kernel, fixed by phase, rank and shape).
+int choose_path(int T, int P, int r_max, int d_in, int d_out)
+{
+    (void)P;
+    (void)r_max;
+    (void)d_in;
+    (void)d_out;
+    (void)T;
+    return LORA_PATH_SPLIT;
+}
+
+// Token block of the expand kernel: the largest of 64, 32, 16, 8 that still
+// gives at least one CTA per SM.
+int choose_tb(int T, int d_out)
+{
+    const int n_ct = d_out / EXP_W, sms = sm_count();
+    int tb = EXP_TB_MAX;
+    while (tb > 8 && (long long)n_ct * ((T + tb - 1) / tb) < sms)
+        tb >>= 1;
+    return tb;
+}
+
+lora_status run_split(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
+                      cudaStream_t st)
+{
+    const PoolDev pd = pool_dev(pool);
+    const int grid = sm_count();
+    cudaError_t e = launch_shrink(static_cast<const __nv_bfloat16 *>(x), pd, ranks, m->dev, SHRINK_RG, grid, st);
+    if (e != cudaSuccess)
+        return from_cuda(e);
+    e = launch_expand(static_cast<__nv_bfloat16 *>(y), pd, ranks, m->dev, m->T, choose_tb(m->T, pool->d_out),
+                      /*pdl=*/true, st);
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lora_status_string(lora_status s)
+{
+    switch (s) {
+    case LORA_OK:
+        return "ok";
+    case LORA_ERR_INVALID_ARG:
+        return "invalid argument";
+    case LORA_ERR_OUT_OF_MEMORY:
+        return "out of device memory";
+    case LORA_ERR_CUDA:
+        return "CUDA error";
+    case LORA_ERR_BAD_ADAPTER:
+        return "bad adapter slot or rank";
+    case LORA_ERR_NOT_SUPPORTED:
+        return "not supported by this implementation";
+    }
+    return "unknown status";
+}
+
+const char *lora_version(void) { return "tclora 0.1 (sm_103a)"; }
+
+int lora_dispatch_choose(int T, int P, int r_max, int d_in, int d_out)
+{
+    return choose_path(T, P, r_max, d_in, d_out);
+}
+
+lora_status lora_pool_create(int d_in, int d_out, int r_max, int capacity, lora_pool **out)
+{
+    if (!out)
+        return LORA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (d_in <= 0 || d_out <= 0 || r_max <= 0 || capacity <= 0)
+        return LORA_ERR_INVALID_ARG;
+    if (d_in % LORA_DIM_MULTIPLE || d_out % LORA_DIM_MULTIPLE || r_max > LORA_MAX_RANK ||
+        capacity > LORA_MAX_CAPACITY)
+        return LORA_ERR_NOT_SUPPORTED;
+    lora_pool *p = static_cast<lora_pool *>(std::calloc(1, sizeof(lora_pool)));
+    if (!p)
+        return LORA_ERR_OUT_OF_MEMORY;
+    p->d_in = d_in;
+    p->d_out = d_out;
+    p->r_max = r_max;
+    p->capacity = capacity;
+    cudaGetDevice(&p->device);
+    const size_t na = (size_t)capacity * r_max * d_in, nb = (size_t)capacity * r_max * d_out;
+    cudaError_t e = dalloc(&p->At, na);
+    if (e == cudaSuccess)
+        e = dalloc(&p->B, nb);
+    if (e == cudaSuccess)
+        e = dalloc(&p->reg_rank, (size_t)capacity);
+    if (e == cudaSuccess)
+        e = cudaMemset(p->At, 0, na * sizeof(__nv_bfloat16));
+    if (e == cudaSuccess)
+        e = cudaMemset(p->B, 0, nb * sizeof(__nv_bfloat16));
+    if (e == cudaSuccess)
+        e = cudaMemset(p->reg_rank, 0xff, (size_t)capacity * sizeof(int32_t));  // -1: unregistered
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        if (p->At)
+            cudaFree(p->At);
+        if (p->B)
+            cudaFree(p->B);
+        if (p->reg_rank)
+            cudaFree(p->reg_rank);
+        std::free(p);
+        return from_cuda(e);
+    }
+    *out = p;
+    return LORA_OK;
+}
+
+lora_status lora_pool_register(lora_pool *pool, int slot, const void *A_dev, const void *B_dev, int k,
+                               lora_stream_t stream)
+{
+    if (!pool || !A_dev || !B_dev || slot < 0 || slot >= pool->capacity || k < 0 || k > pool->r_max)
+        return LORA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t off_a = (size_t)slot * pool->r_max * pool->d_in;
+    const size_t off_b = (size_t)slot * pool->r_max * pool->d_out;
+    cudaError_t e = launch_transpose_bf16(static_cast<const __nv_bfloat16 *>(A_dev), pool->At + off_a, pool->d_in,
+                                          pool->r_max, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(pool->B + off_b, B_dev, (size_t)pool->r_max * pool->d_out * sizeof(__nv_bfloat16),
+                            cudaMemcpyDeviceToDevice, st);
+    if (e == cudaSuccess)
+        e = launch_set_int(pool->reg_rank + slot, k, st);
+    return from_cuda(e);
+}
+
+lora_status lora_pool_unregister(lora_pool *pool, int slot, lora_stream_t stream)
+{
+    if (!pool || slot < 0 || slot >= pool->capacity)
+        return LORA_ERR_INVALID_ARG;
+    return from_cuda(launch_set_int(pool->reg_rank + slot, -1, static_cast<cudaStream_t>(stream)));
+}
+
+lora_status lora_pool_destroy(lora_pool *pool)
+{
+    if (!pool)
+        return LORA_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaFree(pool->At);
+    cudaFree(pool->B);
+    cudaFree(pool->reg_rank);
+    std::free(pool);
+    return from_cuda(e);
+}
+
+lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lora_mapping **out)
+{
+    if (!out)
+        return LORA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (max_tokens < 0 || max_pairs < 0 || capacity <= 0)
+        return LORA_ERR_INVALID_ARG;
+    if (max_tokens > LORA_MAX_TOKENS || max_pairs > LORA_MAX_PAIRS || capacity > LORA_MAX_CAPACITY)
+        return LORA_ERR_NOT_SUPPORTED;
+    lora_mapping *m = static_cast<lora_mapping *>(std::calloc(1, sizeof(lora_mapping)));
+    if (!m)
+        return LORA_ERR_OUT_OF_MEMORY;
+    m->max_tokens = max_tokens;
+    m->max_pairs = max_pairs;
+    m->capacity = capacity;
+    cudaGetDevice(&m->device);
+    MapDev &d = m->dev;
+    const size_t P = (size_t)max_pairs;
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = dalloc(&d.tok, P);
+    if (e == cudaSuccess) e = dalloc(&d.adapter, P);
+    if (e == cudaSuccess) e = dalloc(&d.src, P);
+    if (e == cudaSuccess) e = dalloc(&d.pos, P);
+    if (e == cudaSuccess) e = dalloc(&d.alpha, P);
+    if (e == cudaSuccess) e = dalloc(&d.seg_adapter, (size_t)capacity);
+    if (e == cudaSuccess) e = dalloc(&d.seg_start, (size_t)capacity + 1);
+    if (e == cudaSuccess) e = dalloc(&d.tile, P);
+    if (e == cudaSuccess) e = dalloc(&d.tmp_tok, P);
+    if (e == cudaSuccess) e = dalloc(&d.hdr, (size_t)HDR_WORDS);
+    if (e == cudaSuccess) e = dalloc(&d.z, P * LORA_MAX_RANK);
+    if (e == cudaSuccess) e = cudaMemset(d.hdr, 0, HDR_WORDS * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMemset(d.seg_start, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        free_mapping(m);
+        return from_cuda(e);
+    }
+    *out = m;
+    return LORA_OK;
+}
+
+lora_status lora_build_mapping(lora_mapping *m, const int32_t *offsets_dev, const int32_t *ids_dev,
+                               const float *alpha_dev, int T, int P, lora_stream_t stream)
+{
+    if (!m || !offsets_dev || T < 0 || P < 0 || T > m->max_tokens || P > m->max_pairs)
+        return LORA_ERR_INVALID_ARG;
+    if (P > 0 && (!ids_dev || !alpha_dev))
+        return LORA_ERR_INVALID_ARG;
+    cudaError_t e = launch_build_mapping(m->dev, offsets_dev, ids_dev, alpha_dev, T, P, m->capacity, m->max_pairs,
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return from_cuda(e);
+    m->T = T;
+    m->P = P;
+    m->built = true;
+    return LORA_OK;
+}
+
+lora_status lora_delta_apply_path(const void *x_dev, void *y_dev, const lora_pool *pool, const int32_t *ranks_dev,
+                                  const lora_mapping *m, int path, lora_stream_t stream)
+{
+    if (!x_dev || !y_dev || !pool || !m || !m->built || x_dev == y_dev)
+        return LORA_ERR_INVALID_ARG;
+    if (m->capacity != pool->capacity)
+        return LORA_ERR_INVALID_ARG;
+    if (!aligned16(x_dev) || !aligned16(y_dev))
+        return LORA_ERR_INVALID_ARG;
+    if (m->T == 0 || m->P == 0)
+        return LORA_OK;  // no pair: y is already the result
+    if (path == LORA_PATH_AUTO)
+        path = choose_path(m->T, m->P, pool->r_max, pool->d_in, pool->d_out);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (path) {
+    case LORA_PATH_SPLIT:
+        return run_split(x_dev, y_dev, pool, ranks_dev, m, st);
+    default:
+        return LORA_ERR_NOT_SUPPORTED;
+    }
+}
+
+lora_status lora_delta_apply(const void *x_dev, void *y_dev, const lora_pool *pool, const int32_t *ranks_dev,
+                             const lora_mapping *m, lora_stream_t stream)
+{
+    return lora_delta_apply_path(x_dev, y_dev, pool, ranks_dev, m, LORA_PATH_AUTO, stream);
+}
+
+lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_t *offsets_host,
+                                  const int32_t *ids_host, const float *alpha_host, int T, int P,
+                                  const lora_pool *pool, const int32_t *ranks_dev, lora_mapping *m,
+                                  lora_stream_t stream)
+{
+    if (!x_host || !y_host || !offsets_host || !pool || !m || T < 0 || P < 0 || T > m->max_tokens ||
+        P > m->max_pairs || m->capacity != pool->capacity)
+        return LORA_ERR_INVALID_ARG;
+    if (P > 0 && (!ids_host || !alpha_host))
+        return LORA_ERR_INVALID_ARG;
+    cudaError_t e = cudaSuccess;
+    if (!m->sx || m->s_d_in != pool->d_in || m->s_d_out != pool->d_out) {
+        e = cudaDeviceSynchronize();
+        if (m->sx) cudaFree(m->sx);
+        if (m->sy) cudaFree(m->sy);
+        if (m->soff) cudaFree(m->soff);
+        if (m->sids) cudaFree(m->sids);
+        if (m->salpha) cudaFree(m->salpha);
+        m->sx = m->sy = nullptr;
+        m->soff = m->sids = nullptr;
+        m->salpha = nullptr;
+        const size_t mt = (size_t)(m->max_tokens > 0 ? m->max_tokens : 1);
+        if (e == cudaSuccess) e = cudaMalloc(&m->sx, mt * pool->d_in * sizeof(__nv_bfloat16));
+        if (e == cudaSuccess) e = cudaMalloc(&m->sy, mt * pool->d_out * sizeof(__nv_bfloat16));
+        if (e == cudaSuccess) e = dalloc(&m->soff, mt + 1);
+        if (e == cudaSuccess) e = dalloc(&m->sids, (size_t)m->max_pairs);
+        if (e == cudaSuccess) e = dalloc(&m->salpha, (size_t)m->max_pairs);
+        if (e != cudaSuccess)
+            return from_cuda(e);
+        m->s_d_in = pool->d_in;
+        m->s_d_out = pool->d_out;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t xb = (size_t)T * pool->d_in * sizeof(__nv_bfloat16);
+    const size_t yb = (size_t)T * pool->d_out * sizeof(__nv_bfloat16);
+    e = cudaMemcpyAsync(m->soff, offsets_host, (size_t)(T + 1) * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && P > 0)
+        e = cudaMemcpyAsync(m->sids, ids_host, (size_t)P * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && P > 0)
+        e = cudaMemcpyAsync(m->salpha, alpha_host, (size_t)P * sizeof(float), cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && xb)
+        e = cudaMemcpyAsync(m->sx, x_host, xb, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess && yb)
+        e = cudaMemcpyAsync(m->sy, y_host, yb, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess)
+        return from_cuda(e);
+    lora_status s = lora_build_mapping(m, m->soff, m->sids, m->salpha, T, P, stream);
+    if (s != LORA_OK)
+        return s;
+    s = lora_delta_apply(m->sx, m->sy, pool, ranks_dev, m, stream);
+    if (s != LORA_OK)
+        return s;
+    if (yb)
+        e = cudaMemcpyAsync(y_host, m->sy, yb, cudaMemcpyDeviceToHost, st);
+    return from_cuda(e);
+}
+
+lora_status lora_mapping_status(const lora_mapping *m, lora_stream_t stream, int *device_error)
+{
+    if (!m || !device_error)
+        return LORA_ERR_INVALID_ARG;
+    int32_t v = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&v, m->dev.hdr + HDR_STATUS, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    *device_error = v;
+    return from_cuda(e);
+}
+
+lora_status lora_mapping_export(const lora_mapping *m, lora_stream_t stream, int32_t *tok, int32_t *adapter,
+                                float *alpha, int32_t *src, int32_t *pos, int32_t *seg_adapter, int32_t *seg_start,
+                                int32_t *counts)
+{
+    if (!m)
+        return LORA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t hdr[HDR_WORDS];
+    cudaError_t e = cudaMemcpyAsync(hdr, m->dev.hdr, sizeof hdr, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return from_cuda(e);
+    const size_t U = (size_t)hdr[HDR_U], Pv = (size_t)hdr[HDR_PVALID], P = (size_t)(m->built ? m->P : 0);
+    struct {
+        void *dst;
+        const void *src;
+        size_t bytes;
+    } cp[] = {
+        {tok, m->dev.tok, Pv * 4},          {adapter, m->dev.adapter, Pv * 4}, {alpha, m->dev.alpha, Pv * 4},
+        {src, m->dev.src, Pv * 4},          {pos, m->dev.pos, P * 4},          {seg_adapter, m->dev.seg_adapter, U * 4},
+        {seg_start, m->dev.seg_start, (U + 1) * 4},
+    };
+    for (auto &c : cp)
+        if (c.dst && c.bytes && e == cudaSuccess)
+            e = cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (counts) {
+        counts[0] = hdr[HDR_U];
+        counts[1] = hdr[HDR_PVALID];
+        counts[2] = hdr[HDR_STATUS];
+    }
+    return from_cuda(e);
+}
+
+lora_status lora_mapping_destroy(lora_mapping *m)
+{
+    if (!m)
+        return LORA_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    free_mapping(m);
+    return from_cuda(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,70 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/lora.h"
+
+namespace tcl {
+
+// Shrink tile: at most SHRINK_TT pairs (tokens) of one adapter segment and
+// SHRINK_RG retained-rank rows per work unit.
+constexpr int SHRINK_TT = 8;
+constexpr int SHRINK_RG = 4;
+constexpr int SHRINK_DC = 2048;      // d_in elements per pipeline chunk
+constexpr int SHRINK_THREADS = 256;  // one 16-byte vector of each row per thread and chunk
+constexpr int SHRINK_STAGES = 2;
+
+// Expand (RowExpand) tile: EXP_W output columns per CTA, token blocks of up
+// to EXP_TB_MAX tokens, jobs of at most EXP_JP pairs of one segment.
+constexpr int EXP_W = 64;
+constexpr int EXP_TB_MAX = 64;
+constexpr int EXP_JP = 16;
+constexpr int EXP_THREADS = 256;
+constexpr int EXP_MAX_JOBS = 256;
+constexpr int EXP_B_BYTES = 48 * 1024;
+constexpr int EXP_Z_BYTES = 16 * 1024;
+
+constexpr int MAP_THREADS = 1024;
+constexpr int MAP_HIST_BYTES = 192 * 1024;
+
+// Header words of the mapping (device int32).
+enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_WORDS = 8 };
+
+struct PoolDev {
+    const __nv_bfloat16 *At;  // [capacity][r_max][d_in]
+    const __nv_bfloat16 *B;   // [capacity][r_max][d_out]
+    const int32_t *reg_rank;  // [capacity], -1 = unregistered
+    int d_in, d_out, r_max, capacity;
+};
+
+struct MapDev {
+    int32_t *tok, *adapter, *src, *pos;  // [max_pairs]
+    float *alpha;                        // [max_pairs]
+    int32_t *seg_adapter, *seg_start;    // [capacity], [capacity+1]
+    int4 *tile;                          // [max_pairs] shrink tiles {adapter, q0, n, segment}
+    int32_t *tmp_tok;                    // [max_pairs] scratch
+    int32_t *hdr;                        // [HDR_WORDS]
+    float *z;                            // [max_pairs][LORA_MAX_RANK] shrink output
+};
+
+// Launchers (each returns cudaGetLastError()).
+cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const int32_t *ids,
+                                 const float *alpha, int T, int P, int capacity, int max_pairs,
+                                 cudaStream_t st);
+cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int32_t *ranks,
+                          const MapDev &m, int rg, int grid, cudaStream_t st);
+
+// z row stride (floats): r_max rounded up to a multiple of 4 (16-byte rows).
+inline int z_stride(int r_max) { return (r_max + 3) & ~3; }
+cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
+                          const MapDev &m, int T, int tb, bool pdl, cudaStream_t st);
+cudaError_t launch_transpose_bf16(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int rows, int cols,
+                                  cudaStream_t st);
+cudaError_t launch_set_int(int32_t *p, int v, cudaStream_t st);
+
+int sm_count();
+
+}  // namespace tcl

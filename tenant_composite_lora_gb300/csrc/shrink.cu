@@ -1,0 +1,261 @@
+// Shrink: z_q[j] = alpha_q * sum_{d < d_in} x[tok_q, d] * A_{a_q}[d, j]   for j < k_{a_q}
+//
+// LoRAForge summary page, "Approach" (4) and "Developer view": the shrink
+// keeps the retained rank k_m (a rank-aware segmented shrink, CSGMV) so that
+// only the first k rows of the factor are read.  DyMerge-LoRA summary page,
+// "Core idea" (paper Sec. 4.3): one CTA processes the tokens of one adapter
+// together, so the adapter's A is read once for all of them.  The alpha of
+// each pair is folded into z here (the delta is linear in alpha, DyMerge-LoRA
+// page, "Core idea", paper Sec. 3.1 M1).
+//
+// Work unit = (segment tile of <= SHRINK_TT pairs of one adapter, group of <=
+// SHRINK_RG retained rows).  The pool stores A transposed (r_max x d_in), so a
+// unit's rows are contiguous, 16-byte aligned runs that one thread streams
+// into shared memory with bulk (TMA) copies completing on an mbarrier; x rows
+// of the tile's tokens come the same way.  d_in is consumed in chunks of
+// SHRINK_DC through a SHRINK_STAGES-deep ring.  Each thread owns one 16-byte
+// vector of every staged row, accumulates TT x RG partial dot products in
+// fp32, and the CTA reduces them with a warp-shuffle reduce-scatter (32
+// values over 32 lanes in 31 shuffles) and one cross-warp pass.
+//
+// Persistent grid: CTA b takes units b, b + G, b + 2G, ... of the list
+// ordered rowgroup-major, which mixes light and heavy units across CTAs.
+// The kernel calls griddepcontrol.launch_dependents at entry so the expand
+// kernel that follows can start staging B while this one runs.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tcl {
+
+namespace {
+
+constexpr int TT = SHRINK_TT, RG = SHRINK_RG, DC = SHRINK_DC, S = SHRINK_STAGES;
+constexpr int STG = (RG + TT) * DC;  // bf16 elements per stage
+constexpr int MAX_LIST = SHRINK_THREADS;
+static_assert(TT * RG == 32, "one reduced value per lane");
+
+struct ShrinkArgs {
+    const __nv_bfloat16 *x;
+    PoolDev pool;
+    const int32_t *ranks;
+    MapDev m;
+    int rg;  // rows per unit, <= RG
+    int zs;  // z row stride (floats)
+};
+
+__device__ __forceinline__ void unpack8(const uint4 w, float f[8])
+{
+    f[0] = bf16lo(w.x);
+    f[1] = bf16hi(w.x);
+    f[2] = bf16lo(w.y);
+    f[3] = bf16hi(w.y);
+    f[4] = bf16lo(w.z);
+    f[5] = bf16hi(w.z);
+    f[6] = bf16lo(w.w);
+    f[7] = bf16hi(w.w);
+}
+
+__global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
+{
+    extern __shared__ __align__(128) unsigned char smem_raw[];
+    __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
+    __shared__ __align__(8) uint64_t full[S];
+    __shared__ float red[2][8][32];
+    __shared__ int4 s_unit[MAX_LIST];  // {adapter, q0, n, (j0 << 8) | R}
+    __shared__ int s_tok[MAX_LIST][TT];
+    __shared__ int s_wcount[8];
+
+    pdl_launch_dependents();
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int d_in = a.pool.d_in, r_max = a.pool.r_max;
+    int32_t *status = a.m.hdr + HDR_STATUS;
+    const int ntiles = a.m.hdr[HDR_NTILES];
+    const int rgm = (r_max + a.rg - 1) / a.rg;
+    const long long nunits = (long long)ntiles * rgm;
+    const int nch = (d_in + DC - 1) / DC;
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s)
+            mbar_init(&full[s], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    uint32_t g_base = 0;  // chunk sequence number (drives ring slot and parity)
+    int unit_parity = 0;
+    for (long long pass = blockIdx.x; pass < nunits; pass += (long long)gridDim.x * MAX_LIST) {
+        // ---- resolve this pass's units in parallel and compact the live ones
+        const long long u = pass + (long long)tid * gridDim.x;
+        bool live = false;
+        int4 rec = make_int4(0, 0, 0, 0);
+        int toks[TT];
+#pragma unroll
+        for (int i = 0; i < TT; ++i)
+            toks[i] = 0;
+        if (u < nunits) {
+            const int rg = (int)(u / ntiles), tile = (int)(u % ntiles);
+            const int4 t = a.m.tile[tile];  // {adapter, q0, n, segment}
+            const int k = effective_rank(a.pool, a.ranks, t.x);
+            if (k < 0) {
+                if (rg == 0)
+                    atomicOr(status, k == -1 ? LORA_DEV_UNREGISTERED : LORA_DEV_BAD_RANK);
+            } else {
+                const int j0 = rg * a.rg;
+                if (j0 < k) {
+                    live = true;
+                    rec = make_int4(t.x, t.y, t.z, (j0 << 8) | min(a.rg, k - j0));
+#pragma unroll
+                    for (int i = 0; i < TT; ++i)
+                        if (i < t.z)
+                            toks[i] = a.m.tok[t.y + i];
+                }
+            }
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, live);
+        if (lane == 0)
+            s_wcount[warp] = __popc(bal);
+        __syncthreads();
+        int before = 0, L = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            before += (w < warp) ? s_wcount[w] : 0;
+            L += s_wcount[w];
+        }
+        if (live) {
+            const int idx = before + __popc(bal & ((1u << lane) - 1u));
+            s_unit[idx] = rec;
+#pragma unroll
+            for (int i = 0; i < TT; ++i)
+                s_tok[idx][i] = toks[i];
+        }
+        __syncthreads();
+
+        // ---- pipeline over L units x nch chunks
+        const int total = L * nch;
+        auto issue = [&](int c, uint32_t g) {
+            const int e = c / nch, ch = c % nch;
+            const int4 r = s_unit[e];
+            const int n = r.z, R = r.w & 0xff, j0 = r.w >> 8;
+            const int c0 = ch * DC, clen = min(DC, d_in - c0);
+            const uint32_t row_bytes = (uint32_t)clen * 2u;
+            __nv_bfloat16 *dst = stage + (size_t)(g % S) * STG;
+            uint64_t *bar = &full[g % S];
+            mbar_arrive_expect_tx(bar, row_bytes * (uint32_t)(R + n));
+            const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
+            for (int rr = 0; rr < R; ++rr)
+                bulk_g2s(dst + rr * DC, Abase + (size_t)rr * d_in, row_bytes, bar);
+            for (int i = 0; i < n; ++i)
+                bulk_g2s(dst + (RG + i) * DC, a.x + (size_t)s_tok[e][i] * d_in + c0, row_bytes, bar);
+        };
+        if (tid == 0)
+            for (int c = 0; c < total && c < S; ++c)
+                issue(c, g_base + c);
+
+        float acc[TT][RG];
+        for (int c = 0; c < total; ++c) {
+            const uint32_t g = g_base + c;
+            const bool ok = mbar_wait_bounded(&full[g % S], (g / S) & 1u, status);
+            const int e = c / nch, ch = c % nch;
+            const int4 r = s_unit[e];
+            const int n = r.z, R = r.w & 0xff;
+            if (ch == 0) {
+#pragma unroll
+                for (int i = 0; i < TT; ++i)
+#pragma unroll
+                    for (int rr = 0; rr < RG; ++rr)
+                        acc[i][rr] = 0.f;
+            }
+            const int clen = min(DC, d_in - ch * DC);
+            const __nv_bfloat16 *sA = stage + (size_t)(g % S) * STG;
+            if (ok && tid * 8 < clen) {
+                float av[RG][8];
+#pragma unroll
+                for (int rr = 0; rr < RG; ++rr)
+                    if (rr < R)
+                        unpack8(lds128(sA + rr * DC + tid * 8), av[rr]);
+#pragma unroll
+                for (int i = 0; i < TT; ++i) {
+                    if (i < n) {
+                        float xv[8];
+                        unpack8(lds128(sA + (RG + i) * DC + tid * 8), xv);
+#pragma unroll
+                        for (int rr = 0; rr < RG; ++rr) {
+                            if (rr < R) {
+                                float s = acc[i][rr];
+#pragma unroll
+                                for (int v = 0; v < 8; ++v)
+                                    s = fmaf(xv[v], av[rr][v], s);
+                                acc[i][rr] = s;
+                            }
+                        }
+                    }
+                }
+            }
+            const bool last = (ch == nch - 1);
+            if (last) {
+                // reduce-scatter: lane l ends with the warp sum of value l = i * RG + r
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < TT; ++i)
+#pragma unroll
+                    for (int rr = 0; rr < RG; ++rr)
+                        v[i * RG + rr] = acc[i][rr];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) {
+                    const bool upper = (lane & off) != 0;
+#pragma unroll
+                    for (int i = 0; i < off; ++i) {
+                        const float send = upper ? v[i] : v[i + off];
+                        const float keep = upper ? v[i + off] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                red[unit_parity][warp][lane] = v[0];
+            }
+            const int any_bad = __syncthreads_or(!ok);
+            if (any_bad)
+                return;  // a copy never landed: status already records it
+            if (tid == 0 && c + S < total)
+                issue(c + S, g + S);
+            if (last) {
+                if (warp == 0) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        s += red[unit_parity][w][lane];
+                    const int i = lane / RG, rr = lane % RG, j0 = r.w >> 8;
+                    if (i < n && rr < R) {
+                        const int q = r.y + i;
+                        a.m.z[(size_t)q * a.zs + j0 + rr] = a.m.alpha[q] * s;
+                    }
+                }
+                unit_parity ^= 1;
+            }
+        }
+        g_base += (uint32_t)total;
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int32_t *ranks,
+                          const MapDev &m, int rg, int grid, cudaStream_t st)
+{
+    const size_t smem = (size_t)S * STG * sizeof(__nv_bfloat16);
+    static int attr_done = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_done != dev) {
+        cudaError_t e = cudaFuncSetAttribute(k_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_done = dev;
+    }
+    ShrinkArgs a{x, pool, ranks, m, rg, z_stride(pool.r_max)};
+    k_shrink<<<grid, SHRINK_THREADS, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace tcl

@@ -1,0 +1,212 @@
+"""ctypes binding of libtclora.so: the C-ABI entry points under the same names.
+
+Argument marshalling only.  Device arrays are passed as torch CUDA tensors
+(their data_ptr) or raw integer addresses; streams as torch.cuda.Stream, a raw
+cudaStream_t integer, or None for the current torch stream.  Every step of the
+delta runs inside the library's CUDA kernels; nothing here computes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtclora.so")
+
+LORA_OK = 0
+LORA_ERR_INVALID_ARG = 1
+LORA_ERR_OUT_OF_MEMORY = 2
+LORA_ERR_CUDA = 3
+LORA_ERR_BAD_ADAPTER = 4
+LORA_ERR_NOT_SUPPORTED = 5
+
+LORA_DEV_BAD_ID = 1
+LORA_DEV_BAD_OFFSETS = 2
+LORA_DEV_UNREGISTERED = 4
+LORA_DEV_BAD_RANK = 8
+LORA_DEV_TIMEOUT = 16
+
+LORA_PATH_AUTO = 0
+LORA_PATH_SPLIT = 1
+LORA_PATH_FUSED = 2
+LORA_PATH_MMA = 3
+
+LORA_MAX_RANK = 64
+LORA_MAX_CAPACITY = 49152
+
+# every entry point of include/lora.h
+EXPORTS = [
+    "lora_pool_create", "lora_pool_register", "lora_pool_unregister", "lora_pool_destroy",
+    "lora_mapping_create", "lora_build_mapping", "lora_delta_apply", "lora_delta_apply_path",
+    "lora_dispatch_choose", "lora_delta_apply_host", "lora_mapping_status", "lora_mapping_export",
+    "lora_mapping_destroy", "lora_status_string", "lora_version",
+]
+
+
+class LoraError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Loads libtclora.so; raises if it has not been built (there is no
+    fallback path)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m tenant_composite_lora_gb300.build` "
+            "(there is no CPU or Python fallback)")
+    lib = ctypes.CDLL(path)
+    V, I, PP = ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(ctypes.c_void_p)
+    sig = {
+        "lora_pool_create": ([I, I, I, I, PP], I),
+        "lora_pool_register": ([V, I, V, V, I, V], I),
+        "lora_pool_unregister": ([V, I, V], I),
+        "lora_pool_destroy": ([V], I),
+        "lora_mapping_create": ([I, I, I, PP], I),
+        "lora_build_mapping": ([V, V, V, V, I, I, V], I),
+        "lora_delta_apply": ([V, V, V, V, V, V], I),
+        "lora_delta_apply_path": ([V, V, V, V, V, I, V], I),
+        "lora_dispatch_choose": ([I, I, I, I, I], I),
+        "lora_delta_apply_host": ([V, V, V, V, V, I, I, V, V, V, V], I),
+        "lora_mapping_status": ([V, V, ctypes.POINTER(ctypes.c_int)], I),
+        "lora_mapping_export": ([V, V, V, V, V, V, V, V, V, V], I),
+        "lora_mapping_destroy": ([V], I),
+        "lora_status_string": ([I], ctypes.c_char_p),
+        "lora_version": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def status_string(s: int) -> str:
+    try:
+        return load().lora_status_string(int(s)).decode()
+    except Exception:  # pragma: no cover
+        return f"status {s}"
+
+
+def _check(fn: str, s: int):
+    if s != LORA_OK:
+        raise LoraError(fn, s)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+# ------------------------------------------------------------------ pools
+def lora_pool_create(d_in: int, d_out: int, r_max: int, capacity: int) -> int:
+    out = ctypes.c_void_p()
+    _check("lora_pool_create", load().lora_pool_create(d_in, d_out, r_max, capacity, ctypes.byref(out)))
+    return out.value
+
+
+def lora_pool_register(pool: int, slot: int, A, B, k: int, stream=None):
+    _check("lora_pool_register", load().lora_pool_register(pool, slot, _ptr(A), _ptr(B), k, _stream(stream)))
+
+
+def lora_pool_unregister(pool: int, slot: int, stream=None):
+    _check("lora_pool_unregister", load().lora_pool_unregister(pool, slot, _stream(stream)))
+
+
+def lora_pool_destroy(pool: int):
+    _check("lora_pool_destroy", load().lora_pool_destroy(pool))
+
+
+# ------------------------------------------------------------------ mappings
+def lora_mapping_create(max_tokens: int, max_pairs: int, capacity: int) -> int:
+    out = ctypes.c_void_p()
+    _check("lora_mapping_create",
+           load().lora_mapping_create(max_tokens, max_pairs, capacity, ctypes.byref(out)))
+    return out.value
+
+
+def lora_build_mapping(m: int, offsets, ids, alpha, T: int, P: int, stream=None):
+    _check("lora_build_mapping",
+           load().lora_build_mapping(m, _ptr(offsets), _ptr(ids), _ptr(alpha), T, P, _stream(stream)))
+
+
+def lora_delta_apply(x, y, pool: int, ranks, m: int, stream=None):
+    _check("lora_delta_apply",
+           load().lora_delta_apply(_ptr(x), _ptr(y), pool, _ptr(ranks), m, _stream(stream)))
+
+
+def lora_delta_apply_path(x, y, pool: int, ranks, m: int, path: int, stream=None):
+    _check("lora_delta_apply_path",
+           load().lora_delta_apply_path(_ptr(x), _ptr(y), pool, _ptr(ranks), m, path, _stream(stream)))
+
+
+def lora_dispatch_choose(T: int, P: int, r_max: int, d_in: int, d_out: int) -> int:
+    return int(load().lora_dispatch_choose(T, P, r_max, d_in, d_out))
+
+
+def lora_delta_apply_host(x_host, y_host, offsets_host, ids_host, alpha_host, T: int, P: int,
+                          pool: int, ranks, m: int, stream=None):
+    _check("lora_delta_apply_host",
+           load().lora_delta_apply_host(_ptr(x_host), _ptr(y_host), _ptr(offsets_host), _ptr(ids_host),
+                                        _ptr(alpha_host), T, P, pool, _ptr(ranks), m, _stream(stream)))
+
+
+def lora_mapping_status(m: int, stream=None) -> int:
+    v = ctypes.c_int()
+    _check("lora_mapping_status", load().lora_mapping_status(m, _stream(stream), ctypes.byref(v)))
+    return int(v.value)
+
+
+def lora_mapping_export(m: int, P: int, capacity: int, stream=None) -> dict:
+    """Copies the mapping to host numpy arrays (for checking)."""
+    n = max(P, 1)
+    tok = np.zeros(n, np.int32)
+    adapter = np.zeros(n, np.int32)
+    alpha = np.zeros(n, np.float32)
+    src = np.zeros(n, np.int32)
+    pos = np.zeros(n, np.int32)
+    nseg = max(min(P, capacity), 1)
+    seg_adapter = np.zeros(nseg, np.int32)
+    seg_start = np.zeros(nseg + 1, np.int32)
+    counts = np.zeros(3, np.int32)
+    _check("lora_mapping_export",
+           load().lora_mapping_export(m, _stream(stream), tok.ctypes.data, adapter.ctypes.data,
+                                      alpha.ctypes.data, src.ctypes.data, pos.ctypes.data,
+                                      seg_adapter.ctypes.data, seg_start.ctypes.data, counts.ctypes.data))
+    U, Pv = int(counts[0]), int(counts[1])
+    return {"tok": tok[:Pv], "adapter": adapter[:Pv], "alpha": alpha[:Pv], "src": src[:Pv],
+            "pos": pos[:P], "seg_adapter": seg_adapter[:U], "seg_start": seg_start[:U + 1],
+            "U": U, "P_valid": Pv, "status": int(counts[2])}
+
+
+def lora_mapping_destroy(m: int):
+    _check("lora_mapping_destroy", load().lora_mapping_destroy(m))
+
+
+def lora_version() -> str:
+    return load().lora_version().decode()

@@ -1,0 +1,299 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Mapping: bit-exact (tuples, alpha bits, inverse permutation, segments).
+Delta: |y - y_ref| <= 1e-2 + 1e-2 |y_ref| per element (the stated gate), and
+on runs with y_in = 0 the delta-only bound |y - ref| <= 2^-7 |ref| +
+1e-3 rms(ref), which one bf16 rounding plus fp32 summation noise satisfy and a
+wrong or missing term does not (|delta| is far below the bf16 spacing of y_in).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from workloads import bf16_bits_to_f32
+from workloads.device import DeviceWorkload, bf16_tensor, bf16_to_numpy_bits
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_and_stream():
+    from tenant_composite_lora_gb300 import build
+    build.build()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        yield s
+    torch.cuda.synchronize()
+
+
+def stated_gate(y_bits, yref_bits):
+    y = bf16_bits_to_f32(y_bits).astype(np.float64)
+    r = bf16_bits_to_f32(yref_bits).astype(np.float64)
+    bad = np.abs(y - r) > 1e-2 + 1e-2 * np.abs(r)
+    assert not bad.any(), f"{bad.sum()} elements outside the stated tolerance"
+
+
+def delta_gate(y_bits, acc):
+    y = bf16_bits_to_f32(y_bits).astype(np.float64)
+    rms = float(np.sqrt(np.mean(acc ** 2))) if acc.size else 0.0
+    err = np.abs(y - acc)
+    lim = 2.0 ** -7 * np.abs(acc) + 1e-3 * rms
+    bad = err > lim
+    assert not bad.any(), (f"{bad.sum()} / {acc.size} elements outside the delta bound; "
+                           f"worst {float((err - lim).max()):.3g}, rms {rms:.3g}")
+    assert rms > 0
+
+
+def run_gpu(wl, ranks=None, path=0, y_in=None):
+    dw = DeviceWorkload(wl)
+    try:
+        y = dw.y0.clone() if y_in is None else bf16_tensor(y_in)
+        r = None if ranks is None else torch.from_numpy(np.asarray(ranks, np.int32)).cuda()
+        dw.apply(y=y, ranks=r, path=path)
+        torch.cuda.synchronize()
+        st = dw.mapping.status()
+        return bf16_to_numpy_bits(y), st
+    finally:
+        dw.close()
+
+
+# ---------------------------------------------------------------- mapping
+def compare_mapping(got, ref):
+    assert got["U"] == ref["U"] and got["P_valid"] == ref["P_valid"]
+    for k in ("tok", "adapter", "src", "pos", "seg_adapter", "seg_start"):
+        np.testing.assert_array_equal(got[k], ref[k], err_msg=k)
+    assert got["alpha"].tobytes() == ref["alpha"].tobytes()
+    assert got["status"] == ref["status"]
+
+
+MAP_CASES = ["tiny", "distinct", "zipf", "prefill", "sweep1", "sweep8", "sweep64", "sweep256"]
+
+
+@pytest.mark.parametrize("name", MAP_CASES)
+def test_mapping_bit_exact(name):
+    wl = W.make(name)
+    dw = DeviceWorkload(wl)
+    try:
+        got = dw.mapping.export()
+    finally:
+        dw.close()
+    compare_mapping(got, oracle.build_mapping(wl.offsets, wl.ids, wl.alpha, capacity=wl.capacity))
+
+
+def _map_raw(offsets, ids, alpha, cap):
+    import tenant_composite_lora_gb300 as tcl
+    m = tcl.LoraMapping(max(len(offsets) - 1, 1), max(len(ids), 1), cap)
+    try:
+        m.build(torch.from_numpy(np.asarray(offsets, np.int32)).cuda(),
+                torch.from_numpy(np.asarray(ids, np.int32)).cuda(),
+                torch.from_numpy(np.asarray(alpha, np.float32)).cuda())
+        return m.export()
+    finally:
+        m.close()
+
+
+def test_mapping_invalid_ids_and_empty_tokens():
+    rng = np.random.default_rng(11)
+    cap = 37
+    counts = rng.integers(0, 5, size=300)
+    offsets = np.zeros(301, np.int32)
+    offsets[1:] = np.cumsum(counts)
+    ids = rng.integers(-3, cap + 3, size=int(counts.sum())).astype(np.int32)
+    alpha = rng.standard_normal(ids.size).astype(np.float32)
+    compare_mapping(_map_raw(offsets, ids, alpha, cap), oracle.build_mapping(offsets, ids, alpha, capacity=cap))
+
+
+def test_mapping_bad_offsets_and_degenerate():
+    for offsets, ids in (([0, 2, 1, 3], [0, 1, 2]), ([1, 2, 3], [0, 1, 2]), ([0, 1, 2], [0, 1, 2])):
+        ref = oracle.build_mapping(np.array(offsets, np.int32), np.array(ids, np.int32),
+                                   np.ones(len(ids), np.float32), capacity=4)
+        got = _map_raw(offsets, ids, np.ones(len(ids)), 4)
+        compare_mapping(got, ref)
+        assert got["status"] & 2
+    # no pairs at all, and one token with every adapter of a large pool
+    compare_mapping(_map_raw([0, 0, 0], [], [], 5), oracle.build_mapping(
+        np.zeros(3, np.int32), np.zeros(0, np.int32), np.zeros(0, np.float32), capacity=5))
+    cap = 3000
+    ids = np.random.default_rng(3).permutation(cap).astype(np.int32)
+    offsets = np.array([0, cap], np.int32)
+    compare_mapping(_map_raw(offsets, ids, np.ones(cap), cap),
+                    oracle.build_mapping(offsets, ids, np.ones(cap, np.float32), capacity=cap))
+
+
+# ---------------------------------------------------------------- delta, element-wise
+APPLY_CASES = ["tiny", "distinct", "zipf", "sweep1", "sweep8", "sweep64", "sweep256"]
+
+
+@pytest.mark.parametrize("name", APPLY_CASES)
+def test_apply_matches_oracle(name):
+    wl = W.make(name)
+    y, st = run_gpu(wl)
+    yref, _, ost = oracle.apply_workload(wl, threads=0)
+    assert st == ost == 0
+    stated_gate(y, yref)
+
+
+@pytest.mark.parametrize("name", APPLY_CASES + ["prefill_small"])
+def test_apply_delta_only(name):
+    wl = W.sparse_prefill(n_requests=3, y_zero=True) if name == "prefill_small" else W.make(name, y_zero=True)
+    y, st = run_gpu(wl)
+    _, acc, ost = oracle.apply_workload(wl, threads=0)
+    assert st == ost == 0
+    delta_gate(y, acc)
+
+
+def test_prefill_full_size_sampled():
+    """The full sparse-prefill batch in the benchmark's launch configuration;
+    the oracle checks sampled tokens (first/last of the batch, request
+    boundaries, random)."""
+    wl = W.sparse_prefill(y_zero=True)
+    y, st = run_gpu(wl)
+    assert st == 0
+    rng = np.random.default_rng(0)
+    toks = sorted(set([0, 1, wl.T - 1, wl.T // 2] + list(rng.choice(wl.T, 40, replace=False))))
+    _, acc, ost = oracle.apply_tokens(wl, toks)
+    delta_gate(y[toks], acc)
+    assert np.isfinite(bf16_bits_to_f32(y)).all()
+
+
+# ---------------------------------------------------------------- contracts
+def test_garbage_padding_is_inert():
+    zero = W.rank_sweep(64)
+    garb = W.rank_sweep(64, garbage_padding=True)
+    y0, _ = run_gpu(zero)
+    y1, _ = run_gpu(garb)
+    np.testing.assert_array_equal(y0, y1)
+
+
+def test_rank_override_and_bad_rank():
+    wl = W.rank_sweep(64, y_zero=True)
+    rng = np.random.default_rng(5)
+    ranks = np.minimum(wl.ranks, rng.integers(0, 65, size=wl.capacity)).astype(np.int32)
+    y, st = run_gpu(wl, ranks=ranks)
+    _, acc, _ = oracle.apply_workload(wl, ranks=ranks)
+    assert st == 0
+    delta_gate(y, acc)
+    bad = ranks.copy()
+    victim = int(wl.ids[0])
+    bad[victim] = wl.r_max + 5
+    y, st = run_gpu(wl, ranks=bad)
+    assert st & 8
+    ok = bad.copy()
+    ok[victim] = 0
+    _, acc, _ = oracle.apply_workload(wl, ranks=ok)
+    delta_gate(y, acc)
+
+
+def test_unregistered_slot():
+    wl = W.zipf_decode(y_zero=True)
+    victim = int(wl.ids[1])
+    reg = wl.ranks.copy()
+    reg[victim] = -1
+    dw = DeviceWorkload(wl, register_ranks=reg)
+    try:
+        y = dw.apply(y=torch.zeros_like(dw.y0))
+        st = dw.mapping.status()
+    finally:
+        dw.close()
+    assert st & 4
+    _, acc, ost = oracle.apply_workload(wl, ranks=reg)
+    assert ost & 4
+    delta_gate(bf16_to_numpy_bits(y), acc)
+
+
+def test_deterministic():
+    wl = W.rank_sweep(256)
+    dw = DeviceWorkload(wl)
+    try:
+        a = bf16_to_numpy_bits(dw.apply())
+        b = bf16_to_numpy_bits(dw.apply())
+    finally:
+        dw.close()
+    np.testing.assert_array_equal(a, b)
+
+
+def test_noops():
+    wl = W.tiny()
+    wl.alpha[:] = 0
+    y, _ = run_gpu(wl)
+    np.testing.assert_array_equal(bf16_bits_to_f32(y), bf16_bits_to_f32(wl.y))
+    wl = W.tiny()
+    y, _ = run_gpu(wl, ranks=np.zeros(wl.capacity, np.int32))
+    np.testing.assert_array_equal(bf16_bits_to_f32(y), bf16_bits_to_f32(wl.y))
+
+
+def test_order_invariance():
+    wl = W.zipf_decode(y_zero=True)
+    y0, _ = run_gpu(wl)
+    rng = np.random.default_rng(9)
+    for t in range(wl.T):
+        a, b = wl.offsets[t], wl.offsets[t + 1]
+        perm = rng.permutation(b - a) + a
+        wl.ids[a:b] = wl.ids[perm]
+        wl.alpha[a:b] = wl.alpha[perm]
+    y1, _ = run_gpu(wl)
+    _, acc, _ = oracle.apply_workload(wl)
+    delta_gate(y0, acc)
+    delta_gate(y1, acc)
+
+
+def test_host_entry_point_matches_device_path():
+    import tenant_composite_lora_gb300 as tcl
+    wl = W.zipf_decode()
+    dw = DeviceWorkload(wl)
+    try:
+        ref = bf16_to_numpy_bits(dw.apply())
+        y_host = torch.from_numpy(wl.y.view(np.int16).copy()).pin_memory()
+        x_host = torch.from_numpy(wl.x.view(np.int16).copy()).pin_memory()
+        off = torch.from_numpy(wl.offsets).pin_memory()
+        ids = torch.from_numpy(wl.ids).pin_memory()
+        al = torch.from_numpy(wl.alpha).pin_memory()
+        tcl.lora_delta_apply_host(x_host, y_host, off, ids, al, wl.T, wl.P, dw.pool.handle, None,
+                                  dw.mapping.handle)
+        torch.cuda.current_stream().synchronize()
+        got = y_host.numpy().view(np.uint16)
+    finally:
+        dw.close()
+    np.testing.assert_array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- edge shapes
+def _custom(rng, d_in, d_out, r, cap, lists, ranks=None):
+    alpha_lists = [list(rng.random(len(l)).astype(np.float32)) for l in lists]
+    return W.make_custom(rng, d_in=d_in, d_out=d_out, r_max=r, capacity=cap, id_lists=lists,
+                         alpha_lists=alpha_lists, ranks=ranks, y_sigma=0.0)
+
+
+def test_big_segments_and_many_pairs_per_token():
+    rng = np.random.default_rng(21)
+    lists = [[0, 1, 2] for _ in range(300)] + [list(rng.permutation(64)[:40])] + [[]] + [[5]]
+    wl = _custom(rng, 128, 192, 16, 64, lists)
+    y, st = run_gpu(wl)
+    _, acc, _ = oracle.apply_workload(wl)
+    assert st == 0
+    delta_gate(y, acc)
+
+
+@pytest.mark.parametrize("d_in,d_out,r,k", [(64, 128, 1, 1), (6208, 64, 5, 3), (14336, 4096, 8, 8),
+                                            (256, 256, 64, 64), (192, 320, 13, 7)])
+def test_shapes(d_in, d_out, r, k):
+    rng = np.random.default_rng(d_in + d_out)
+    cap = 6
+    lists = [list(rng.permutation(cap)[:rng.integers(1, 4)]) for _ in range(9)]
+    ranks = np.full(cap, k, np.int32)
+    ranks[0] = 0
+    wl = _custom(rng, d_in, d_out, r, cap, lists, ranks)
+    y, st = run_gpu(wl)
+    _, acc, _ = oracle.apply_workload(wl)
+    delta_gate(y, acc)
+
+
+def test_no_pairs_leaves_y():
+    rng = np.random.default_rng(2)
+    wl = W.make_custom(rng, d_in=64, d_out=64, r_max=4, capacity=2, id_lists=[[], []],
+                       alpha_lists=[[], []])
+    y, st = run_gpu(wl)
+    np.testing.assert_array_equal(y, wl.y)
