@@ -118,7 +118,7 @@ cudaError_t dalloc(T **p, size_t count)
 void free_mapping(lora_mapping *m)
 {
     MapDev &d = m->dev;
-    void *ptrs[] = {d.tok, d.adapter, d.src, d.pos, d.alpha, d.seg_adapter, d.seg_start, d.tile,
+    void *ptrs[] = {d.tok, d.adapter, d.src, d.pos, d.alpha, d.seg_adapter, d.seg_start, d.tile, d.tile_tok,
                     d.tmp_tok, d.hdr, d.z, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
@@ -138,15 +138,16 @@ int choose_path(int T, int P, int r_max, int d_in, int d_out)
     return LORA_PATH_SPLIT;
 }
 
-// Token block of the expand kernel: the largest of 64, 32, 16, 8 that still
-// gives at least one CTA per SM.
-int choose_tb(int T, int d_out)
+// Expand tile: 64 columns when that alone gives a CTA per SM, else 32; then
+// the largest token block of 64, 32, 16, 8 that still gives a CTA per SM.
+void choose_expand_tile(int T, int d_out, int &tb, int &w)
 {
-    const int n_ct = d_out / EXP_W, sms = sm_count();
-    int tb = EXP_TB_MAX;
+    const int sms = sm_count();
+    w = (d_out / 64 >= sms) ? 64 : 32;
+    const int n_ct = d_out / w;
+    tb = EXP_TB_MAX;
     while (tb > 8 && (long long)n_ct * ((T + tb - 1) / tb) < sms)
         tb >>= 1;
-    return tb;
 }
 
 lora_status run_split(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
@@ -154,11 +155,13 @@ lora_status run_split(const void *x, void *y, const lora_pool *pool, const int32
 {
     const PoolDev pd = pool_dev(pool);
     const int grid = sm_count();
-    cudaError_t e = launch_shrink(static_cast<const __nv_bfloat16 *>(x), pd, ranks, m->dev, SHRINK_RG, grid, st);
+    cudaError_t e =
+        launch_shrink(static_cast<const __nv_bfloat16 *>(x), pd, ranks, m->dev, m->P, SHRINK_RG, grid, st);
     if (e != cudaSuccess)
         return from_cuda(e);
-    e = launch_expand(static_cast<__nv_bfloat16 *>(y), pd, ranks, m->dev, m->T, choose_tb(m->T, pool->d_out),
-                      /*pdl=*/true, st);
+    int tb = 0, w = 0;
+    choose_expand_tile(m->T, pool->d_out, tb, w);
+    e = launch_expand(static_cast<__nv_bfloat16 *>(y), pd, ranks, m->dev, m->T, m->P, tb, w, /*pdl=*/true, st);
     return from_cuda(e);
 }
 
@@ -302,6 +305,7 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.seg_adapter, (size_t)capacity);
     if (e == cudaSuccess) e = dalloc(&d.seg_start, (size_t)capacity + 1);
     if (e == cudaSuccess) e = dalloc(&d.tile, P);
+    if (e == cudaSuccess) e = dalloc(&d.tile_tok, P * SHRINK_TT);
     if (e == cudaSuccess) e = dalloc(&d.tmp_tok, P);
     if (e == cudaSuccess) e = dalloc(&d.hdr, (size_t)HDR_WORDS);
     if (e == cudaSuccess) e = dalloc(&d.z, P * LORA_MAX_RANK);

@@ -6,8 +6,8 @@
 // LoRA summary page, "Core idea" (paper Sec. 4.3): pairs are walked in adapter
 // order, so each adapter's B tile is staged once for all of its tokens.
 //
-// CTA = (token block [t0, t0 + tb), blockIdx.x) x (EXP_W output columns,
-// blockIdx.y).  The CTA owns
+// CTA = (token block [t0, t0 + tb), blockIdx.x) x (32 or 64 output
+// columns, blockIdx.y).  The CTA owns
 // its y tile outright: every pair of every token of the block is summed into
 // an fp32 accumulator tile in shared memory, in a fixed order (segment
 // ascending, then pair order), and the tile is rounded once to bf16 and
@@ -18,7 +18,9 @@
 // into jobs of <= EXP_JP pairs; a window of jobs is staged with 16-byte
 // cp.async copies: the k retained B rows x EXP_W columns of each job, the
 // jobs' z rows, the tokens.  Warp w owns the block tokens with
-// (t - t0) % 8 == w; lane l owns columns 2l and 2l + 1.
+// (t - t0) % 8 == w; each lane owns one or two columns.  The segment list,
+// the header and a shared-memory table of retained ranks are read at entry in
+// one round trip; a decode batch (T <= token block) needs no search.
 //
 // Launched with programmatic dependent launch after the shrink kernel: the
 // first window's B tiles and the y tile (neither written by the shrink) are
@@ -32,11 +34,12 @@ namespace tcl {
 
 namespace {
 
-constexpr int W = EXP_W, NWARP = EXP_THREADS / 32;
+constexpr int NWARP = EXP_THREADS / 32;
+constexpr int WMAX = EXP_W;
 constexpr int B_ELEMS = EXP_B_BYTES / 2;
 constexpr int Z_FLOATS = EXP_Z_BYTES / 4;
 constexpr int WIN_PAIRS = 1024;
-static_assert(W == 64 && NWARP == 8, "lane owns two columns, warp owns tokens mod 8");
+static_assert(NWARP == 8, "warp owns tokens mod 8");
 
 struct ExpandArgs {
     __nv_bfloat16 *y;
@@ -44,16 +47,19 @@ struct ExpandArgs {
     const int32_t *ranks;
     MapDev m;
     int T, tb, zs;
+    int seg_bound;  // host-known bound on the number of segments
+    int use_tab;    // ranks staged in shared memory
 };
 
 struct Smem {
-    float acc[EXP_TB_MAX * W];
-    __nv_bfloat16 yin[EXP_TB_MAX * W];
+    float acc[EXP_TB_MAX * WMAX];
+    __nv_bfloat16 yin[EXP_TB_MAX * WMAX];
     __nv_bfloat16 B[B_ELEMS];
     float Z[Z_FLOATS];
     int tok[WIN_PAIRS];
     int4 jobA[EXP_MAX_JOBS];  // {adapter, q, len, k}
     int4 jobB[EXP_MAX_JOBS];  // {B offset (elements), Z offset (floats), tok offset, kp}
+    int rank_tab[RANK_TAB_MAX];
 };
 
 __device__ __forceinline__ int lower_bound_tok(const int32_t *tok, int lo, int hi, int v)
@@ -69,7 +75,7 @@ __device__ __forceinline__ int lower_bound_tok(const int32_t *tok, int lo, int h
 }
 
 // Block-wide exclusive scan of an int4 over EXP_THREADS threads.
-__device__ int4 block_scan4(int4 v, int4 &total, int4 *sh /* [NWARP + 1] */)
+__device__ int4 block_scan4(int4 v, int4 &total, int4 *sh /* [NWARP] */)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int4 inc = v;
@@ -111,8 +117,12 @@ __device__ int4 block_scan4(int4 v, int4 &total, int4 *sh /* [NWARP + 1] */)
                      before.w + inc.w - v.w);
 }
 
+// W output columns per CTA: 64 (lane owns 2 columns) or 32 (lane owns 1).
+template <int W>
 __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
 {
+    static_assert(W == 32 || W == 64, "tile width");
+    constexpr int VPR = W / 8;  // 16-byte vectors per tile row
     extern __shared__ __align__(128) unsigned char smem_raw[];
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
     __shared__ int4 s_scan[NWARP];
@@ -122,17 +132,21 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
     const int d_out = a.pool.d_out, r_max = a.pool.r_max;
     const int c0 = blockIdx.y * W;
     const int t0 = blockIdx.x * a.tb, t1 = min(a.T, t0 + a.tb), nt = t1 - t0;
-    const int U = a.m.hdr[HDR_U];
     const bool full_range = (t0 == 0 && t1 >= a.T);
 
-    // y tile and accumulator
-    for (int i = tid; i < nt * (W / 8); i += EXP_THREADS) {
-        const int t = i >> 3, v = i & 7;
+    // y tile (not written by the shrink: legal before the dependency wait)
+    for (int i = tid; i < nt * VPR; i += EXP_THREADS) {
+        const int t = i / VPR, v = i % VPR;
         cp_async16(&sm.yin[t * W + v * 8], a.y + (size_t)(t0 + t) * d_out + c0 + v * 8);
     }
     cp_async_commit();
+    if (a.use_tab)
+        for (int i = tid; i < a.pool.capacity; i += EXP_THREADS)
+            sm.rank_tab[i] = effective_rank(a.pool, a.ranks, i);
     for (int i = tid; i < nt * W; i += EXP_THREADS)
         sm.acc[i] = 0.f;
+    const int U = min(a.m.hdr[HDR_U], a.seg_bound);
+    __syncthreads();
 
     bool waited = false;
     int s_next = 0, piece_next = 0;
@@ -143,7 +157,7 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
         if (s < U) {
             adapter = a.m.seg_adapter[s];
             const int sa = a.m.seg_start[s], sb = a.m.seg_start[s + 1];
-            k = effective_rank(a.pool, a.ranks, adapter);
+            k = a.use_tab ? sm.rank_tab[adapter] : effective_rank(a.pool, a.ranks, adapter);
             if (k < 0)
                 k = 0;
             if (k > 0) {
@@ -169,7 +183,7 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
             s_cur_p = 0;
         }
         int4 total;
-        const int4 ex = block_scan4(mine, total, s_scan);  // also orders the s_* writes above
+        const int4 ex = block_scan4(mine, total, s_scan);  // its barriers order the s_* writes above
         {
             int pairs_before = 0;
             for (int pi = 0; pi < np; ++pi) {
@@ -208,8 +222,8 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
             const int4 ja = sm.jobA[j];
             const int bo = sm.jobB[j].x;
             const __nv_bfloat16 *src = a.pool.B + (size_t)ja.x * r_max * d_out + c0;
-            for (int i = lane; i < ja.w * (W / 8); i += 32) {
-                const int r = i >> 3, v = i & 7;
+            for (int i = lane; i < ja.w * VPR; i += 32) {
+                const int r = i / VPR, v = i % VPR;
                 cp_async16(&sm.B[bo + r * W + v * 8], src + (size_t)r * d_out + v * 8);
             }
         }
@@ -229,27 +243,35 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
         cp_async_wait_all();
         __syncthreads();
 
-        // ---- accumulate: warp owns tokens (t - t0) % 8 == warp, lane owns 2 columns
+        // ---- accumulate: warp owns tokens (t - t0) % 8 == warp, lane owns W/32 columns
         for (int j = 0; j < njobs; ++j) {
             const int4 ja = sm.jobA[j], jb = sm.jobB[j];
-            const uint32_t *brow = reinterpret_cast<const uint32_t *>(&sm.B[jb.x]) + lane;
             for (int i = 0; i < ja.z; ++i) {
                 const int t = sm.tok[jb.z + i] - t0;
                 if ((t & (NWARP - 1)) != warp)
                     continue;
                 const float *zr = &sm.Z[jb.y + i * jb.w];
-                float d0 = 0.f, d1 = 0.f;
-                for (int jj = 0; jj < ja.w; ++jj) {
-                    const uint32_t b = brow[jj * (W / 2)];
-                    const float zz = zr[jj];
-                    d0 = fmaf(zz, bf16lo(b), d0);
-                    d1 = fmaf(zz, bf16hi(b), d1);
+                if (W == 64) {
+                    const uint32_t *brow = reinterpret_cast<const uint32_t *>(&sm.B[jb.x]) + lane;
+                    float d0 = 0.f, d1 = 0.f;
+                    for (int jj = 0; jj < ja.w; ++jj) {
+                        const uint32_t b = brow[jj * (W / 2)];
+                        const float zz = zr[jj];
+                        d0 = fmaf(zz, bf16lo(b), d0);
+                        d1 = fmaf(zz, bf16hi(b), d1);
+                    }
+                    float2 *ap = reinterpret_cast<float2 *>(&sm.acc[t * W]) + lane;
+                    float2 cur = *ap;
+                    cur.x += d0;
+                    cur.y += d1;
+                    *ap = cur;
+                } else {
+                    const unsigned short *brow = reinterpret_cast<const unsigned short *>(&sm.B[jb.x]) + lane;
+                    float d0 = 0.f;
+                    for (int jj = 0; jj < ja.w; ++jj)
+                        d0 = fmaf(zr[jj], __uint_as_float((uint32_t)brow[jj * W] << 16), d0);
+                    sm.acc[t * W + lane] += d0;
                 }
-                float2 *ap = reinterpret_cast<float2 *>(&sm.acc[t * W]) + lane;
-                float2 cur = *ap;
-                cur.x += d0;
-                cur.y += d1;
-                *ap = cur;
             }
         }
         __syncthreads();
@@ -261,8 +283,8 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
     __syncthreads();
 
     // ---- y = bf16(y_in + acc), one rounding
-    for (int i = tid; i < nt * (W / 8); i += EXP_THREADS) {
-        const int t = i >> 3, v = i & 7;
+    for (int i = tid; i < nt * VPR; i += EXP_THREADS) {
+        const int t = i / VPR, v = i % VPR;
         const uint4 yi = *reinterpret_cast<const uint4 *>(&sm.yin[t * W + v * 8]);
         const float *ac = &sm.acc[t * W + v * 8];
         const uint32_t w[4] = {yi.x, yi.y, yi.z, yi.w};
@@ -280,21 +302,24 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
 }  // namespace
 
 cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks, const MapDev &m, int T,
-                          int tb, bool pdl, cudaStream_t st)
+                          int P, int tb, int w, bool pdl, cudaStream_t st)
 {
     const size_t smem = sizeof(Smem);
     static int attr_done = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_expand, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(k_expand<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_expand<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
             return e;
         attr_done = dev;
     }
-    ExpandArgs a{y, pool, ranks, m, T, tb, z_stride(pool.r_max)};
+    const int seg_bound = P < pool.capacity ? P : pool.capacity;
+    ExpandArgs a{y, pool, ranks, m, T, tb, z_stride(pool.r_max), seg_bound, pool.capacity <= RANK_TAB_MAX ? 1 : 0};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((T + tb - 1) / tb, pool.d_out / W, 1);
+    cfg.gridDim = dim3((T + tb - 1) / tb, pool.d_out / w, 1);
     cfg.blockDim = dim3(EXP_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -303,7 +328,9 @@ cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_expand, a);
+    if (w == 32)
+        return cudaLaunchKernelEx(&cfg, k_expand<32>, a);
+    return cudaLaunchKernelEx(&cfg, k_expand<64>, a);
 }
 
 }  // namespace tcl

@@ -13,9 +13,10 @@ namespace tcl {
 // SHRINK_RG retained-rank rows per work unit.
 constexpr int SHRINK_TT = 8;
 constexpr int SHRINK_RG = 4;
-constexpr int SHRINK_DC = 2048;      // d_in elements per pipeline chunk
-constexpr int SHRINK_THREADS = 256;  // one 16-byte vector of each row per thread and chunk
-constexpr int SHRINK_STAGES = 2;
+constexpr int SHRINK_DC = 2048;      // d_in elements per pipeline entry
+constexpr int SHRINK_THREADS = 256;  // one 16-byte vector of each row per thread and entry
+constexpr int SHRINK_RING_BYTES = 96 * 1024;
+constexpr int SHRINK_MAX_INFLIGHT = 8;
 
 // Expand (RowExpand) tile: EXP_W output columns per CTA, token blocks of up
 // to EXP_TB_MAX tokens, jobs of at most EXP_JP pairs of one segment.
@@ -24,11 +25,15 @@ constexpr int EXP_TB_MAX = 64;
 constexpr int EXP_JP = 16;
 constexpr int EXP_THREADS = 256;
 constexpr int EXP_MAX_JOBS = 256;
-constexpr int EXP_B_BYTES = 48 * 1024;
+constexpr int EXP_B_BYTES = 40 * 1024;
 constexpr int EXP_Z_BYTES = 16 * 1024;
 
 constexpr int MAP_THREADS = 1024;
-constexpr int MAP_HIST_BYTES = 192 * 1024;
+constexpr int MAP_SMEM_BYTES = 200 * 1024;
+
+// Ranks of pools up to this capacity are staged in shared memory by the
+// apply kernels (one coalesced read instead of a dependent lookup).
+constexpr int RANK_TAB_MAX = 2048;
 
 // Header words of the mapping (device int32).
 enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_WORDS = 8 };
@@ -45,6 +50,7 @@ struct MapDev {
     float *alpha;                        // [max_pairs]
     int32_t *seg_adapter, *seg_start;    // [capacity], [capacity+1]
     int4 *tile;                          // [max_pairs] shrink tiles {adapter, q0, n, segment}
+    int32_t *tile_tok;                   // [max_pairs][SHRINK_TT] tokens of each tile's pairs
     int32_t *tmp_tok;                    // [max_pairs] scratch
     int32_t *hdr;                        // [HDR_WORDS]
     float *z;                            // [max_pairs][LORA_MAX_RANK] shrink output
@@ -55,16 +61,20 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
                                  const float *alpha, int T, int P, int capacity, int max_pairs,
                                  cudaStream_t st);
 cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int32_t *ranks,
-                          const MapDev &m, int rg, int grid, cudaStream_t st);
+                          const MapDev &m, int P, int rg, int grid, cudaStream_t st);
 
 // z row stride (floats): r_max rounded up to a multiple of 4 (16-byte rows).
 inline int z_stride(int r_max) { return (r_max + 3) & ~3; }
 cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
-                          const MapDev &m, int T, int tb, bool pdl, cudaStream_t st);
+                          const MapDev &m, int T, int P, int tb, int w, bool pdl, cudaStream_t st);
 cudaError_t launch_transpose_bf16(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int rows, int cols,
                                   cudaStream_t st);
 cudaError_t launch_set_int(int32_t *p, int v, cudaStream_t st);
 
 int sm_count();
+
+// Upper bound of the number of shrink tiles of P pairs over `capacity` ids
+// (host-computable; the mapping fills unused tile slots with empty records).
+int shrink_tile_bound(int P, int capacity);
 
 }  // namespace tcl

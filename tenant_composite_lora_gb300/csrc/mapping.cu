@@ -7,15 +7,19 @@
 // B are read once.
 //
 // One CTA of 1024 threads performs a stable counting sort on the adapter id
-// (the key range is the pool capacity, a few thousand at most):
-//   1. check the CSR offsets; expand them into the token of each pair;
-//   2. per-warp histograms of the adapter ids over contiguous chunks of the
-//      pairs (warp-level match + popcount, no atomics);
-//   3. one block scan over (bin, warp) gives every warp's first output slot
-//      per bin, the segment starts, and the shrink tiles (<= SHRINK_TT pairs
-//      of one segment);
+// (the key range is the pool capacity):
+//   0. stage the offsets, ids and alpha bits in shared memory when they fit
+//      (one coalesced read; every later step works on shared memory);
+//   1. check the CSR offsets;
+//   2. expand the offsets into the token of each pair, and build per-warp
+//      histograms of the ids over contiguous chunks of the pairs (warp-level
+//      match + popcount, no atomics; layout [warp][bin], conflict-free);
+//   3. block scans over the bins give every warp's first output slot per
+//      bin, the segments, and the shrink tiles (<= SHRINK_TT pairs of one
+//      segment; slots up to the host-known bound get empty sentinels);
 //   4. each warp rescans its chunk and scatters: rank among equal keys =
-//      earlier lanes with the same key + the warp's running cursor.
+//      earlier lanes with the same key + the warp's running cursor; the
+//      token also goes to its shrink tile's token list.
 // Stability: chunks are in CSR order, warps are ranked by chunk, lanes by
 // pair index, so ties keep CSR order -- the tuples come out ordered by
 // (adapter, p).  The result does not depend on timing.
@@ -30,17 +34,17 @@ struct Scan3 {
     int a, b, c;
 };
 
-// Block-wide exclusive scan of three ints (1024 threads); returns the
+// Block-wide exclusive scan of three ints (MAP_THREADS threads); returns the
 // exclusive prefix and writes the block totals.
-__device__ Scan3 block_exclusive_scan3(Scan3 v, Scan3 &total, int *sh /* [3][32] */)
+__device__ Scan3 block_exclusive_scan3(Scan3 v, Scan3 &total, int *sh /* [3 * 32 + 3] */)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     Scan3 inc = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        int a = __shfl_up_sync(0xffffffffu, inc.a, off);
-        int b = __shfl_up_sync(0xffffffffu, inc.b, off);
-        int c = __shfl_up_sync(0xffffffffu, inc.c, off);
+        const int a = __shfl_up_sync(0xffffffffu, inc.a, off);
+        const int b = __shfl_up_sync(0xffffffffu, inc.b, off);
+        const int c = __shfl_up_sync(0xffffffffu, inc.c, off);
         if (lane >= off) {
             inc.a += a;
             inc.b += b;
@@ -54,20 +58,20 @@ __device__ Scan3 block_exclusive_scan3(Scan3 v, Scan3 &total, int *sh /* [3][32]
     }
     __syncthreads();
     if (warp == 0) {
-        int a = sh[lane], b = sh[32 + lane], c = sh[64 + lane];
+        const int a = sh[lane], b = sh[32 + lane], c = sh[64 + lane];
         int ia = a, ib = b, ic = c;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            int xa = __shfl_up_sync(0xffffffffu, ia, off);
-            int xb = __shfl_up_sync(0xffffffffu, ib, off);
-            int xc = __shfl_up_sync(0xffffffffu, ic, off);
+            const int xa = __shfl_up_sync(0xffffffffu, ia, off);
+            const int xb = __shfl_up_sync(0xffffffffu, ib, off);
+            const int xc = __shfl_up_sync(0xffffffffu, ic, off);
             if (lane >= off) {
                 ia += xa;
                 ib += xb;
                 ic += xc;
             }
         }
-        sh[lane] = ia - a;  // exclusive warp offsets
+        sh[lane] = ia - a;
         sh[32 + lane] = ib - b;
         sh[64 + lane] = ic - c;
         if (lane == 31) {
@@ -88,27 +92,61 @@ __device__ Scan3 block_exclusive_scan3(Scan3 v, Scan3 &total, int *sh /* [3][32]
     return r;
 }
 
-__global__ void __launch_bounds__(MAP_THREADS, 1)
-    k_build_mapping(MapDev m, const int32_t *__restrict__ off, const int32_t *__restrict__ ids,
-                    const float *__restrict__ alpha, int T, int P, int cap, int nw)
+struct MapArgs {
+    MapDev m;
+    const int32_t *off, *ids;
+    const float *alpha;
+    int T, P, cap, nw, staged, tile_bound;
+};
+
+__global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
 {
-    extern __shared__ int32_t hist[];  // [cap][nw]: counts, then cursors
-    __shared__ int s_bad;
+    extern __shared__ int32_t sh[];
     __shared__ int s_scan[3 * 32 + 3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.T, P = a.P, cap = a.cap, nw = a.nw;
+    MapDev &m = a.m;
 
-    if (tid == 0) {
-        s_bad = (off[0] != 0 || off[T] != P) ? 1 : 0;
-        m.hdr[HDR_STATUS] = 0;
+    const int32_t *off, *ids, *alb;
+    int32_t *tok, *hist;
+    if (a.staged) {
+        int32_t *s_off = sh, *s_ids = sh + (T + 1), *s_al = s_ids + P;
+        tok = s_al + P;
+        hist = tok + P;
+        for (int i = tid; i <= T; i += MAP_THREADS)
+            s_off[i] = a.off[i];
+        const int32_t *alg = reinterpret_cast<const int32_t *>(a.alpha);
+        for (int p = tid; p < P; p += MAP_THREADS) {
+            s_ids[p] = a.ids[p];
+            s_al[p] = alg[p];
+        }
+        off = s_off;
+        ids = s_ids;
+        alb = s_al;
+    } else {
+        off = a.off;
+        ids = a.ids;
+        alb = reinterpret_cast<const int32_t *>(a.alpha);
+        tok = m.tmp_tok;
+        hist = sh;
     }
+    // per bin: first sorted position and first shrink tile of its segment
+    int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
+    for (int i = tid; i < nw * cap; i += MAP_THREADS)
+        hist[i] = 0;
+    if (tid == 0)
+        m.hdr[HDR_STATUS] = 0;
     __syncthreads();
+
+    // 1. CSR check
+    int bad = (tid == 0) && (off[0] != 0 || off[T] != P);
     for (int t = tid; t < T; t += MAP_THREADS)
-        if (off[t + 1] < off[t])
-            s_bad = 1;
-    __syncthreads();
-    if (s_bad) {
+        bad |= off[t + 1] < off[t];
+    if (__syncthreads_or(bad)) {
         for (int p = tid; p < P; p += MAP_THREADS)
             m.pos[p] = -1;
+        for (int i = tid; i < a.tile_bound; i += MAP_THREADS)
+            m.tile[i] = make_int4(0, 0, 0, -1);
         if (tid == 0) {
             m.hdr[HDR_U] = 0;
             m.hdr[HDR_PVALID] = 0;
@@ -120,21 +158,17 @@ __global__ void __launch_bounds__(MAP_THREADS, 1)
         return;
     }
 
-    // 1. token of each pair
+    // 2. token of each pair; per-warp histograms
     for (int t = tid; t < T; t += MAP_THREADS) {
-        const int a = off[t], b = off[t + 1];
-        for (int p = a; p < b; ++p)
-            m.tmp_tok[p] = t;
+        const int p0 = off[t], p1 = off[t + 1];
+        for (int p = p0; p < p1; ++p)
+            tok[p] = t;
     }
-    for (int i = tid; i < cap * nw; i += MAP_THREADS)
-        hist[i] = 0;
-    __syncthreads();
-
-    // 2. per-warp histograms over contiguous chunks
     const int chunk = (P + nw - 1) / nw;
     bool bad_id = false;
     if (warp < nw) {
         const int lo = warp * chunk, hi = min(P, lo + chunk);
+        int32_t *h = hist + warp * cap;
         for (int base = lo; base < hi; base += 32) {
             const int p = base + lane;
             const bool valid = p < hi;
@@ -143,63 +177,58 @@ __global__ void __launch_bounds__(MAP_THREADS, 1)
             bad_id |= valid && !ok;
             const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
             if (ok && lane == __ffs(peers) - 1)
-                hist[id * nw + warp] += __popc(peers);
+                h[id] += __popc(peers);
         }
     }
     if (bad_id)
         atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_ID);
     __syncthreads();
 
-    // 3. scan over bins (each thread owns a contiguous range of bins)
-    const int bpt = (cap + MAP_THREADS - 1) / MAP_THREADS;
-    const int b0 = min(cap, tid * bpt), b1 = min(cap, b0 + bpt);
-    Scan3 mine = {0, 0, 0};
-    for (int b = b0; b < b1; ++b) {
+    // 3. scan over bins, 1024 bins per round, bin-ascending
+    Scan3 carry = {0, 0, 0};
+    for (int base = 0; base < cap; base += MAP_THREADS) {
+        const int b = base + tid;
         int c = 0;
-        for (int w = 0; w < nw; ++w)
-            c += hist[b * nw + w];
-        mine.a += c;
-        if (c > 0) {
-            mine.b += 1;
-            mine.c += (c + SHRINK_TT - 1) / SHRINK_TT;
-        }
-    }
-    Scan3 total;
-    Scan3 base = block_exclusive_scan3(mine, total, s_scan);
-    {
-        int run = base.a, sidx = base.b, tix = base.c;
-        for (int b = b0; b < b1; ++b) {
-            int c = 0;
+        if (b < cap)
             for (int w = 0; w < nw; ++w)
-                c += hist[b * nw + w];
-            if (c > 0) {
-                m.seg_adapter[sidx] = b;
-                m.seg_start[sidx] = run;
-                const int ntl = (c + SHRINK_TT - 1) / SHRINK_TT;
-                for (int i = 0; i < ntl; ++i)
-                    m.tile[tix + i] = make_int4(b, run + i * SHRINK_TT, min(SHRINK_TT, c - i * SHRINK_TT), sidx);
-                tix += ntl;
-                ++sidx;
-            }
+                c += hist[w * cap + b];
+        const Scan3 mine = {c, c > 0 ? 1 : 0, (c + SHRINK_TT - 1) / SHRINK_TT};
+        Scan3 tot;
+        const Scan3 ex = block_exclusive_scan3(mine, tot, s_scan);
+        if (c > 0) {
+            int run = carry.a + ex.a;
+            const int sidx = carry.b + ex.b, tix = carry.c + ex.c;
+            m.seg_adapter[sidx] = b;
+            m.seg_start[sidx] = run;
+            bin_first[b] = run;
+            bin_tile[b] = tix;
+            for (int i = 0; i < mine.c; ++i)
+                m.tile[tix + i] = make_int4(b, run + i * SHRINK_TT, min(SHRINK_TT, c - i * SHRINK_TT), sidx);
             for (int w = 0; w < nw; ++w) {
-                const int v = hist[b * nw + w];
-                hist[b * nw + w] = run;
+                const int v = hist[w * cap + b];
+                hist[w * cap + b] = run;
                 run += v;
             }
         }
+        carry.a += tot.a;
+        carry.b += tot.b;
+        carry.c += tot.c;
     }
+    for (int i = carry.c + tid; i < a.tile_bound; i += MAP_THREADS)
+        m.tile[i] = make_int4(0, 0, 0, -1);  // empty slots up to the host-known bound
     if (tid == 0) {
-        m.hdr[HDR_U] = total.b;
-        m.hdr[HDR_PVALID] = total.a;
-        m.hdr[HDR_NTILES] = total.c;
+        m.hdr[HDR_U] = carry.b;
+        m.hdr[HDR_PVALID] = carry.a;
+        m.hdr[HDR_NTILES] = carry.c;
         m.hdr[HDR_T] = T;
-        m.seg_start[total.b] = total.a;
+        m.seg_start[carry.b] = carry.a;
     }
     __syncthreads();
 
     // 4. stable scatter
     if (warp < nw) {
         const int lo = warp * chunk, hi = min(P, lo + chunk);
+        int32_t *h = hist + warp * cap;
         const unsigned lt = (1u << lane) - 1u;
         for (int bse = lo; bse < hi; bse += 32) {
             const int p = bse + lane;
@@ -207,12 +236,15 @@ __global__ void __launch_bounds__(MAP_THREADS, 1)
             const int id = valid ? ids[p] : 0;
             const bool ok = valid && id >= 0 && id < cap;
             const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
-            const int cur = ok ? hist[id * nw + warp] : 0;
+            const int cur = ok ? h[id] : 0;
             if (ok) {
                 const int dst = cur + __popc(peers & lt);
-                m.tok[dst] = m.tmp_tok[p];
+                const int t = tok[p];
+                m.tok[dst] = t;
+                const int r = dst - bin_first[id];
+                m.tile_tok[(bin_tile[id] + r / SHRINK_TT) * SHRINK_TT + r % SHRINK_TT] = t;
                 m.adapter[dst] = id;
-                m.alpha[dst] = alpha[p];
+                reinterpret_cast<int32_t *>(m.alpha)[dst] = alb[p];
                 m.src[dst] = p;
                 m.pos[p] = dst;
             } else if (valid) {
@@ -220,7 +252,7 @@ __global__ void __launch_bounds__(MAP_THREADS, 1)
             }
             __syncwarp();
             if (ok && lane == __ffs(peers) - 1)
-                hist[id * nw + warp] = cur + __popc(peers);
+                h[id] = cur + __popc(peers);
             __syncwarp();
         }
     }
@@ -228,28 +260,50 @@ __global__ void __launch_bounds__(MAP_THREADS, 1)
 
 }  // namespace
 
+int shrink_tile_bound(int P, int capacity)
+{
+    if (P <= 0)
+        return 0;
+    const long long b = (long long)(P + SHRINK_TT - 1) / SHRINK_TT + (P < capacity ? P : capacity);
+    return (int)(b < P ? b : P);
+}
+
 cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const int32_t *ids,
                                  const float *alpha, int T, int P, int capacity, int max_pairs,
                                  cudaStream_t st)
 {
     (void)max_pairs;
-    int nw = MAP_HIST_BYTES / (4 * capacity);
-    if (nw > 32)
-        nw = 32;
+    const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
+    const long long staged_words = (long long)(T + 1) + 3LL * P;
+    int nw = (P + 63) / 64;
+    nw = nw < 1 ? 1 : (nw > 32 ? 32 : nw);
+    int staged = 0;
+    // words: [staged arrays] + nw histograms + two per-bin arrays
+    if (staged_words + 3LL * capacity <= budget) {
+        staged = 1;
+        const long long fit = (budget - staged_words) / capacity - 2;
+        if (nw > fit)
+            nw = (int)fit;
+    } else {
+        const long long fit = budget / capacity - 2;
+        if (nw > fit)
+            nw = (int)fit;
+    }
     if (nw < 1)
         return cudaErrorInvalidValue;
-    const size_t smem = (size_t)capacity * nw * sizeof(int32_t);
+    const size_t smem = 4 * ((staged ? (size_t)staged_words : 0) + (size_t)(nw + 2) * capacity);
     static int attr_done = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_build_mapping, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             MAP_HIST_BYTES);
+        cudaError_t e =
+            cudaFuncSetAttribute(k_build_mapping, cudaFuncAttributeMaxDynamicSharedMemorySize, MAP_SMEM_BYTES);
         if (e != cudaSuccess)
             return e;
         attr_done = dev;
     }
-    k_build_mapping<<<1, MAP_THREADS, smem, st>>>(m, offsets, ids, alpha, T, P, capacity, nw);
+    MapArgs a{m, offsets, ids, alpha, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity)};
+    k_build_mapping<<<1, MAP_THREADS, smem, st>>>(a);
     return cudaGetLastError();
 }
 

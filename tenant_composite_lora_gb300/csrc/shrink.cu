@@ -9,19 +9,22 @@
 // page, "Core idea", paper Sec. 3.1 M1).
 //
 // Work unit = (segment tile of <= SHRINK_TT pairs of one adapter, group of <=
-// SHRINK_RG retained rows).  The pool stores A transposed (r_max x d_in), so a
-// unit's rows are contiguous, 16-byte aligned runs that one thread streams
-// into shared memory with bulk (TMA) copies completing on an mbarrier; x rows
-// of the tile's tokens come the same way.  d_in is consumed in chunks of
-// SHRINK_DC through a SHRINK_STAGES-deep ring.  Each thread owns one 16-byte
-// vector of every staged row, accumulates TT x RG partial dot products in
-// fp32, and the CTA reduces them with a warp-shuffle reduce-scatter (32
-// values over 32 lanes in 31 shuffles) and one cross-warp pass.
+// SHRINK_RG retained rows).  Units are numbered rowgroup-major over the
+// host-known tile bound, so a CTA resolves its units with one round trip
+// (tile record and its token list, same index) and the retained ranks come
+// from a table staged in shared memory.  The pool stores A transposed
+// (r_max x d_in): a unit's rows are 16-byte-aligned contiguous runs that one
+// thread streams with bulk (TMA) copies into a byte ring in shared memory,
+// each entry (unit, d_in chunk) completing on its own mbarrier; entries are
+// issued as long as ring space and barrier slots allow, so every byte a CTA
+// needs is in flight from the start when it fits.  Each thread owns one
+// 16-byte vector of every staged row, accumulates SHRINK_TT x SHRINK_RG fp32
+// partial dot products, and the CTA reduces them with a warp-shuffle
+// reduce-scatter (32 values over 32 lanes in 31 shuffles) and one cross-warp
+// pass.
 //
-// Persistent grid: CTA b takes units b, b + G, b + 2G, ... of the list
-// ordered rowgroup-major, which mixes light and heavy units across CTAs.
-// The kernel calls griddepcontrol.launch_dependents at entry so the expand
-// kernel that follows can start staging B while this one runs.
+// Persistent grid; griddepcontrol.launch_dependents at entry lets the expand
+// kernel that follows start staging B while this one runs.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -29,18 +32,21 @@ namespace tcl {
 
 namespace {
 
-constexpr int TT = SHRINK_TT, RG = SHRINK_RG, DC = SHRINK_DC, S = SHRINK_STAGES;
-constexpr int STG = (RG + TT) * DC;  // bf16 elements per stage
+constexpr int TT = SHRINK_TT, RG = SHRINK_RG, DC = SHRINK_DC;
+constexpr int RING = SHRINK_RING_BYTES, MAXE = SHRINK_MAX_INFLIGHT;
 constexpr int MAX_LIST = SHRINK_THREADS;
 static_assert(TT * RG == 32, "one reduced value per lane");
+static_assert((RG + TT) * DC * 2 <= RING, "one entry of any shape fits the empty ring");
 
 struct ShrinkArgs {
     const __nv_bfloat16 *x;
     PoolDev pool;
     const int32_t *ranks;
     MapDev m;
-    int rg;  // rows per unit, <= RG
-    int zs;  // z row stride (floats)
+    int rg;          // rows per unit, <= RG
+    int zs;          // z row stride (floats)
+    int tile_bound;  // tile slots written by the mapping
+    int use_tab;     // ranks staged in shared memory
 };
 
 __device__ __forceinline__ void unpack8(const uint4 w, float f[8])
@@ -58,8 +64,10 @@ __device__ __forceinline__ void unpack8(const uint4 w, float f[8])
 __global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    __nv_bfloat16 *stage = reinterpret_cast<__nv_bfloat16 *>(smem_raw);
-    __shared__ __align__(8) uint64_t full[S];
+    unsigned char *ring = smem_raw;
+    int *rank_tab = reinterpret_cast<int *>(smem_raw + RING);
+    __shared__ __align__(8) uint64_t bar[MAXE];
+    __shared__ int e_off[MAXE];
     __shared__ float red[2][8][32];
     __shared__ int4 s_unit[MAX_LIST];  // {adapter, q0, n, (j0 << 8) | R}
     __shared__ int s_tok[MAX_LIST][TT];
@@ -70,45 +78,46 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d_in = a.pool.d_in, r_max = a.pool.r_max;
     int32_t *status = a.m.hdr + HDR_STATUS;
-    const int ntiles = a.m.hdr[HDR_NTILES];
     const int rgm = (r_max + a.rg - 1) / a.rg;
-    const long long nunits = (long long)ntiles * rgm;
+    const long long nunits = (long long)a.tile_bound * rgm;
     const int nch = (d_in + DC - 1) / DC;
 
+    if (a.use_tab)
+        for (int i = tid; i < a.pool.capacity; i += SHRINK_THREADS)
+            rank_tab[i] = effective_rank(a.pool, a.ranks, i);
     if (tid == 0) {
-        for (int s = 0; s < S; ++s)
-            mbar_init(&full[s], 1);
+        for (int s = 0; s < MAXE; ++s)
+            mbar_init(&bar[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
 
-    uint32_t g_base = 0;  // chunk sequence number (drives ring slot and parity)
+    uint32_t e_base = 0;  // entry sequence number of this pass's first entry
     int unit_parity = 0;
     for (long long pass = blockIdx.x; pass < nunits; pass += (long long)gridDim.x * MAX_LIST) {
-        // ---- resolve this pass's units in parallel and compact the live ones
+        // ---- resolve this pass's units (one round trip) and compact the live ones
         const long long u = pass + (long long)tid * gridDim.x;
         bool live = false;
         int4 rec = make_int4(0, 0, 0, 0);
         int toks[TT];
-#pragma unroll
-        for (int i = 0; i < TT; ++i)
-            toks[i] = 0;
         if (u < nunits) {
-            const int rg = (int)(u / ntiles), tile = (int)(u % ntiles);
-            const int4 t = a.m.tile[tile];  // {adapter, q0, n, segment}
-            const int k = effective_rank(a.pool, a.ranks, t.x);
-            if (k < 0) {
-                if (rg == 0)
-                    atomicOr(status, k == -1 ? LORA_DEV_UNREGISTERED : LORA_DEV_BAD_RANK);
-            } else {
-                const int j0 = rg * a.rg;
-                if (j0 < k) {
-                    live = true;
-                    rec = make_int4(t.x, t.y, t.z, (j0 << 8) | min(a.rg, k - j0));
-#pragma unroll
-                    for (int i = 0; i < TT; ++i)
-                        if (i < t.z)
-                            toks[i] = a.m.tok[t.y + i];
+            const int rg = (int)(u / a.tile_bound), tile = (int)(u % a.tile_bound);
+            const int4 t = a.m.tile[tile];  // {adapter, q0, n, segment}; n = 0: empty slot
+            const int4 tk0 = reinterpret_cast<const int4 *>(a.m.tile_tok)[2 * tile];
+            const int4 tk1 = reinterpret_cast<const int4 *>(a.m.tile_tok)[2 * tile + 1];
+            toks[0] = tk0.x; toks[1] = tk0.y; toks[2] = tk0.z; toks[3] = tk0.w;
+            toks[4] = tk1.x; toks[5] = tk1.y; toks[6] = tk1.z; toks[7] = tk1.w;
+            if (t.z > 0) {
+                const int k = a.use_tab ? rank_tab[t.x] : effective_rank(a.pool, a.ranks, t.x);
+                if (k < 0) {
+                    if (rg == 0)
+                        atomicOr(status, k == -1 ? LORA_DEV_UNREGISTERED : LORA_DEV_BAD_RANK);
+                } else {
+                    const int j0 = rg * a.rg;
+                    if (j0 < k) {
+                        live = true;
+                        rec = make_int4(t.x, t.y, t.z, (j0 << 8) | min(a.rg, k - j0));
+                    }
                 }
             }
         }
@@ -131,31 +140,64 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
         }
         __syncthreads();
 
-        // ---- pipeline over L units x nch chunks
+        // ---- entries = L units x nch chunks through the byte ring
         const int total = L * nch;
-        auto issue = [&](int c, uint32_t g) {
-            const int e = c / nch, ch = c % nch;
-            const int4 r = s_unit[e];
-            const int n = r.z, R = r.w & 0xff, j0 = r.w >> 8;
-            const int c0 = ch * DC, clen = min(DC, d_in - c0);
-            const uint32_t row_bytes = (uint32_t)clen * 2u;
-            __nv_bfloat16 *dst = stage + (size_t)(g % S) * STG;
-            uint64_t *bar = &full[g % S];
-            mbar_arrive_expect_tx(bar, row_bytes * (uint32_t)(R + n));
-            const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
-            for (int rr = 0; rr < R; ++rr)
-                bulk_g2s(dst + rr * DC, Abase + (size_t)rr * d_in, row_bytes, bar);
-            for (int i = 0; i < n; ++i)
-                bulk_g2s(dst + (RG + i) * DC, a.x + (size_t)s_tok[e][i] * d_in + c0, row_bytes, bar);
+        // producer state, used by thread 0 only
+        int p_next = 0, head = 0;
+        auto entry_bytes = [&](int c) -> int {
+            const int4 r = s_unit[c / nch];
+            const int clen = min(DC, d_in - (c % nch) * DC);
+            return ((r.w & 0xff) + r.z) * clen * 2;
+        };
+        auto issue_more = [&](int c_done) {
+            while (p_next < total && p_next - c_done < MAXE) {
+                const int size = entry_bytes(p_next);
+                int pos;
+                if (p_next == c_done) {
+                    pos = 0;  // ring empty
+                } else {
+                    const int tail = e_off[(e_base + c_done) % MAXE];
+                    if (head > tail) {
+                        if (head + size <= RING)
+                            pos = head;
+                        else if (size < tail)
+                            pos = 0;
+                        else
+                            break;
+                    } else {
+                        if (head + size < tail)
+                            pos = head;
+                        else
+                            break;
+                    }
+                }
+                const int slot = (e_base + p_next) % MAXE;
+                e_off[slot] = pos;
+                const int e = p_next / nch, ch = p_next % nch;
+                const int4 r = s_unit[e];
+                const int n = r.z, R = r.w & 0xff, j0 = r.w >> 8;
+                const int c0 = ch * DC, clen = min(DC, d_in - c0);
+                const uint32_t row_bytes = (uint32_t)clen * 2u;
+                unsigned char *dst = ring + pos;
+                mbar_arrive_expect_tx(&bar[slot], row_bytes * (uint32_t)(R + n));
+                const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
+                for (int rr = 0; rr < R; ++rr)
+                    bulk_g2s(dst + rr * row_bytes, Abase + (size_t)rr * d_in, row_bytes, &bar[slot]);
+                for (int i = 0; i < n; ++i)
+                    bulk_g2s(dst + (R + i) * row_bytes, a.x + (size_t)s_tok[e][i] * d_in + c0, row_bytes,
+                             &bar[slot]);
+                head = pos + size;
+                ++p_next;
+            }
         };
         if (tid == 0)
-            for (int c = 0; c < total && c < S; ++c)
-                issue(c, g_base + c);
+            issue_more(0);
 
         float acc[TT][RG];
         for (int c = 0; c < total; ++c) {
-            const uint32_t g = g_base + c;
-            const bool ok = mbar_wait_bounded(&full[g % S], (g / S) & 1u, status);
+            const uint32_t g = e_base + c;
+            const int slot = g % MAXE;
+            const bool ok = mbar_wait_bounded(&bar[slot], (g / MAXE) & 1u, status);
             const int e = c / nch, ch = c % nch;
             const int4 r = s_unit[e];
             const int n = r.z, R = r.w & 0xff;
@@ -167,18 +209,18 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
                         acc[i][rr] = 0.f;
             }
             const int clen = min(DC, d_in - ch * DC);
-            const __nv_bfloat16 *sA = stage + (size_t)(g % S) * STG;
+            const __nv_bfloat16 *sA = reinterpret_cast<const __nv_bfloat16 *>(ring + e_off[slot]);
             if (ok && tid * 8 < clen) {
                 float av[RG][8];
 #pragma unroll
                 for (int rr = 0; rr < RG; ++rr)
                     if (rr < R)
-                        unpack8(lds128(sA + rr * DC + tid * 8), av[rr]);
+                        unpack8(lds128(sA + rr * clen + tid * 8), av[rr]);
 #pragma unroll
                 for (int i = 0; i < TT; ++i) {
                     if (i < n) {
                         float xv[8];
-                        unpack8(lds128(sA + (RG + i) * DC + tid * 8), xv);
+                        unpack8(lds128(sA + (R + i) * clen + tid * 8), xv);
 #pragma unroll
                         for (int rr = 0; rr < RG; ++rr) {
                             if (rr < R) {
@@ -215,9 +257,9 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
             }
             const int any_bad = __syncthreads_or(!ok);
             if (any_bad)
-                return;  // a copy never landed: status already records it
-            if (tid == 0 && c + S < total)
-                issue(c + S, g + S);
+                return;  // a copy never landed: the status word records it
+            if (tid == 0)
+                issue_more(c + 1);
             if (last) {
                 if (warp == 0) {
                     float s = 0.f;
@@ -233,7 +275,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
                 unit_parity ^= 1;
             }
         }
-        g_base += (uint32_t)total;
+        e_base += (uint32_t)total;
         __syncthreads();
     }
 }
@@ -241,19 +283,21 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
 }  // namespace
 
 cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int32_t *ranks,
-                          const MapDev &m, int rg, int grid, cudaStream_t st)
+                          const MapDev &m, int P, int rg, int grid, cudaStream_t st)
 {
-    const size_t smem = (size_t)S * STG * sizeof(__nv_bfloat16);
+    const int use_tab = pool.capacity <= RANK_TAB_MAX ? 1 : 0;
+    const size_t smem = (size_t)RING + (use_tab ? (size_t)((pool.capacity + 3) & ~3) * sizeof(int) : 0);
     static int attr_done = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(k_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             RING + RANK_TAB_MAX * (int)sizeof(int));
         if (e != cudaSuccess)
             return e;
         attr_done = dev;
     }
-    ShrinkArgs a{x, pool, ranks, m, rg, z_stride(pool.r_max)};
+    ShrinkArgs a{x, pool, ranks, m, rg, z_stride(pool.r_max), shrink_tile_bound(P, pool.capacity), use_tab};
     k_shrink<<<grid, SHRINK_THREADS, smem, st>>>(a);
     return cudaGetLastError();
 }
