@@ -138,16 +138,42 @@ int choose_path(int T, int P, int r_max, int d_in, int d_out)
     return LORA_PATH_SPLIT;
 }
 
-// Expand tile: 64 columns when that alone gives a CTA per SM, else 32; then
-// the largest token block of 64, 32, 16, 8 that still gives a CTA per SM.
-void choose_expand_tile(int T, int d_out, int &tb, int &w)
+// Expand plan.  Decode batches (T * 32 <= EXP_TILE_ELEMS) take the whole
+// batch as one token block and split each column tile's segments over a
+// cluster of ng CTAs, choosing (W, ng) for the most CTAs that still fit one
+// per SM beside the shrink (ties: the middle width, then wider).  Longer
+// batches take 64 columns and the largest token block that gives a CTA per SM.
+ExpandPlan choose_expand_plan(int T, int d_out)
 {
     const int sms = sm_count();
-    w = (d_out / 64 >= sms) ? 64 : 32;
-    const int n_ct = d_out / w;
-    tb = EXP_TB_MAX;
-    while (tb > 8 && (long long)n_ct * ((T + tb - 1) / tb) < sms)
-        tb >>= 1;
+    ExpandPlan best{0, 0, 0};
+    if ((long long)T * 32 <= EXP_TILE_ELEMS) {
+        int best_ctas = -1;
+        const int order[3] = {64, 128, 32};
+        for (int w : order) {
+            if (d_out % w || (long long)T * w > EXP_TILE_ELEMS)
+                continue;
+            const int n_ct = d_out / w;
+            if (n_ct > sms)
+                continue;
+            int ng = 1;
+            while (ng < 8 && (long long)n_ct * ng * 2 <= sms)
+                ng *= 2;
+            if (n_ct * ng > best_ctas) {
+                best_ctas = n_ct * ng;
+                best = ExpandPlan{T, w, ng};
+            }
+        }
+        if (best_ctas > 0)
+            return best;
+    }
+    best.w = 64;
+    best.ng = 1;
+    const int n_ct = d_out / 64;
+    best.tb = EXP_TILE_ELEMS / 64;
+    while (best.tb > 8 && (long long)n_ct * ((T + best.tb - 1) / best.tb) < sms)
+        best.tb >>= 1;
+    return best;
 }
 
 lora_status run_split(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
@@ -159,9 +185,8 @@ lora_status run_split(const void *x, void *y, const lora_pool *pool, const int32
         launch_shrink(static_cast<const __nv_bfloat16 *>(x), pd, ranks, m->dev, m->P, SHRINK_RG, grid, st);
     if (e != cudaSuccess)
         return from_cuda(e);
-    int tb = 0, w = 0;
-    choose_expand_tile(m->T, pool->d_out, tb, w);
-    e = launch_expand(static_cast<__nv_bfloat16 *>(y), pd, ranks, m->dev, m->T, m->P, tb, w, /*pdl=*/true, st);
+    const ExpandPlan plan = choose_expand_plan(m->T, pool->d_out);
+    e = launch_expand(static_cast<__nv_bfloat16 *>(y), pd, ranks, m->dev, m->T, plan, /*pdl=*/true, st);
     return from_cuda(e);
 }
 

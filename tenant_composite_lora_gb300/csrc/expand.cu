@@ -6,25 +6,28 @@
 // LoRA summary page, "Core idea" (paper Sec. 4.3): pairs are walked in adapter
 // order, so each adapter's B tile is staged once for all of its tokens.
 //
-// CTA = (token block [t0, t0 + tb), blockIdx.x) x (32 or 64 output
-// columns, blockIdx.y).  The CTA owns
-// its y tile outright: every pair of every token of the block is summed into
-// an fp32 accumulator tile in shared memory, in a fixed order (segment
-// ascending, then pair order), and the tile is rounded once to bf16 and
-// written.  No global atomics; the result does not depend on timing.
+// CTA = (token block [t0, t0 + tb), blockIdx.y) x (W output columns) x
+// (segment group g of ng).  The ng CTAs of one column tile form a thread-block
+// cluster: each sums the pairs of its share of the segments into an fp32
+// accumulator tile in shared memory, then the cluster reduces the ng tiles
+// through distributed shared memory in a fixed order, adds y and rounds once
+// to bf16.  The result does not depend on timing and needs no global atomics.
+// For a decode batch the token block is the whole batch (no search); for
+// longer batches the block's pairs of a segment are found by binary search
+// (tokens are ascending inside a segment) and ng = 1.
 //
-// Inside a segment the pairs are ordered by token, so the block's pairs of a
-// segment are one contiguous range (found by binary search).  Ranges are cut
-// into jobs of <= EXP_JP pairs; a window of jobs is staged with 16-byte
-// cp.async copies: the k retained B rows x EXP_W columns of each job, the
-// jobs' z rows, the tokens.  Warp w owns the block tokens with
-// (t - t0) % 8 == w; each lane owns one or two columns.  The segment list,
-// the header and a shared-memory table of retained ranks are read at entry in
-// one round trip; a decode batch (T <= token block) needs no search.
+// Segment ranges are cut into jobs of <= EXP_JP pairs; a window of jobs is
+// staged with 16-byte cp.async copies (the k retained B rows x W columns of
+// each job, the jobs' z rows, their tokens).  On its first visit of a segment
+// the CTA also prefetches that segment's B rows into L2 with bulk prefetches,
+// so windows after the first hit L2.  Warp w owns the block tokens with
+// (t - t0) % 8 == w; each lane owns W / 32 columns and keeps its slice of up
+// to 16 B rows in registers while it walks the job's pairs.
 //
 // Launched with programmatic dependent launch after the shrink kernel: the
-// first window's B tiles and the y tile (neither written by the shrink) are
-// staged before griddepcontrol.wait, overlapping the shrink; z is read after.
+// metadata, the first window's B tiles, the L2 prefetches and the y tile
+// (none of them written by the shrink) come before griddepcontrol.wait; z is
+// read after.
 #include <climits>
 
 #include "internal.h"
@@ -35,10 +38,9 @@ namespace tcl {
 namespace {
 
 constexpr int NWARP = EXP_THREADS / 32;
-constexpr int WMAX = EXP_W;
 constexpr int B_ELEMS = EXP_B_BYTES / 2;
 constexpr int Z_FLOATS = EXP_Z_BYTES / 4;
-constexpr int WIN_PAIRS = 1024;
+constexpr int WIN_PAIRS = EXP_WIN_PAIRS;
 static_assert(NWARP == 8, "warp owns tokens mod 8");
 
 struct ExpandArgs {
@@ -47,19 +49,25 @@ struct ExpandArgs {
     const int32_t *ranks;
     MapDev m;
     int T, tb, zs;
-    int seg_bound;  // host-known bound on the number of segments
-    int use_tab;    // ranks staged in shared memory
+    int ng;       // segment groups = cluster size along x
+    int use_tab;  // ranks staged in shared memory
 };
 
-struct Smem {
-    float acc[EXP_TB_MAX * WMAX];
-    __nv_bfloat16 yin[EXP_TB_MAX * WMAX];
-    __nv_bfloat16 B[B_ELEMS];
-    float Z[Z_FLOATS];
-    int tok[WIN_PAIRS];
-    int4 jobA[EXP_MAX_JOBS];  // {adapter, q, len, k}
-    int4 jobB[EXP_MAX_JOBS];  // {B offset (elements), Z offset (floats), tok offset, kp}
-    int rank_tab[RANK_TAB_MAX];
+// Dynamic shared memory layout (byte offsets), identical on host and device.
+struct ExpLayout {
+    int acc, yin, B, Z, tok, jobA, jobB, rank, total;
+    __host__ __device__ ExpLayout(int tb, int w, int cap_tab)
+    {
+        acc = 0;
+        yin = acc + tb * w * 4;
+        B = (yin + tb * w * 2 + 127) & ~127;
+        Z = B + EXP_B_BYTES;
+        tok = Z + EXP_Z_BYTES;
+        jobA = tok + WIN_PAIRS * 4;
+        jobB = jobA + EXP_MAX_JOBS * 16;
+        rank = jobB + EXP_MAX_JOBS * 16;
+        total = rank + ((cap_tab + 3) & ~3) * 4;
+    }
 };
 
 __device__ __forceinline__ int lower_bound_tok(const int32_t *tok, int lo, int hi, int v)
@@ -117,47 +125,88 @@ __device__ int4 block_scan4(int4 v, int4 &total, int4 *sh /* [NWARP] */)
                      before.w + inc.w - v.w);
 }
 
-// W output columns per CTA: 64 (lane owns 2 columns) or 32 (lane owns 1).
-template <int W>
-__global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
 {
-    static_assert(W == 32 || W == 64, "tile width");
-    constexpr int VPR = W / 8;  // 16-byte vectors per tile row
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank)
+{
+    uint32_t raddr;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(raddr)
+                 : "memory");
+    return v;
+}
+
+template <int W>
+__global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
+{
+    static_assert(W == 32 || W == 64 || W == 128, "tile width");
+    constexpr int VPR = W / 8;   // 16-byte vectors per tile row
+    constexpr int CPL = W / 32;  // columns per lane
     extern __shared__ __align__(128) unsigned char smem_raw[];
-    Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
+    const ExpLayout L(a.tb, W, a.use_tab ? a.pool.capacity : 0);
+    float *acc = reinterpret_cast<float *>(smem_raw + L.acc);
+    __nv_bfloat16 *yin = reinterpret_cast<__nv_bfloat16 *>(smem_raw + L.yin);
+    __nv_bfloat16 *sB = reinterpret_cast<__nv_bfloat16 *>(smem_raw + L.B);
+    float *sZ = reinterpret_cast<float *>(smem_raw + L.Z);
+    int *sTok = reinterpret_cast<int *>(smem_raw + L.tok);
+    int4 *jobA = reinterpret_cast<int4 *>(smem_raw + L.jobA);  // {adapter, q, len, k}
+    int4 *jobB = reinterpret_cast<int4 *>(smem_raw + L.jobB);  // {B offset, Z offset, tok offset, kp}
+    int *rank_tab = reinterpret_cast<int *>(smem_raw + L.rank);
     __shared__ int4 s_scan[NWARP];
     __shared__ int s_cutjob, s_cur_s, s_cur_p;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d_out = a.pool.d_out, r_max = a.pool.r_max;
-    const int c0 = blockIdx.y * W;
-    const int t0 = blockIdx.x * a.tb, t1 = min(a.T, t0 + a.tb), nt = t1 - t0;
+    const int ng = a.ng;
+    const int g = ng > 1 ? (int)cluster_ctarank() : 0;
+    const int c0 = (blockIdx.x / ng) * W;
+    const int t0 = blockIdx.y * a.tb, t1 = min(a.T, t0 + a.tb), nt = t1 - t0;
     const bool full_range = (t0 == 0 && t1 >= a.T);
+    // rows of the tile this CTA finalises
+    const int r0 = (nt * g) / ng, r1 = (nt * (g + 1)) / ng;
 
-    // y tile (not written by the shrink: legal before the dependency wait)
-    for (int i = tid; i < nt * VPR; i += EXP_THREADS) {
-        const int t = i / VPR, v = i % VPR;
-        cp_async16(&sm.yin[t * W + v * 8], a.y + (size_t)(t0 + t) * d_out + c0 + v * 8);
+    for (int i = tid; i < (r1 - r0) * VPR; i += EXP_THREADS) {
+        const int t = r0 + i / VPR, v = i % VPR;
+        cp_async16(&yin[t * W + v * 8], a.y + (size_t)(t0 + t) * d_out + c0 + v * 8);
     }
     cp_async_commit();
     if (a.use_tab)
         for (int i = tid; i < a.pool.capacity; i += EXP_THREADS)
-            sm.rank_tab[i] = effective_rank(a.pool, a.ranks, i);
+            rank_tab[i] = effective_rank(a.pool, a.ranks, i);
     for (int i = tid; i < nt * W; i += EXP_THREADS)
-        sm.acc[i] = 0.f;
-    const int U = min(a.m.hdr[HDR_U], a.seg_bound);
+        acc[i] = 0.f;
+    const int U = a.m.hdr[HDR_U];
+    const int s_begin = (int)(((long long)U * g) / ng), s_end = (int)(((long long)U * (g + 1)) / ng);
     __syncthreads();
 
     bool waited = false;
-    int s_next = 0, piece_next = 0;
-    while (s_next < U) {
-        // ---- build a window of jobs from segments s_next .. s_next + 255
+    int s_next = s_begin, piece_next = 0;
+    while (s_next < s_end) {
+        // ---- build a window of jobs from segments s_next .. s_next + 255 of the group
         const int s = s_next + tid;
         int k = 0, lo = 0, hi = 0, adapter = 0, pfirst = 0, np = 0;
-        if (s < U) {
+        if (s < s_end) {
             adapter = a.m.seg_adapter[s];
             const int sa = a.m.seg_start[s], sb = a.m.seg_start[s + 1];
-            k = a.use_tab ? sm.rank_tab[adapter] : effective_rank(a.pool, a.ranks, adapter);
+            k = a.use_tab ? rank_tab[adapter] : effective_rank(a.pool, a.ranks, adapter);
             if (k < 0)
                 k = 0;
             if (k > 0) {
@@ -172,11 +221,16 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
             if (hi > lo) {
                 pfirst = (tid == 0) ? piece_next : 0;
                 np = (hi - lo + EXP_JP - 1) / EXP_JP - pfirst;
+                if (pfirst == 0) {  // first visit of the segment: warm L2 with its B rows
+                    const __nv_bfloat16 *src = a.pool.B + (size_t)adapter * r_max * d_out + c0;
+                    for (int r = 0; r < k; ++r)
+                        prefetch_l2(src + (size_t)r * d_out, W * 2);
+                }
             }
         }
         const int kp = (k + 3) & ~3;
         const int my_pairs = np > 0 ? (hi - lo - pfirst * EXP_JP) : 0;
-        int4 mine = make_int4(np, np * k * W, my_pairs * kp, my_pairs);
+        const int4 mine = make_int4(np, np * k * W, my_pairs * kp, my_pairs);
         if (tid == 0) {
             s_cutjob = INT_MAX;
             s_cur_s = s_next + EXP_THREADS;
@@ -193,16 +247,16 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
                 const int bo = ex.y + pi * k * W;
                 const int zo = ex.z + pairs_before * kp;
                 const int to = ex.w + pairs_before;
-                const bool fits = job < EXP_MAX_JOBS && bo + k * W <= B_ELEMS &&
-                                  zo + len * kp <= Z_FLOATS && to + len <= WIN_PAIRS;
+                const bool fits = job < EXP_MAX_JOBS && bo + k * W <= B_ELEMS && zo + len * kp <= Z_FLOATS &&
+                                  to + len <= WIN_PAIRS;
                 if (!fits) {
                     atomicMin(&s_cutjob, job);
                     break;
                 }
-                sm.jobA[job] = make_int4(adapter, qs, len, k);
-                sm.jobB[job] = make_int4(bo, zo, to, kp);
+                jobA[job] = make_int4(adapter, qs, len, k);
+                jobB[job] = make_int4(bo, zo, to, kp);
                 for (int i = 0; i < len; ++i)
-                    sm.tok[to + i] = a.m.tok[qs + i];
+                    sTok[to + i] = a.m.tok[qs + i];
                 pairs_before += len;
             }
         }
@@ -219,12 +273,12 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
 
         // ---- stage B tiles (pool data: legal before the dependency wait)
         for (int j = warp; j < njobs; j += NWARP) {
-            const int4 ja = sm.jobA[j];
-            const int bo = sm.jobB[j].x;
+            const int4 ja = jobA[j];
+            const int bo = jobB[j].x;
             const __nv_bfloat16 *src = a.pool.B + (size_t)ja.x * r_max * d_out + c0;
             for (int i = lane; i < ja.w * VPR; i += 32) {
                 const int r = i / VPR, v = i % VPR;
-                cp_async16(&sm.B[bo + r * W + v * 8], src + (size_t)r * d_out + v * 8);
+                cp_async16(&sB[bo + r * W + v * 8], src + (size_t)r * d_out + v * 8);
             }
         }
         if (!waited) {
@@ -232,45 +286,71 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
             waited = true;
         }
         for (int j = warp; j < njobs; j += NWARP) {
-            const int4 ja = sm.jobA[j], jb = sm.jobB[j];
+            const int4 ja = jobA[j], jb = jobB[j];
             const int nv = jb.w >> 2;
             for (int i = lane; i < ja.z * nv; i += 32) {
                 const int r = i / nv, v = i - r * nv;
-                cp_async16(&sm.Z[jb.y + r * jb.w + v * 4], a.m.z + (size_t)(ja.y + r) * a.zs + v * 4);
+                cp_async16(&sZ[jb.y + r * jb.w + v * 4], a.m.z + (size_t)(ja.y + r) * a.zs + v * 4);
             }
         }
         cp_async_commit();
         cp_async_wait_all();
         __syncthreads();
 
-        // ---- accumulate: warp owns tokens (t - t0) % 8 == warp, lane owns W/32 columns
+        // ---- accumulate: warp owns tokens (t - t0) % 8 == warp, lane owns CPL columns
         for (int j = 0; j < njobs; ++j) {
-            const int4 ja = sm.jobA[j], jb = sm.jobB[j];
-            for (int i = 0; i < ja.z; ++i) {
-                const int t = sm.tok[jb.z + i] - t0;
-                if ((t & (NWARP - 1)) != warp)
-                    continue;
-                const float *zr = &sm.Z[jb.y + i * jb.w];
-                if (W == 64) {
-                    const uint32_t *brow = reinterpret_cast<const uint32_t *>(&sm.B[jb.x]) + lane;
-                    float d0 = 0.f, d1 = 0.f;
-                    for (int jj = 0; jj < ja.w; ++jj) {
-                        const uint32_t b = brow[jj * (W / 2)];
-                        const float zz = zr[jj];
-                        d0 = fmaf(zz, bf16lo(b), d0);
-                        d1 = fmaf(zz, bf16hi(b), d1);
+            const int4 ja = jobA[j], jb = jobB[j];
+            bool any = false;
+            for (int i = 0; i < ja.z && !any; ++i)
+                any = ((sTok[jb.z + i] - t0) & (NWARP - 1)) == warp;
+            if (!any)
+                continue;
+            const int kk = ja.w;
+            for (int jc = 0; jc < kk; jc += 16) {
+                // this lane's slice of up to 16 B rows, kept in registers across the pairs
+                float breg[16 * CPL];
+                const int rows = min(16, kk - jc);
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    if (r < rows) {
+                        const __nv_bfloat16 *bp = &sB[jb.x + (jc + r) * W + lane * CPL];
+                        if constexpr (CPL == 1) {
+                            breg[r] = __uint_as_float((uint32_t)__bfloat16_as_ushort(bp[0]) << 16);
+                        } else if constexpr (CPL == 2) {
+                            const uint32_t w = *reinterpret_cast<const uint32_t *>(bp);
+                            breg[2 * r] = bf16lo(w);
+                            breg[2 * r + 1] = bf16hi(w);
+                        } else {
+                            const uint2 w = *reinterpret_cast<const uint2 *>(bp);
+                            breg[4 * r] = bf16lo(w.x);
+                            breg[4 * r + 1] = bf16hi(w.x);
+                            breg[4 * r + 2] = bf16lo(w.y);
+                            breg[4 * r + 3] = bf16hi(w.y);
+                        }
                     }
-                    float2 *ap = reinterpret_cast<float2 *>(&sm.acc[t * W]) + lane;
-                    float2 cur = *ap;
-                    cur.x += d0;
-                    cur.y += d1;
-                    *ap = cur;
-                } else {
-                    const unsigned short *brow = reinterpret_cast<const unsigned short *>(&sm.B[jb.x]) + lane;
-                    float d0 = 0.f;
-                    for (int jj = 0; jj < ja.w; ++jj)
-                        d0 = fmaf(zr[jj], __uint_as_float((uint32_t)brow[jj * W] << 16), d0);
-                    sm.acc[t * W + lane] += d0;
+                }
+                for (int i = 0; i < ja.z; ++i) {
+                    const int t = sTok[jb.z + i] - t0;
+                    if ((t & (NWARP - 1)) != warp)
+                        continue;
+                    const float *zr = &sZ[jb.y + i * jb.w + jc];
+                    float d[CPL];
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c)
+                        d[c] = 0.f;
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        if (r < rows) {
+                            const float zz = zr[r];
+#pragma unroll
+                            for (int c = 0; c < CPL; ++c)
+                                d[c] = fmaf(zz, breg[r * CPL + c], d[c]);
+                        }
+                    }
+                    float *ap = &acc[t * W + lane * CPL];
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c)
+                        ap[c] += d[c];
                 }
             }
         }
@@ -282,55 +362,95 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_expand(ExpandArgs a)
     cp_async_wait_all();
     __syncthreads();
 
-    // ---- y = bf16(y_in + acc), one rounding
-    for (int i = tid; i < nt * VPR; i += EXP_THREADS) {
-        const int t = i / VPR, v = i % VPR;
-        const uint4 yi = *reinterpret_cast<const uint4 *>(&sm.yin[t * W + v * 8]);
-        const float *ac = &sm.acc[t * W + v * 8];
+    // ---- reduce the ng accumulators of the cluster (fixed order), add y, round once
+    if (ng > 1)
+        cluster_sync();
+    for (int i = tid; i < (r1 - r0) * VPR; i += EXP_THREADS) {
+        const int t = r0 + i / VPR, v = i % VPR;
+        const float *ap = &acc[t * W + v * 8];
+        float s[8];
+        if (ng > 1) {
+            const float4 p0 = ld_dsmem_f4(ap, 0), p1 = ld_dsmem_f4(ap + 4, 0);
+            s[0] = p0.x; s[1] = p0.y; s[2] = p0.z; s[3] = p0.w;
+            s[4] = p1.x; s[5] = p1.y; s[6] = p1.z; s[7] = p1.w;
+            for (int gg = 1; gg < ng; ++gg) {
+                const float4 q0 = ld_dsmem_f4(ap, (uint32_t)gg), q1 = ld_dsmem_f4(ap + 4, (uint32_t)gg);
+                s[0] += q0.x; s[1] += q0.y; s[2] += q0.z; s[3] += q0.w;
+                s[4] += q1.x; s[5] += q1.y; s[6] += q1.z; s[7] += q1.w;
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                s[h] = ap[h];
+        }
+        const uint4 yi = *reinterpret_cast<const uint4 *>(&yin[t * W + v * 8]);
         const uint32_t w[4] = {yi.x, yi.y, yi.z, yi.w};
         uint32_t o[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            const __nv_bfloat16 lo = __float2bfloat16_rn(bf16lo(w[h]) + ac[2 * h]);
-            const __nv_bfloat16 hi = __float2bfloat16_rn(bf16hi(w[h]) + ac[2 * h + 1]);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(bf16lo(w[h]) + s[2 * h]);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(bf16hi(w[h]) + s[2 * h + 1]);
             o[h] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
         }
         *reinterpret_cast<uint4 *>(a.y + (size_t)(t0 + t) * d_out + c0 + v * 8) = make_uint4(o[0], o[1], o[2], o[3]);
     }
+    if (ng > 1)
+        cluster_sync();  // keep this CTA's accumulator alive until the cluster has read it
 }
 
-}  // namespace
-
-cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks, const MapDev &m, int T,
-                          int P, int tb, int w, bool pdl, cudaStream_t st)
+template <int W>
+cudaError_t launch_w(const ExpandArgs &a, dim3 grid, size_t smem, bool pdl, cudaStream_t st)
 {
-    const size_t smem = sizeof(Smem);
     static int attr_done = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_expand<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_expand<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaError_t e = cudaFuncSetAttribute(k_expand<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, EXP_SMEM_MAX);
         if (e != cudaSuccess)
             return e;
         attr_done = dev;
     }
-    const int seg_bound = P < pool.capacity ? P : pool.capacity;
-    ExpandArgs a{y, pool, ranks, m, T, tb, z_stride(pool.r_max), seg_bound, pool.capacity <= RANK_TAB_MAX ? 1 : 0};
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((T + tb - 1) / tb, pool.d_out / w, 1);
+    cfg.gridDim = grid;
     cfg.blockDim = dim3(EXP_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = a.ng;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (w == 32)
-        return cudaLaunchKernelEx(&cfg, k_expand<32>, a);
-    return cudaLaunchKernelEx(&cfg, k_expand<64>, a);
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, k_expand<W>, a);
+}
+
+}  // namespace
+
+size_t expand_smem_bytes(int tb, int w, int capacity)
+{
+    return (size_t)ExpLayout(tb, w, capacity <= RANK_TAB_MAX ? capacity : 0).total;
+}
+
+cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks, const MapDev &m, int T,
+                          const ExpandPlan &plan, bool pdl, cudaStream_t st)
+{
+    const int use_tab = pool.capacity <= RANK_TAB_MAX ? 1 : 0;
+    ExpandArgs a{y, pool, ranks, m, T, plan.tb, z_stride(pool.r_max), plan.ng, use_tab};
+    const size_t smem = expand_smem_bytes(plan.tb, plan.w, pool.capacity);
+    const dim3 grid((pool.d_out / plan.w) * plan.ng, (T + plan.tb - 1) / plan.tb, 1);
+    switch (plan.w) {
+    case 32:
+        return launch_w<32>(a, grid, smem, pdl, st);
+    case 64:
+        return launch_w<64>(a, grid, smem, pdl, st);
+    case 128:
+        return launch_w<128>(a, grid, smem, pdl, st);
+    default:
+        return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace tcl

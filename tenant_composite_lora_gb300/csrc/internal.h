@@ -15,18 +15,24 @@ constexpr int SHRINK_TT = 8;
 constexpr int SHRINK_RG = 4;
 constexpr int SHRINK_DC = 2048;      // d_in elements per pipeline entry
 constexpr int SHRINK_THREADS = 256;  // one 16-byte vector of each row per thread and entry
-constexpr int SHRINK_RING_BYTES = 96 * 1024;
+constexpr int SHRINK_RING_BYTES = 72 * 1024;
 constexpr int SHRINK_MAX_INFLIGHT = 8;
 
-// Expand (RowExpand) tile: EXP_W output columns per CTA, token blocks of up
-// to EXP_TB_MAX tokens, jobs of at most EXP_JP pairs of one segment.
-constexpr int EXP_W = 64;
-constexpr int EXP_TB_MAX = 64;
+// Expand (RowExpand) tile: W in {32, 64, 128} output columns x a token block
+// of tb tokens (tb * W <= EXP_TILE_ELEMS) x one of ng segment groups (a
+// cluster); jobs of at most EXP_JP pairs of one segment.
+constexpr int EXP_TILE_ELEMS = 8192;
 constexpr int EXP_JP = 16;
 constexpr int EXP_THREADS = 256;
 constexpr int EXP_MAX_JOBS = 256;
-constexpr int EXP_B_BYTES = 40 * 1024;
-constexpr int EXP_Z_BYTES = 16 * 1024;
+constexpr int EXP_WIN_PAIRS = 1024;
+constexpr int EXP_B_BYTES = 48 * 1024;
+constexpr int EXP_Z_BYTES = 12 * 1024;
+constexpr int EXP_SMEM_MAX = 136 * 1024;
+
+struct ExpandPlan {
+    int tb, w, ng;
+};
 
 constexpr int MAP_THREADS = 1024;
 constexpr int MAP_SMEM_BYTES = 200 * 1024;
@@ -66,7 +72,8 @@ cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int
 // z row stride (floats): r_max rounded up to a multiple of 4 (16-byte rows).
 inline int z_stride(int r_max) { return (r_max + 3) & ~3; }
 cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
-                          const MapDev &m, int T, int P, int tb, int w, bool pdl, cudaStream_t st);
+                          const MapDev &m, int T, const ExpandPlan &plan, bool pdl, cudaStream_t st);
+size_t expand_smem_bytes(int tb, int w, int capacity);
 cudaError_t launch_transpose_bf16(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int rows, int cols,
                                   cudaStream_t st);
 cudaError_t launch_set_int(int32_t *p, int v, cudaStream_t st);

@@ -61,7 +61,7 @@ __device__ __forceinline__ void unpack8(const uint4 w, float f[8])
     f[7] = bf16hi(w.w);
 }
 
-__global__ void __launch_bounds__(SHRINK_THREADS, 1) k_shrink(ShrinkArgs a)
+__global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
 {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     unsigned char *ring = smem_raw;
