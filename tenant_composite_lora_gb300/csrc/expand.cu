@@ -19,8 +19,9 @@
 // Segment ranges are cut into jobs of <= EXP_JP pairs; a window of jobs is
 // staged with 16-byte cp.async copies (the k retained B rows x W columns of
 // each job, the jobs' z rows, their tokens).  On its first visit of a segment
-// the CTA also prefetches that segment's B rows into L2 with bulk prefetches,
-// so windows after the first hit L2.  Warp w owns the block tokens with
+// that is unlikely to fit the first window, the CTA also prefetches that
+// segment's B rows into L2 (per-line prefetches from many threads), so later
+// windows hit L2.  Warp w owns the block tokens with
 // (t - t0) % 8 == w; each lane owns W / 32 columns and keeps its slice of up
 // to 16 B rows in registers while it walks the job's pairs.
 //
@@ -125,9 +126,11 @@ __device__ int4 block_scan4(int4 v, int4 &total, int4 *sh /* [NWARP] */)
                      before.w + inc.w - v.w);
 }
 
-__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes)
+// Per-thread L2 prefetch of the 128-byte line holding p (load/store unit,
+// not the TMA unit: these are many small, independent requests).
+__device__ __forceinline__ void prefetch_line_l2(const void *p)
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -221,10 +224,12 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
             if (hi > lo) {
                 pfirst = (tid == 0) ? piece_next : 0;
                 np = (hi - lo + EXP_JP - 1) / EXP_JP - pfirst;
-                if (pfirst == 0) {  // first visit of the segment: warm L2 with its B rows
+                if (pfirst == 0 && s >= s_next + EXP_PREFETCH_SKIP) {
+                    // later windows: warm L2 with this segment's B rows now
                     const __nv_bfloat16 *src = a.pool.B + (size_t)adapter * r_max * d_out + c0;
                     for (int r = 0; r < k; ++r)
-                        prefetch_l2(src + (size_t)r * d_out, W * 2);
+                        for (int b = 0; b < W * 2; b += 128)
+                            prefetch_line_l2(reinterpret_cast<const char *>(src + (size_t)r * d_out) + b);
                 }
             }
         }
