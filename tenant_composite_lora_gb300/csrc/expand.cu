@@ -50,21 +50,23 @@ struct ExpandArgs {
     const int32_t *ranks;
     MapDev m;
     int T, tb, zs;
+    int w;        // tile width (columns)
     int ng;       // segment groups = cluster size along x
     int use_tab;  // ranks staged in shared memory
 };
 
 // Dynamic shared memory layout (byte offsets), identical on host and device.
 struct ExpLayout {
-    int acc, yin, B, Z, tok, jobA, jobB, rank, total;
+    int yin, B, Z, tok, pjob, plist, jobA, jobB, rank, total;
     __host__ __device__ ExpLayout(int tb, int w, int cap_tab)
     {
-        acc = 0;
-        yin = acc + tb * w * 4;
-        B = (yin + tb * w * 2 + 127) & ~127;
+        yin = 0;
+        B = (yin + tb * w * 2 + 127) & ~127;  // also the fp32 tile (tb * w * 4 <= EXP_B_BYTES) at the end
         Z = B + EXP_B_BYTES;
         tok = Z + EXP_Z_BYTES;
-        jobA = tok + WIN_PAIRS * 4;
+        pjob = tok + WIN_PAIRS * 4;
+        plist = pjob + WIN_PAIRS * 4;
+        jobA = plist + WIN_PAIRS * 4;
         jobB = jobA + EXP_MAX_JOBS * 16;
         rank = jobB + EXP_MAX_JOBS * 16;
         total = rank + ((cap_tab + 3) & ~3) * 4;
@@ -157,15 +159,18 @@ __device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank)
     return v;
 }
 
-template <int W>
+// CPT: columns of the tile owned by one thread (2, 4, 8, 16 or 32); the
+// tile width W and the threads per token TPT = W / CPT are runtime values.
+template <int CPT>
 __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
 {
-    static_assert(W == 32 || W == 64 || W == 128, "tile width");
-    constexpr int VPR = W / 8;   // 16-byte vectors per tile row
-    constexpr int CPL = W / 32;  // columns per lane
+    static_assert(CPT == 2 || CPT == 4 || CPT == 8 || CPT == 16 || CPT == 32, "columns per thread");
+    const int W = a.w;
+    const int VPR = W / 8;  // 16-byte vectors per tile row
+    const int TPT = W / CPT;
     extern __shared__ __align__(128) unsigned char smem_raw[];
     const ExpLayout L(a.tb, W, a.use_tab ? a.pool.capacity : 0);
-    float *acc = reinterpret_cast<float *>(smem_raw + L.acc);
+    float *acc = reinterpret_cast<float *>(smem_raw + L.B);  // reuses the B area after the last window
     __nv_bfloat16 *yin = reinterpret_cast<__nv_bfloat16 *>(smem_raw + L.yin);
     __nv_bfloat16 *sB = reinterpret_cast<__nv_bfloat16 *>(smem_raw + L.B);
     float *sZ = reinterpret_cast<float *>(smem_raw + L.Z);
@@ -173,8 +178,11 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
     int4 *jobA = reinterpret_cast<int4 *>(smem_raw + L.jobA);  // {adapter, q, len, k}
     int4 *jobB = reinterpret_cast<int4 *>(smem_raw + L.jobB);  // {B offset, Z offset, tok offset, kp}
     int *rank_tab = reinterpret_cast<int *>(smem_raw + L.rank);
+    int *pjob = reinterpret_cast<int *>(smem_raw + L.pjob);  // window pair -> job
+    int *plist = reinterpret_cast<int *>(smem_raw + L.plist);  // window pairs grouped by token
     __shared__ int4 s_scan[NWARP];
     __shared__ int s_cutjob, s_cur_s, s_cur_p;
+    __shared__ int s_cnt[EXP_THREADS], s_start[EXP_THREADS], s_cursor[EXP_THREADS];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int d_out = a.pool.d_out, r_max = a.pool.r_max;
@@ -194,9 +202,13 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
     if (a.use_tab)
         for (int i = tid; i < a.pool.capacity; i += EXP_THREADS)
             rank_tab[i] = effective_rank(a.pool, a.ranks, i);
-    for (int i = tid; i < nt * W; i += EXP_THREADS)
-        acc[i] = 0.f;
     const int U = a.m.hdr[HDR_U];
+    // this thread's token and columns, accumulated in registers over all windows
+    const int my_t = tid / TPT, my_c = (tid % TPT) * CPT;
+    float racc[CPT];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c)
+        racc[c] = 0.f;
     const int s_begin = (int)(((long long)U * g) / ng), s_end = (int)(((long long)U * (g + 1)) / ng);
     __syncthreads();
 
@@ -260,8 +272,10 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
                 }
                 jobA[job] = make_int4(adapter, qs, len, k);
                 jobB[job] = make_int4(bo, zo, to, kp);
-                for (int i = 0; i < len; ++i)
+                for (int i = 0; i < len; ++i) {
                     sTok[to + i] = a.m.tok[qs + i];
+                    pjob[to + i] = job;
+                }
                 pairs_before += len;
             }
         }
@@ -302,60 +316,70 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
         cp_async_wait_all();
         __syncthreads();
 
-        // ---- accumulate: warp owns tokens (t - t0) % 8 == warp, lane owns CPL columns
-        for (int j = 0; j < njobs; ++j) {
-            const int4 ja = jobA[j], jb = jobB[j];
-            bool any = false;
-            for (int i = 0; i < ja.z && !any; ++i)
-                any = ((sTok[jb.z + i] - t0) & (NWARP - 1)) == warp;
-            if (!any)
-                continue;
-            const int kk = ja.w;
-            for (int jc = 0; jc < kk; jc += 16) {
-                // this lane's slice of up to 16 B rows, kept in registers across the pairs
-                float breg[16 * CPL];
-                const int rows = min(16, kk - jc);
+        // ---- list the window's pairs per token (stable), then accumulate per token
+        const int npw = njobs > 0 ? jobB[njobs - 1].z + jobA[njobs - 1].z : 0;
+        s_cnt[tid] = 0;
+        __syncthreads();
+        for (int e = tid; e < npw; e += EXP_THREADS)
+            atomicAdd(&s_cnt[sTok[e] - t0], 1);
+        __syncthreads();
+        {
+            int4 tot4;
+            const int4 ex4 = block_scan4(make_int4(s_cnt[tid], 0, 0, 0), tot4, s_scan);
+            s_start[tid] = ex4.x;
+            s_cursor[tid] = ex4.x;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const unsigned lt = (1u << lane) - 1u;
+            for (int base = 0; base < npw; base += 32) {
+                const int e = base + lane;
+                const bool valid = e < npw;
+                const int t = valid ? sTok[e] - t0 : -1 - lane;
+                const unsigned peers = __match_any_sync(0xffffffffu, t);
+                const int cur = valid ? s_cursor[t] : 0;
+                if (valid)
+                    plist[cur + __popc(peers & lt)] = e;
+                __syncwarp();
+                if (valid && lane == __ffs(peers) - 1)
+                    s_cursor[t] = cur + __popc(peers);
+                __syncwarp();
+            }
+        }
+        __syncthreads();
+        if (my_t < nt) {
+            const int i0 = s_start[my_t], i1 = i0 + s_cnt[my_t];
+            for (int idx = i0; idx < i1; ++idx) {
+                const int e = plist[idx];
+                const int j = pjob[e];
+                const int4 ja = jobA[j], jb = jobB[j];
+                const float *zr = &sZ[jb.y + (e - jb.z) * jb.w];
+                const __nv_bfloat16 *bb = &sB[jb.x + my_c];
+                for (int r = 0; r < ja.w; ++r) {
+                    const float zz = zr[r];
+                    const __nv_bfloat16 *br = bb + r * W;
+                    if constexpr (CPT == 2) {
+                        const uint32_t w = *reinterpret_cast<const uint32_t *>(br);
+                        racc[0] = fmaf(zz, bf16lo(w), racc[0]);
+                        racc[1] = fmaf(zz, bf16hi(w), racc[1]);
+                    } else if constexpr (CPT == 4) {
+                        const uint2 w = *reinterpret_cast<const uint2 *>(br);
+                        racc[0] = fmaf(zz, bf16lo(w.x), racc[0]);
+                        racc[1] = fmaf(zz, bf16hi(w.x), racc[1]);
+                        racc[2] = fmaf(zz, bf16lo(w.y), racc[2]);
+                        racc[3] = fmaf(zz, bf16hi(w.y), racc[3]);
+                    } else {
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    if (r < rows) {
-                        const __nv_bfloat16 *bp = &sB[jb.x + (jc + r) * W + lane * CPL];
-                        if constexpr (CPL == 1) {
-                            breg[r] = __uint_as_float((uint32_t)__bfloat16_as_ushort(bp[0]) << 16);
-                        } else if constexpr (CPL == 2) {
-                            const uint32_t w = *reinterpret_cast<const uint32_t *>(bp);
-                            breg[2 * r] = bf16lo(w);
-                            breg[2 * r + 1] = bf16hi(w);
-                        } else {
-                            const uint2 w = *reinterpret_cast<const uint2 *>(bp);
-                            breg[4 * r] = bf16lo(w.x);
-                            breg[4 * r + 1] = bf16hi(w.x);
-                            breg[4 * r + 2] = bf16lo(w.y);
-                            breg[4 * r + 3] = bf16hi(w.y);
+                        for (int v = 0; v < CPT / 8; ++v) {
+                            const uint4 w = *reinterpret_cast<const uint4 *>(br + v * 8);
+                            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                racc[v * 8 + 2 * h] = fmaf(zz, bf16lo(ww[h]), racc[v * 8 + 2 * h]);
+                                racc[v * 8 + 2 * h + 1] = fmaf(zz, bf16hi(ww[h]), racc[v * 8 + 2 * h + 1]);
+                            }
                         }
                     }
-                }
-                for (int i = 0; i < ja.z; ++i) {
-                    const int t = sTok[jb.z + i] - t0;
-                    if ((t & (NWARP - 1)) != warp)
-                        continue;
-                    const float *zr = &sZ[jb.y + i * jb.w + jc];
-                    float d[CPL];
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c)
-                        d[c] = 0.f;
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        if (r < rows) {
-                            const float zz = zr[r];
-#pragma unroll
-                            for (int c = 0; c < CPL; ++c)
-                                d[c] = fmaf(zz, breg[r * CPL + c], d[c]);
-                        }
-                    }
-                    float *ap = &acc[t * W + lane * CPL];
-#pragma unroll
-                    for (int c = 0; c < CPL; ++c)
-                        ap[c] += d[c];
                 }
             }
         }
@@ -365,6 +389,17 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
         __syncthreads();
     }
     cp_async_wait_all();
+    __syncthreads();
+    if (my_t < nt) {
+        if constexpr (CPT == 2) {
+            *reinterpret_cast<float2 *>(&acc[my_t * W + my_c]) = make_float2(racc[0], racc[1]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPT; c += 4)
+                *reinterpret_cast<float4 *>(&acc[my_t * W + my_c + c]) =
+                    make_float4(racc[c], racc[c + 1], racc[c + 2], racc[c + 3]);
+        }
+    }
     __syncthreads();
 
     // ---- reduce the ng accumulators of the cluster (fixed order), add y, round once
@@ -403,14 +438,14 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
         cluster_sync();  // keep this CTA's accumulator alive until the cluster has read it
 }
 
-template <int W>
-cudaError_t launch_w(const ExpandArgs &a, dim3 grid, size_t smem, bool pdl, cudaStream_t st)
+template <int CPT>
+cudaError_t launch_cpt(const ExpandArgs &a, dim3 grid, size_t smem, bool pdl, cudaStream_t st)
 {
     static int attr_done = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_expand<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, EXP_SMEM_MAX);
+        cudaError_t e = cudaFuncSetAttribute(k_expand<CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, EXP_SMEM_MAX);
         if (e != cudaSuccess)
             return e;
         attr_done = dev;
@@ -429,7 +464,7 @@ cudaError_t launch_w(const ExpandArgs &a, dim3 grid, size_t smem, bool pdl, cuda
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_expand<W>, a);
+    return cudaLaunchKernelEx(&cfg, k_expand<CPT>, a);
 }
 
 }  // namespace
@@ -439,20 +474,36 @@ size_t expand_smem_bytes(int tb, int w, int capacity)
     return (size_t)ExpLayout(tb, w, capacity <= RANK_TAB_MAX ? capacity : 0).total;
 }
 
+// Columns per thread for a tb x w tile over EXP_THREADS threads (power of two,
+// 2..32).  Exposed so that host code and tests agree with the kernel.
+int expand_cpt(int tb, int w)
+{
+    int cpt = 2;
+    while (cpt < 32 && (long long)tb * w > (long long)cpt * EXP_THREADS)
+        cpt *= 2;
+    while (w / cpt > EXP_THREADS)
+        cpt *= 2;
+    return cpt;
+}
+
 cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks, const MapDev &m, int T,
                           const ExpandPlan &plan, bool pdl, cudaStream_t st)
 {
     const int use_tab = pool.capacity <= RANK_TAB_MAX ? 1 : 0;
-    ExpandArgs a{y, pool, ranks, m, T, plan.tb, z_stride(pool.r_max), plan.ng, use_tab};
+    ExpandArgs a{y, pool, ranks, m, T, plan.tb, z_stride(pool.r_max), plan.w, plan.ng, use_tab};
     const size_t smem = expand_smem_bytes(plan.tb, plan.w, pool.capacity);
     const dim3 grid((pool.d_out / plan.w) * plan.ng, (T + plan.tb - 1) / plan.tb, 1);
-    switch (plan.w) {
+    switch (expand_cpt(plan.tb, plan.w)) {
+    case 2:
+        return launch_cpt<2>(a, grid, smem, pdl, st);
+    case 4:
+        return launch_cpt<4>(a, grid, smem, pdl, st);
+    case 8:
+        return launch_cpt<8>(a, grid, smem, pdl, st);
+    case 16:
+        return launch_cpt<16>(a, grid, smem, pdl, st);
     case 32:
-        return launch_w<32>(a, grid, smem, pdl, st);
-    case 64:
-        return launch_w<64>(a, grid, smem, pdl, st);
-    case 128:
-        return launch_w<128>(a, grid, smem, pdl, st);
+        return launch_cpt<32>(a, grid, smem, pdl, st);
     default:
         return cudaErrorInvalidValue;
     }

@@ -13,9 +13,9 @@ namespace tcl {
 // SHRINK_RG retained-rank rows per work unit.
 constexpr int SHRINK_TT = 8;
 constexpr int SHRINK_RG = 4;
-constexpr int SHRINK_DC = 2048;      // d_in elements per pipeline entry
-constexpr int SHRINK_THREADS = 256;  // one 16-byte vector of each row per thread and entry
-constexpr int SHRINK_RING_BYTES = 72 * 1024;
+constexpr int SHRINK_THREADS = 256;
+constexpr int SHRINK_ENTRY_BYTES = 48 * 1024;  // largest (unit, d_in chunk) entry
+constexpr int SHRINK_RING_BYTES = 96 * 1024;
 constexpr int SHRINK_MAX_INFLIGHT = 8;
 
 // Expand (RowExpand) tile: W in {32, 64, 128} output columns x a token block
@@ -76,6 +76,7 @@ inline int z_stride(int r_max) { return (r_max + 3) & ~3; }
 cudaError_t launch_expand(__nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
                           const MapDev &m, int T, const ExpandPlan &plan, bool pdl, cudaStream_t st);
 size_t expand_smem_bytes(int tb, int w, int capacity);
+int expand_cpt(int tb, int w);
 cudaError_t launch_transpose_bf16(const __nv_bfloat16 *src, __nv_bfloat16 *dst, int rows, int cols,
                                   cudaStream_t st);
 cudaError_t launch_set_int(int32_t *p, int v, cudaStream_t st);

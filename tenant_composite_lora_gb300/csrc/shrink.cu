@@ -9,7 +9,9 @@
 // page, "Core idea", paper Sec. 3.1 M1).
 //
 // Work unit = (segment tile of <= SHRINK_TT pairs of one adapter, group of <=
-// SHRINK_RG retained rows).  Units are numbered rowgroup-major over the
+// SHRINK_RG retained rows); a unit is streamed as one or more entries (d_in
+// chunks sized so the unit's rows of a chunk fit SHRINK_ENTRY_BYTES; whole
+// rows when they fit, so a unit's A rows are a single copy).  Units are numbered rowgroup-major over the
 // host-known tile bound, so a CTA resolves its units with one round trip
 // (tile record and its token list, same index) and the retained ranks come
 // from a table staged in shared memory.  The pool stores A transposed
@@ -32,11 +34,12 @@ namespace tcl {
 
 namespace {
 
-constexpr int TT = SHRINK_TT, RG = SHRINK_RG, DC = SHRINK_DC;
-constexpr int RING = SHRINK_RING_BYTES, MAXE = SHRINK_MAX_INFLIGHT;
+constexpr int TT = SHRINK_TT, RG = SHRINK_RG;
+constexpr int RING = SHRINK_RING_BYTES, MAXE = SHRINK_MAX_INFLIGHT, EMAX = SHRINK_ENTRY_BYTES;
 constexpr int MAX_LIST = SHRINK_THREADS;
 static_assert(TT * RG == 32, "one reduced value per lane");
-static_assert((RG + TT) * DC * 2 <= RING, "one entry of any shape fits the empty ring");
+static_assert(EMAX <= RING, "one entry of any shape fits the empty ring");
+static_assert((RG + TT) * 64 * 2 <= EMAX, "a 64-element chunk of any unit fits an entry");
 
 struct ShrinkArgs {
     const __nv_bfloat16 *x;
@@ -71,6 +74,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
     __shared__ float red[2][8][32];
     __shared__ int4 s_unit[MAX_LIST];  // {adapter, q0, n, (j0 << 8) | R}
     __shared__ int s_tok[MAX_LIST][TT];
+    __shared__ short s_clen[MAX_LIST];  // d_in chunk of the unit's entries (multiple of 64)
     __shared__ int s_wcount[8];
 
     pdl_launch_dependents();
@@ -80,7 +84,6 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
     int32_t *status = a.m.hdr + HDR_STATUS;
     const int rgm = (r_max + a.rg - 1) / a.rg;
     const long long nunits = (long long)a.tile_bound * rgm;
-    const int nch = (d_in + DC - 1) / DC;
 
     if (a.use_tab)
         for (int i = tid; i < a.pool.capacity; i += SHRINK_THREADS)
@@ -131,27 +134,40 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
             before += (w < warp) ? s_wcount[w] : 0;
             L += s_wcount[w];
         }
+        int my_nch = 0;
         if (live) {
             const int idx = before + __popc(bal & ((1u << lane) - 1u));
             s_unit[idx] = rec;
 #pragma unroll
             for (int i = 0; i < TT; ++i)
                 s_tok[idx][i] = toks[i];
+            // longest chunk (multiple of 64 elements) whose rows fit one entry
+            const int rows = (rec.w & 0xff) + rec.z;
+            const int clen = min(d_in, (EMAX / (2 * rows)) & ~63);
+            s_clen[idx] = (short)clen;
+            my_nch = (d_in + clen - 1) / clen;
         }
         __syncthreads();
+        // entries of this pass = sum over units of their chunk counts
+        const unsigned nb = __reduce_add_sync(0xffffffffu, (unsigned)my_nch);
+        if (lane == 0)
+            s_wcount[warp] = (int)nb;
+        __syncthreads();
+        int total = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            total += s_wcount[w];
 
-        // ---- entries = L units x nch chunks through the byte ring
-        const int total = L * nch;
-        // producer state, used by thread 0 only
-        int p_next = 0, head = 0;
-        auto entry_bytes = [&](int c) -> int {
-            const int4 r = s_unit[c / nch];
-            const int clen = min(DC, d_in - (c % nch) * DC);
-            return ((r.w & 0xff) + r.z) * clen * 2;
-        };
+        // ---- entries (unit, chunk) in order through the byte ring
+        // producer state (thread 0 only): next entry, its unit and chunk, ring head
+        int p_next = 0, p_e = 0, p_ch = 0, head = 0;
         auto issue_more = [&](int c_done) {
             while (p_next < total && p_next - c_done < MAXE) {
-                const int size = entry_bytes(p_next);
+                const int4 r = s_unit[p_e];
+                const int n = r.z, R = r.w & 0xff, j0 = r.w >> 8;
+                const int clen_u = s_clen[p_e];
+                const int c0 = p_ch * clen_u, clen = min(clen_u, d_in - c0);
+                const int size = (R + n) * clen * 2;
                 int pos;
                 if (p_next == c_done) {
                     pos = 0;  // ring empty
@@ -173,34 +189,50 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
                 }
                 const int slot = (e_base + p_next) % MAXE;
                 e_off[slot] = pos;
-                const int e = p_next / nch, ch = p_next % nch;
-                const int4 r = s_unit[e];
-                const int n = r.z, R = r.w & 0xff, j0 = r.w >> 8;
-                const int c0 = ch * DC, clen = min(DC, d_in - c0);
                 const uint32_t row_bytes = (uint32_t)clen * 2u;
                 unsigned char *dst = ring + pos;
                 mbar_arrive_expect_tx(&bar[slot], row_bytes * (uint32_t)(R + n));
                 const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
-                for (int rr = 0; rr < R; ++rr)
-                    bulk_g2s(dst + rr * row_bytes, Abase + (size_t)rr * d_in, row_bytes, &bar[slot]);
+                if (clen == d_in) {  // whole rows: the unit's A rows are one contiguous run
+                    bulk_g2s(dst, Abase, row_bytes * (uint32_t)R, &bar[slot]);
+                } else {
+                    for (int rr = 0; rr < R; ++rr)
+                        bulk_g2s(dst + rr * row_bytes, Abase + (size_t)rr * d_in, row_bytes, &bar[slot]);
+                }
                 for (int i = 0; i < n; ++i)
-                    bulk_g2s(dst + (R + i) * row_bytes, a.x + (size_t)s_tok[e][i] * d_in + c0, row_bytes,
+                    bulk_g2s(dst + (R + i) * row_bytes, a.x + (size_t)s_tok[p_e][i] * d_in + c0, row_bytes,
                              &bar[slot]);
                 head = pos + size;
                 ++p_next;
+                if (c0 + clen >= d_in) {
+                    ++p_e;
+                    p_ch = 0;
+                } else {
+                    ++p_ch;
+                }
             }
         };
         if (tid == 0)
             issue_more(0);
 
         float acc[TT][RG];
+        int c_e = 0, c_ch = 0;  // consumer: unit and chunk of entry c
         for (int c = 0; c < total; ++c) {
             const uint32_t g = e_base + c;
             const int slot = g % MAXE;
             const bool ok = mbar_wait_bounded(&bar[slot], (g / MAXE) & 1u, status);
-            const int e = c / nch, ch = c % nch;
+            const int e = c_e, ch = c_ch;
             const int4 r = s_unit[e];
             const int n = r.z, R = r.w & 0xff;
+            const int clen_u = s_clen[e];
+            const int clen = min(clen_u, d_in - ch * clen_u);
+            const bool last = (ch * clen_u + clen >= d_in);
+            if (last) {
+                ++c_e;
+                c_ch = 0;
+            } else {
+                ++c_ch;
+            }
             if (ch == 0) {
 #pragma unroll
                 for (int i = 0; i < TT; ++i)
@@ -208,19 +240,18 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
                     for (int rr = 0; rr < RG; ++rr)
                         acc[i][rr] = 0.f;
             }
-            const int clen = min(DC, d_in - ch * DC);
             const __nv_bfloat16 *sA = reinterpret_cast<const __nv_bfloat16 *>(ring + e_off[slot]);
-            if (ok && tid * 8 < clen) {
+            for (int vb = tid * 8; ok && vb < clen; vb += SHRINK_THREADS * 8) {
                 float av[RG][8];
 #pragma unroll
                 for (int rr = 0; rr < RG; ++rr)
                     if (rr < R)
-                        unpack8(lds128(sA + rr * clen + tid * 8), av[rr]);
+                        unpack8(lds128(sA + rr * clen + vb), av[rr]);
 #pragma unroll
                 for (int i = 0; i < TT; ++i) {
                     if (i < n) {
                         float xv[8];
-                        unpack8(lds128(sA + (R + i) * clen + tid * 8), xv);
+                        unpack8(lds128(sA + (R + i) * clen + vb), xv);
 #pragma unroll
                         for (int rr = 0; rr < RG; ++rr) {
                             if (rr < R) {
@@ -234,7 +265,6 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
                     }
                 }
             }
-            const bool last = (ch == nch - 1);
             if (last) {
                 // reduce-scatter: lane l ends with the warp sum of value l = i * RG + r
                 float v[32];
