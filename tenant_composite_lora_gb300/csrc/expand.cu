@@ -42,7 +42,8 @@ constexpr int NWARP = EXP_THREADS / 32;
 constexpr int B_ELEMS = EXP_B_BYTES / 2;
 constexpr int Z_FLOATS = EXP_Z_BYTES / 4;
 constexpr int WIN_PAIRS = EXP_WIN_PAIRS;
-static_assert(NWARP == 8, "warp owns tokens mod 8");
+static_assert(NWARP == 8, "eight warps per CTA");
+static_assert(EXP_JP <= 32, "one lane per pair of a job");
 
 struct ExpandArgs {
     __nv_bfloat16 *y;
@@ -128,12 +129,6 @@ __device__ int4 block_scan4(int4 v, int4 &total, int4 *sh /* [NWARP] */)
                      before.w + inc.w - v.w);
 }
 
-// Per-thread L2 prefetch of the 128-byte line holding p (load/store unit,
-// not the TMA unit: these are many small, independent requests).
-__device__ __forceinline__ void prefetch_line_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
-}
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
@@ -236,13 +231,6 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
             if (hi > lo) {
                 pfirst = (tid == 0) ? piece_next : 0;
                 np = (hi - lo + EXP_JP - 1) / EXP_JP - pfirst;
-                if (pfirst == 0 && s >= s_next + EXP_PREFETCH_SKIP) {
-                    // later windows: warm L2 with this segment's B rows now
-                    const __nv_bfloat16 *src = a.pool.B + (size_t)adapter * r_max * d_out + c0;
-                    for (int r = 0; r < k; ++r)
-                        for (int b = 0; b < W * 2; b += 128)
-                            prefetch_line_l2(reinterpret_cast<const char *>(src + (size_t)r * d_out) + b);
-                }
             }
         }
         const int kp = (k + 3) & ~3;
@@ -272,10 +260,6 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
                 }
                 jobA[job] = make_int4(adapter, qs, len, k);
                 jobB[job] = make_int4(bo, zo, to, kp);
-                for (int i = 0; i < len; ++i) {
-                    sTok[to + i] = a.m.tok[qs + i];
-                    pjob[to + i] = job;
-                }
                 pairs_before += len;
             }
         }
@@ -290,6 +274,15 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
                 }
         }
 
+        // ---- tokens of the window's pairs (mapping data), one lane per pair
+        for (int j = warp; j < njobs; j += NWARP) {
+            const int4 ja = jobA[j];
+            const int to = jobB[j].z;
+            if (lane < ja.z) {
+                sTok[to + lane] = a.m.tok[ja.y + lane];
+                pjob[to + lane] = j;
+            }
+        }
         // ---- stage B tiles (pool data: legal before the dependency wait)
         for (int j = warp; j < njobs; j += NWARP) {
             const int4 ja = jobA[j];
@@ -300,26 +293,10 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
                 cp_async16(&sB[bo + r * W + v * 8], src + (size_t)r * d_out + v * 8);
             }
         }
-        if (!waited) {
-            pdl_wait();  // z comes from the shrink kernel
-            waited = true;
-        }
-        for (int j = warp; j < njobs; j += NWARP) {
-            const int4 ja = jobA[j], jb = jobB[j];
-            const int nv = jb.w >> 2;
-            for (int i = lane; i < ja.z * nv; i += 32) {
-                const int r = i / nv, v = i - r * nv;
-                cp_async16(&sZ[jb.y + r * jb.w + v * 4], a.m.z + (size_t)(ja.y + r) * a.zs + v * 4);
-            }
-        }
-        cp_async_commit();
-        cp_async_wait_all();
-        __syncthreads();
-
-        // ---- list the window's pairs per token (stable), then accumulate per token
+        // ---- list the window's pairs per token (stable, window order kept)
         const int npw = njobs > 0 ? jobB[njobs - 1].z + jobA[njobs - 1].z : 0;
         s_cnt[tid] = 0;
-        __syncthreads();
+        __syncthreads();  // also publishes the tokens staged above
         for (int e = tid; e < npw; e += EXP_THREADS)
             atomicAdd(&s_cnt[sTok[e] - t0], 1);
         __syncthreads();
@@ -347,6 +324,23 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
             }
         }
         __syncthreads();
+        if (!waited) {
+            pdl_wait();  // z comes from the shrink kernel
+            waited = true;
+        }
+        for (int j = warp; j < njobs; j += NWARP) {
+            const int4 ja = jobA[j], jb = jobB[j];
+            const int nv = jb.w >> 2;
+            for (int i = lane; i < ja.z * nv; i += 32) {
+                const int r = i / nv, v = i - r * nv;
+                cp_async16(&sZ[jb.y + r * jb.w + v * 4], a.m.z + (size_t)(ja.y + r) * a.zs + v * 4);
+            }
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        __syncthreads();
+
+        // ---- accumulate this thread's token over its pairs of the window
         if (my_t < nt) {
             const int i0 = s_start[my_t], i1 = i0 + s_cnt[my_t];
             for (int idx = i0; idx < i1; ++idx) {
@@ -446,6 +440,9 @@ cudaError_t launch_cpt(const ExpandArgs &a, dim3 grid, size_t smem, bool pdl, cu
     cudaGetDevice(&dev);
     if (attr_done != dev) {
         cudaError_t e = cudaFuncSetAttribute(k_expand<CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, EXP_SMEM_MAX);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_expand<CPT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         attr_done = dev;

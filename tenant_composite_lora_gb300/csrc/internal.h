@@ -5,7 +5,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include "../../include/lora.h"
+#include "lora.h"
 
 namespace tcl {
 
@@ -29,8 +29,6 @@ constexpr int EXP_WIN_PAIRS = 1024;
 constexpr int EXP_B_BYTES = 48 * 1024;
 constexpr int EXP_Z_BYTES = 12 * 1024;
 constexpr int EXP_SMEM_MAX = 136 * 1024;
-// Segments of a window beyond this index get an early L2 prefetch of B.
-constexpr int EXP_PREFETCH_SKIP = 16;
 
 struct ExpandPlan {
     int tb, w, ng;

@@ -15,11 +15,13 @@
 // host-known tile bound, so a CTA resolves its units with one round trip
 // (tile record and its token list, same index) and the retained ranks come
 // from a table staged in shared memory.  The pool stores A transposed
-// (r_max x d_in): a unit's rows are 16-byte-aligned contiguous runs that one
-// thread streams with bulk (TMA) copies into a byte ring in shared memory,
-// each entry (unit, d_in chunk) completing on its own mbarrier; entries are
-// issued as long as ring space and barrier slots allow, so every byte a CTA
-// needs is in flight from the start when it fits.  Each thread owns one
+// (r_max x d_in): a unit's rows are 16-byte-aligned contiguous runs that all
+// threads stream with 16-byte asynchronous copies into a byte ring in shared
+// memory, each entry (unit, d_in chunk) completing on its own mbarrier
+// (cp.async.mbarrier.arrive); entries are issued as long as ring space and
+// barrier slots allow, so every byte a CTA needs is in flight from the start
+// when it fits.  (One thread issuing a bulk copy per row was measured to
+// serialise on the copy engine: ~0.2 us per copy.)  Each thread owns one
 // 16-byte vector of every staged row, accumulates SHRINK_TT x SHRINK_RG fp32
 // partial dot products, and the CTA reduces them with a warp-shuffle
 // reduce-scatter (32 values over 32 lanes in 31 shuffles) and one cross-warp
@@ -70,7 +72,6 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
     unsigned char *ring = smem_raw;
     int *rank_tab = reinterpret_cast<int *>(smem_raw + RING);
     __shared__ __align__(8) uint64_t bar[MAXE];
-    __shared__ int e_off[MAXE];
     __shared__ float red[2][8][32];
     __shared__ int4 s_unit[MAX_LIST];  // {adapter, q0, n, (j0 << 8) | R}
     __shared__ int s_tok[MAX_LIST][TT];
@@ -90,7 +91,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
             rank_tab[i] = effective_rank(a.pool, a.ranks, i);
     if (tid == 0) {
         for (int s = 0; s < MAXE; ++s)
-            mbar_init(&bar[s], 1);
+            mbar_init(&bar[s], SHRINK_THREADS);
         fence_mbar_init();
     }
     __syncthreads();
@@ -158,8 +159,11 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
         for (int w = 0; w < 8; ++w)
             total += s_wcount[w];
 
-        // ---- entries (unit, chunk) in order through the byte ring
-        // producer state (thread 0 only): next entry, its unit and chunk, ring head
+        // ---- entries (unit, chunk) in order through the byte ring.  Every thread
+        // runs the same allocation (uniform state) and issues its share of each
+        // entry's 16-byte copies; the entry's mbarrier completes when all
+        // threads' copies have landed.
+        int my_off[MAXE];  // ring offset of the entries in flight, by slot
         int p_next = 0, p_e = 0, p_ch = 0, head = 0;
         auto issue_more = [&](int c_done) {
             while (p_next < total && p_next - c_done < MAXE) {
@@ -172,7 +176,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
                 if (p_next == c_done) {
                     pos = 0;  // ring empty
                 } else {
-                    const int tail = e_off[(e_base + c_done) % MAXE];
+                    const int tail = my_off[(e_base + c_done) % MAXE];
                     if (head > tail) {
                         if (head + size <= RING)
                             pos = head;
@@ -188,20 +192,18 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
                     }
                 }
                 const int slot = (e_base + p_next) % MAXE;
-                e_off[slot] = pos;
-                const uint32_t row_bytes = (uint32_t)clen * 2u;
+                my_off[slot] = pos;
+                const int vpr = clen / 8;  // 16-byte vectors per row
+                const int nvec = (R + n) * vpr;
                 unsigned char *dst = ring + pos;
-                mbar_arrive_expect_tx(&bar[slot], row_bytes * (uint32_t)(R + n));
                 const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
-                if (clen == d_in) {  // whole rows: the unit's A rows are one contiguous run
-                    bulk_g2s(dst, Abase, row_bytes * (uint32_t)R, &bar[slot]);
-                } else {
-                    for (int rr = 0; rr < R; ++rr)
-                        bulk_g2s(dst + rr * row_bytes, Abase + (size_t)rr * d_in, row_bytes, &bar[slot]);
+                for (int v = tid; v < nvec; v += SHRINK_THREADS) {
+                    const int row = v / vpr, cv = v - row * vpr;
+                    const __nv_bfloat16 *src = row < R ? Abase + (size_t)row * d_in + cv * 8
+                                                       : a.x + (size_t)s_tok[p_e][row - R] * d_in + c0 + cv * 8;
+                    cp_async16(dst + (size_t)v * 16, src);
                 }
-                for (int i = 0; i < n; ++i)
-                    bulk_g2s(dst + (R + i) * row_bytes, a.x + (size_t)s_tok[p_e][i] * d_in + c0, row_bytes,
-                             &bar[slot]);
+                cp_async_mbar_arrive(&bar[slot]);
                 head = pos + size;
                 ++p_next;
                 if (c0 + clen >= d_in) {
@@ -212,8 +214,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
                 }
             }
         };
-        if (tid == 0)
-            issue_more(0);
+        issue_more(0);
 
         float acc[TT][RG];
         int c_e = 0, c_ch = 0;  // consumer: unit and chunk of entry c
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
                     for (int rr = 0; rr < RG; ++rr)
                         acc[i][rr] = 0.f;
             }
-            const __nv_bfloat16 *sA = reinterpret_cast<const __nv_bfloat16 *>(ring + e_off[slot]);
+            const __nv_bfloat16 *sA = reinterpret_cast<const __nv_bfloat16 *>(ring + my_off[slot]);
             for (int vb = tid * 8; ok && vb < clen; vb += SHRINK_THREADS * 8) {
                 float av[RG][8];
 #pragma unroll
@@ -288,8 +289,7 @@ __global__ void __launch_bounds__(SHRINK_THREADS, 2) k_shrink(ShrinkArgs a)
             const int any_bad = __syncthreads_or(!ok);
             if (any_bad)
                 return;  // a copy never landed: the status word records it
-            if (tid == 0)
-                issue_more(c + 1);
+            issue_more(c + 1);
             if (last) {
                 if (warp == 0) {
                     float s = 0.f;
@@ -323,6 +323,10 @@ cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int
     if (attr_done != dev) {
         cudaError_t e = cudaFuncSetAttribute(k_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              RING + RANK_TAB_MAX * (int)sizeof(int));
+        // the largest shared-memory carveout, so an expand CTA fits beside this one
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_shrink, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         attr_done = dev;
