@@ -172,10 +172,12 @@ def bench_ours(args, rank, world, dist):
         def step(rep):
             native.lora_build_mapping(rep["mapping"].handle, rep["off"], rep["ids"], rep["alpha"],
                                       wl.T, wl.P, stream)
-            native.lora_delta_apply(rep["x"], rep["y"], rep["pool"].handle, None, rep["mapping"].handle, stream)
+            native.lora_delta_apply_path(rep["x"], rep["y"], rep["pool"].handle, None, rep["mapping"].handle,
+                                         args.path_id, stream)
 
         def apply_only(rep):
-            native.lora_delta_apply(rep["x"], rep["y"], rep["pool"].handle, None, rep["mapping"].handle, stream)
+            native.lora_delta_apply_path(rep["x"], rep["y"], rep["pool"].handle, None, rep["mapping"].handle,
+                                         args.path_id, stream)
 
         # correctness spot check of replica 0 (one step from y0)
         reps[0]["y"].copy_(reps[0]["y0"])
@@ -275,6 +277,7 @@ def bench_ours(args, rank, world, dist):
             "T": wl.T, "P": wl.P, "d_in": wl.d_in, "d_out": wl.d_out, "r_max": wl.r_max,
             "pool": wl.capacity, "distinct_adapters": ab["U"], "sum_k": ab["sum_k"],
             "step": "lora_build_mapping + lora_delta_apply",
+            "path": args.path,
             "l2_protocol": f"inputs larger than L2: {R} rotating replicas, {R * ab['total'] / 1e6:.0f} MB "
                            f"touched per pass vs {l2 / 1e6:.0f} MB L2",
             "parallelism": "replicas only" if world > 1 else "single GPU",
@@ -324,7 +327,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--max-replicas", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "split", "fused", "mma"],
+                    help="force an execution path (default: the library's dispatch table)")
     args = ap.parse_args()
+    args.path_id = {"auto": 0, "split": 1, "fused": 2, "mma": 3}[args.path]
     args.warmup = max(3, args.warmup)
     rank, world, dist = dist_setup(args.gpus)
 

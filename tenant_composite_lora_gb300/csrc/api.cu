@@ -119,7 +119,7 @@ void free_mapping(lora_mapping *m)
 {
     MapDev &d = m->dev;
     void *ptrs[] = {d.tok, d.adapter, d.src, d.pos, d.alpha, d.seg_adapter, d.seg_start, d.tile, d.tile_tok,
-                    d.tmp_tok, d.hdr, d.z, m->sx, m->sy, m->soff, m->sids, m->salpha};
+                    d.tmp_tok, d.hdr, d.z, d.partial, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -133,8 +133,8 @@ int choose_path(int T, int P, int r_max, int d_in, int d_out)
     (void)P;
     (void)r_max;
     (void)d_in;
-    (void)d_out;
-    (void)T;
+    if (fused_supported(T, d_out))
+        return LORA_PATH_FUSED;  // decode: one launch
     return LORA_PATH_SPLIT;
 }
 
@@ -176,13 +176,26 @@ ExpandPlan choose_expand_plan(int T, int d_out)
     return best;
 }
 
+lora_status run_fused(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
+                      cudaStream_t st)
+{
+    if (!fused_supported(m->T, pool->d_out))
+        return LORA_ERR_NOT_SUPPORTED;
+    const ExpandPlan plan = choose_expand_plan(m->T, pool->d_out);
+    const cudaError_t e = launch_fused(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
+                                       pool_dev(pool), ranks, m->dev, m->T, m->P, plan, sm_count(), st);
+    if (e == cudaErrorInvalidValue)
+        return LORA_ERR_NOT_SUPPORTED;
+    return from_cuda(e);
+}
+
 lora_status run_split(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
                       cudaStream_t st)
 {
     const PoolDev pd = pool_dev(pool);
     const int grid = sm_count();
     cudaError_t e =
-        launch_shrink(static_cast<const __nv_bfloat16 *>(x), pd, ranks, m->dev, m->P, SHRINK_RG, grid, st);
+        launch_shrink(static_cast<const __nv_bfloat16 *>(x), pd, ranks, m->dev, m->P, grid, st);
     if (e != cudaSuccess)
         return from_cuda(e);
     const ExpandPlan plan = choose_expand_plan(m->T, pool->d_out);
@@ -334,6 +347,8 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.tmp_tok, P);
     if (e == cudaSuccess) e = dalloc(&d.hdr, (size_t)HDR_WORDS);
     if (e == cudaSuccess) e = dalloc(&d.z, P * LORA_MAX_RANK);
+    d.partial_ctas = sm_count();
+    if (e == cudaSuccess) e = dalloc(&d.partial, (size_t)d.partial_ctas * EXP_TILE_ELEMS);
     if (e == cudaSuccess) e = cudaMemset(d.hdr, 0, HDR_WORDS * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(d.seg_start, 0, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -379,6 +394,8 @@ lora_status lora_delta_apply_path(const void *x_dev, void *y_dev, const lora_poo
     switch (path) {
     case LORA_PATH_SPLIT:
         return run_split(x_dev, y_dev, pool, ranks_dev, m, st);
+    case LORA_PATH_FUSED:
+        return run_fused(x_dev, y_dev, pool, ranks_dev, m, st);
     default:
         return LORA_ERR_NOT_SUPPORTED;
     }

@@ -9,13 +9,12 @@
 
 namespace tcl {
 
-// Shrink tile: at most SHRINK_TT pairs (tokens) of one adapter segment and
-// SHRINK_RG retained-rank rows per work unit.
+// Shrink tile: at most SHRINK_TT pairs (tokens) of one adapter segment.
 constexpr int SHRINK_TT = 8;
-constexpr int SHRINK_RG = 4;
 constexpr int SHRINK_THREADS = 256;
-constexpr int SHRINK_ENTRY_BYTES = 48 * 1024;  // largest (unit, d_in chunk) entry
-constexpr int SHRINK_RING_BYTES = 96 * 1024;
+constexpr int SHRINK_RING_BYTES = 64 * 1024;   // split path (beside an expand CTA)
+constexpr int SHRINK_MIN_ENTRY = 12 * 64 * 2;  // a 64-element chunk of the largest unit
+constexpr int SHRINK_ROUND_TILES = 2048;       // tile records scanned per round
 constexpr int SHRINK_MAX_INFLIGHT = 8;
 
 // Expand (RowExpand) tile: W in {32, 64, 128} output columns x a token block
@@ -42,7 +41,14 @@ constexpr int MAP_SMEM_BYTES = 200 * 1024;
 constexpr int RANK_TAB_MAX = 2048;
 
 // Header words of the mapping (device int32).
-enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_WORDS = 8 };
+// HDR_BAR, HDR_BAR_BASE, HDR_EXIT: grid-barrier counters of the fused kernel.
+enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_BAR = 5, HDR_BAR_BASE = 6,
+       HDR_EXIT = 7, HDR_WORDS = 8 };
+
+// Fused decode kernel: one CTA per SM; dynamic shared memory = the expand
+// layout + an entry ring of at most FUSED_RING_MAX bytes.
+constexpr int FUSED_SMEM_MAX = 184 * 1024;  // + ~42 KB static <= 227 KB
+constexpr int FUSED_RING_MAX = 96 * 1024;
 
 struct PoolDev {
     const __nv_bfloat16 *At;  // [capacity][r_max][d_in]
@@ -60,6 +66,8 @@ struct MapDev {
     int32_t *tmp_tok;                    // [max_pairs] scratch
     int32_t *hdr;                        // [HDR_WORDS]
     float *z;                            // [max_pairs][LORA_MAX_RANK] shrink output
+    float *partial;                      // [partial_ctas][EXP_TILE_ELEMS] fused-kernel tiles
+    int partial_ctas;
 };
 
 // Launchers (each returns cudaGetLastError()).
@@ -67,7 +75,7 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
                                  const float *alpha, int T, int P, int capacity, int max_pairs,
                                  cudaStream_t st);
 cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int32_t *ranks,
-                          const MapDev &m, int P, int rg, int grid, cudaStream_t st);
+                          const MapDev &m, int P, int grid, cudaStream_t st);
 
 // z row stride (floats): r_max rounded up to a multiple of 4 (16-byte rows).
 inline int z_stride(int r_max) { return (r_max + 3) & ~3; }
@@ -84,5 +92,9 @@ int sm_count();
 // Upper bound of the number of shrink tiles of P pairs over `capacity` ids
 // (host-computable; the mapping fills unused tile slots with empty records).
 int shrink_tile_bound(int P, int capacity);
+
+bool fused_supported(int T, int d_out);
+cudaError_t launch_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
+                         const MapDev &m, int T, int P, const ExpandPlan &plan, int grid, cudaStream_t st);
 
 }  // namespace tcl

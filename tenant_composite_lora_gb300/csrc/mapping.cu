@@ -134,8 +134,12 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
     int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
     for (int i = tid; i < nw * cap; i += MAP_THREADS)
         hist[i] = 0;
-    if (tid == 0)
+    if (tid == 0) {
         m.hdr[HDR_STATUS] = 0;
+        m.hdr[HDR_BAR] = 0;  // fused-kernel barrier counters start over with every mapping
+        m.hdr[HDR_BAR_BASE] = 0;
+        m.hdr[HDR_EXIT] = 0;
+    }
     __syncthreads();
 
     // 1. CSR check

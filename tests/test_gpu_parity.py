@@ -125,6 +125,8 @@ def test_mapping_bad_offsets_and_degenerate():
 
 # ---------------------------------------------------------------- delta, element-wise
 APPLY_CASES = ["tiny", "distinct", "zipf", "sweep1", "sweep8", "sweep64", "sweep256"]
+PATH_AUTO, PATH_SPLIT, PATH_FUSED, PATH_MMA = 0, 1, 2, 3
+DECODE_PATHS = [PATH_AUTO, PATH_SPLIT, PATH_FUSED]
 
 
 @pytest.mark.parametrize("name", APPLY_CASES)
@@ -136,13 +138,36 @@ def test_apply_matches_oracle(name):
     stated_gate(y, yref)
 
 
-@pytest.mark.parametrize("name", APPLY_CASES + ["prefill_small"])
-def test_apply_delta_only(name):
-    wl = W.sparse_prefill(n_requests=3, y_zero=True) if name == "prefill_small" else W.make(name, y_zero=True)
+@pytest.mark.parametrize("path", DECODE_PATHS)
+@pytest.mark.parametrize("name", APPLY_CASES)
+def test_apply_delta_only(name, path):
+    wl = W.make(name, y_zero=True)
+    y, st = run_gpu(wl, path=path)
+    _, acc, ost = oracle.apply_workload(wl, threads=0)
+    assert st == ost == 0
+    delta_gate(y, acc)
+
+
+def test_prefill_small_delta_only():
+    wl = W.sparse_prefill(n_requests=3, y_zero=True)
     y, st = run_gpu(wl)
     _, acc, ost = oracle.apply_workload(wl, threads=0)
     assert st == ost == 0
     delta_gate(y, acc)
+
+
+def test_paths_agree_bitwise_where_order_matches():
+    """Split and fused paths sum in the same order only per window; both must
+    pass the delta bound, and repeated fused launches (barrier counters
+    carried across launches) must give identical bits."""
+    wl = W.zipf_decode(y_zero=True)
+    dw = DeviceWorkload(wl)
+    try:
+        runs = [bf16_to_numpy_bits(dw.apply(path=PATH_FUSED)) for _ in range(4)]
+    finally:
+        dw.close()
+    for r in runs[1:]:
+        np.testing.assert_array_equal(r, runs[0])
 
 
 def test_prefill_full_size_sampled():
@@ -204,12 +229,13 @@ def test_unregistered_slot():
     delta_gate(bf16_to_numpy_bits(y), acc)
 
 
-def test_deterministic():
+@pytest.mark.parametrize("path", DECODE_PATHS)
+def test_deterministic(path):
     wl = W.rank_sweep(256)
     dw = DeviceWorkload(wl)
     try:
-        a = bf16_to_numpy_bits(dw.apply())
-        b = bf16_to_numpy_bits(dw.apply())
+        a = bf16_to_numpy_bits(dw.apply(path=path))
+        b = bf16_to_numpy_bits(dw.apply(path=path))
     finally:
         dw.close()
     np.testing.assert_array_equal(a, b)
@@ -267,9 +293,12 @@ def _custom(rng, d_in, d_out, r, cap, lists, ranks=None):
                          alpha_lists=alpha_lists, ranks=ranks, y_sigma=0.0)
 
 
-def test_big_segments_and_many_pairs_per_token():
+@pytest.mark.parametrize("ntok", [300, 200])
+def test_big_segments_and_many_pairs_per_token(ntok):
+    """Segments far longer than a shrink tile or an expand job, one token with
+    40 pairs, an empty token; 200 tokens also runs the fused path."""
     rng = np.random.default_rng(21)
-    lists = [[0, 1, 2] for _ in range(300)] + [list(rng.permutation(64)[:40])] + [[]] + [[5]]
+    lists = [[0, 1, 2] for _ in range(ntok)] + [list(rng.permutation(64)[:40])] + [[]] + [[5]]
     wl = _custom(rng, 128, 192, 16, 64, lists)
     y, st = run_gpu(wl)
     _, acc, _ = oracle.apply_workload(wl)
@@ -277,16 +306,17 @@ def test_big_segments_and_many_pairs_per_token():
     delta_gate(y, acc)
 
 
+@pytest.mark.parametrize("path", DECODE_PATHS)
 @pytest.mark.parametrize("d_in,d_out,r,k", [(64, 128, 1, 1), (6208, 64, 5, 3), (14336, 4096, 8, 8),
                                             (256, 256, 64, 64), (192, 320, 13, 7)])
-def test_shapes(d_in, d_out, r, k):
+def test_shapes(d_in, d_out, r, k, path):
     rng = np.random.default_rng(d_in + d_out)
     cap = 6
     lists = [list(rng.permutation(cap)[:rng.integers(1, 4)]) for _ in range(9)]
     ranks = np.full(cap, k, np.int32)
     ranks[0] = 0
     wl = _custom(rng, d_in, d_out, r, cap, lists, ranks)
-    y, st = run_gpu(wl)
+    y, st = run_gpu(wl, path=path)
     _, acc, _ = oracle.apply_workload(wl)
     delta_gate(y, acc)
 
