@@ -63,6 +63,7 @@ struct ShrinkShared {
     int tok[SHR_LIST][SHRINK_TT];
     short clen[SHR_LIST];
     int wsum[8];
+    int capsum[6][8];
     int2 tcache[SHRINK_ROUND_TILES];  // {adapter | n << 16 | k << 20, q0} per tile of the round
     int prefix[SHRINK_ROUND_TILES + 1];
 };
@@ -202,7 +203,7 @@ static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsig
 
     if (tid == 0) {
         for (int s = 0; s < SHR_MAXE; ++s)
-            mbar_init(&sh.bar[s], SHRINK_THREADS);
+            mbar_init(&sh.bar[s], 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -210,22 +211,51 @@ static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsig
     uint32_t e_base = 0;  // entry sequence number (drives barrier slot and parity)
     int unit_parity = 0;
     for (int rbase = 0; rbase < a.tile_bound; rbase += SHRINK_ROUND_TILES) {
-        // ---- count the units of every tile of the round, scan
+        // ---- units of every tile of the round.  Rows per unit: the tile shape's
+        // maximum, capped by the largest cap in {32, 16, 8, 4, 2, 1} that still
+        // gives at least one unit per CTA (small batches spread over all SMs).
         const int ntr = min(SHRINK_ROUND_TILES, a.tile_bound - rbase);
+        int part[6] = {0, 0, 0, 0, 0, 0};
         for (int i = tid; i < ntr; i += SHRINK_THREADS) {
             const int4 t = a.m.tile[rbase + i];  // {adapter, q0, n, segment}; n = 0: empty slot
-            int cnt = 0, k = 0;
+            int k = 0;
             if (t.z > 0) {
                 k = a.use_tab ? rank_tab[t.x] : effective_rank(a.pool, a.ranks, t.x);
                 if (k < 0) {
                     atomicOr(status, k == -1 ? LORA_DEV_UNREGISTERED : LORA_DEV_BAD_RANK);
                     k = 0;
                 }
-                const int rows = shrink_rows_for<WIDE>(t.z);
-                cnt = (k + rows - 1) / rows;
+                const int rmax = shrink_rows_for<WIDE>(t.z);
+#pragma unroll
+                for (int ci = 0; ci < 6; ++ci) {
+                    const int rows = min(rmax, 32 >> ci);
+                    part[ci] += (k + rows - 1) / rows;
+                }
             }
             sh.tcache[i] = make_int2(t.x | (t.z << 16) | (k << 20), t.y);
-            sh.prefix[i] = cnt;
+        }
+#pragma unroll
+        for (int ci = 0; ci < 6; ++ci) {
+            const int v = __reduce_add_sync(0xffffffffu, part[ci]);
+            if (lane == 0)
+                sh.capsum[ci][warp] = v;
+        }
+        __syncthreads();
+        int cap_rows = 1;
+#pragma unroll
+        for (int ci = 5; ci >= 0; --ci) {
+            int tot = 0;
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                tot += sh.capsum[ci][w];
+            if (tot >= ncta)
+                cap_rows = 32 >> ci;  // the largest cap that still fills the grid
+        }
+        for (int i = tid; i < ntr; i += SHRINK_THREADS) {
+            const int2 tc = sh.tcache[i];
+            const int n = (tc.x >> 16) & 0xf, k = (tc.x >> 20) & 0x7f;
+            const int rows = min(shrink_rows_for<WIDE>(n), cap_rows);
+            sh.prefix[i] = n > 0 ? (k + rows - 1) / rows : 0;
         }
         __syncthreads();
         shrink_scan(sh.prefix, ntr, sh.wsum);
@@ -247,7 +277,7 @@ static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsig
                 }
                 const int2 tc = sh.tcache[lo];
                 const int adapter = tc.x & 0xffff, n = (tc.x >> 16) & 0xf, k = (tc.x >> 20) & 0x7f;
-                const int rows = shrink_rows_for<WIDE>(n);
+                const int rows = min(shrink_rows_for<WIDE>(n), cap_rows);
                 const int j0 = (u - sh.prefix[lo]) * rows;
                 const int R = min(rows, k - j0);
                 sh.unit[tid] = make_int4(adapter, tc.y, n, (j0 << 8) | R);
@@ -278,8 +308,8 @@ static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsig
             (void)L;
 
             // ---- entries (unit, chunk) in order through the byte ring.  Every
-            // thread runs the same allocation (uniform state) and issues its
-            // share of each entry's 16-byte copies.
+            // thread runs the same allocation (uniform state); thread 0 issues
+            // the entry's bulk copies.
             int my_off[SHR_MAXE];
             int p_next = 0, p_e = 0, p_ch = 0, head = 0;
             auto issue_more = [&](int c_done) {
@@ -310,17 +340,21 @@ static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsig
                     }
                     const int slot = (e_base + p_next) % SHR_MAXE;
                     my_off[slot] = pos;
-                    const int vpr = clen / 8;  // 16-byte vectors per row
-                    const int nvec = (R + n) * vpr;
-                    unsigned char *dst = ring + pos;
-                    const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
-                    for (int v = tid; v < nvec; v += SHRINK_THREADS) {
-                        const int row = v / vpr, cv = v - row * vpr;
-                        const __nv_bfloat16 *src = row < R ? Abase + (size_t)row * d_in + cv * 8
-                                                           : a.x + (size_t)sh.tok[p_e][row - R] * d_in + c0 + cv * 8;
-                        cp_async16(dst + (size_t)v * 16, src);
+                    if (tid == 0) {
+                        const uint32_t row_bytes = (uint32_t)clen * 2u;
+                        unsigned char *dst = ring + pos;
+                        mbar_arrive_expect_tx(&sh.bar[slot], row_bytes * (uint32_t)(R + n));
+                        const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
+                        if (clen == d_in) {  // whole rows: the unit's A rows are one contiguous run
+                            bulk_g2s(dst, Abase, row_bytes * (uint32_t)R, &sh.bar[slot]);
+                        } else {
+                            for (int rr = 0; rr < R; ++rr)
+                                bulk_g2s(dst + rr * row_bytes, Abase + (size_t)rr * d_in, row_bytes, &sh.bar[slot]);
+                        }
+                        for (int i = 0; i < n; ++i)
+                            bulk_g2s(dst + (R + i) * row_bytes, a.x + (size_t)sh.tok[p_e][i] * d_in + c0, row_bytes,
+                                     &sh.bar[slot]);
                     }
-                    cp_async_mbar_arrive(&sh.bar[slot]);
                     head = pos + size;
                     ++p_next;
                     if (c0 + clen >= d_in) {
@@ -343,7 +377,7 @@ static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsig
                 const int e = c_e, ch = c_ch;
                 const int4 r = sh.unit[e];
                 const int n = r.z, R = r.w & 0xff;
-                const int rows = shrink_rows_for<WIDE>(n);
+                const int rows = shrink_rows_for<WIDE>(n);  // accumulator shape (R <= rows)
                 const int clen_u = sh.clen[e];
                 const int clen = min(clen_u, d_in - ch * clen_u);
                 const bool last = (ch * clen_u + clen >= d_in);
