@@ -7,11 +7,12 @@
 //
 // One cooperative launch of one CTA per SM (all resident).  Every CTA:
 //   1. stages the rank table and, if it has an expand role (column tile x
-//      segment group), the y rows it will finalise, builds its first window
-//      of jobs and stages their B tiles and per-token pair lists -- none of it
-//      depends on z, so these loads are in flight during step 2;
-//   2. runs its share of the shrink (shrink_core.cuh), writing z to global
-//      memory (it stays in L2);
+//      segment group), the y rows it will finalise;
+//   2. starts its share of the shrink (shrink_core.cuh): units resolved and
+//      their A / x copies issued; then, while those land, builds its first
+//      expand window and stages the B tiles and per-token pair lists (none of
+//      it depends on z); then finishes the shrink, writing z to global memory
+//      (it stays in L2);
 //   3. meets the others at a grid barrier (bounded wait, LORA_DEV_TIMEOUT on
 //      expiry) so that every z is visible;
 //   4. stages z and accumulates its tile token-major in registers
@@ -107,10 +108,14 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_fused(FusedArgs a)
         racc[c] = 0.f;
     __syncthreads();
 
-    // 2-4. shrink inside the hook that runs before the first z read
+    // 2. the shrink's first copies go out first; the expand's z-independent
+    // work (window build, B tiles, pair lists) overlaps them; the shrink is
+    // finished and the grid meets in the hook that runs before the first z read
+    ShrinkRun<true> run(a.s, sh, ring, rank_tab, blockIdx.x, G);
+    run.begin();
     bool ok = true;
     expand_accumulate<CPT>(e, smem_raw, es, c0, 0, nt, true, s_begin, s_end, racc, [&] {
-        ok = shrink_phase<true>(a.s, sh, ring, rank_tab, blockIdx.x, G);
+        ok = run.finish();
         ok = grid_barrier(bar_count, base + (unsigned)G, status) && ok;
     });
 

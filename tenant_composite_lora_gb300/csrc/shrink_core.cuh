@@ -21,12 +21,13 @@
 // over all CTAs.
 //
 // The pool stores A transposed (r_max x d_in): a unit's rows are
-// 16-byte-aligned contiguous runs.  All threads stream each entry (a unit's
-// rows over one d_in chunk, whole rows when they fit SHRINK_ENTRY_BYTES) into
-// a byte ring in shared memory with 16-byte asynchronous copies, completing
-// on the entry's mbarrier (cp.async.mbarrier.arrive); entries are issued as
-// long as ring space and barrier slots allow.  (One thread issuing a bulk copy
-// per row was measured to serialise on the copy engine, ~0.2 us per copy.)
+// 16-byte-aligned contiguous runs.  Each entry (a unit's rows over one d_in
+// chunk; whole rows when they fit the entry size, so that the unit's A rows
+// are a single copy) streams into a byte ring in shared memory with bulk
+// (TMA) copies that complete on the entry's mbarrier; entries are issued as
+// long as ring space and barrier slots allow.  (16-byte cp.async copies from
+// every thread were measured to cap a CTA near 20 GB/s: each ties up an L1
+// miss slot, while the copy engine keeps far more bytes in flight.)
 // Each thread owns 16-byte vectors of every staged row, accumulates 32 fp32
 // partial dot products, and the CTA reduces them with a warp-shuffle
 // reduce-scatter (32 values over 32 lanes in 31 shuffles) and one cross-warp
@@ -61,6 +62,7 @@ struct ShrinkShared {
     float red[2][8][32];
     int4 unit[SHR_LIST];  // {adapter, q0, n, (j0 << 8) | R}
     int tok[SHR_LIST][SHRINK_TT];
+    float alpha[SHR_LIST][SHRINK_TT];  // pair weights of each unit's tile
     short clen[SHR_LIST];
     int wsum[8];
     int capsum[6][8];
@@ -189,32 +191,43 @@ __device__ __forceinline__ void shrink_scan(int *s, int n, int *wsum)
     __syncthreads();
 }
 
-// The whole shrink of this CTA: units cta, cta + ncta, ... of the live list.
+// The whole shrink of this CTA: units cta, cta + ncta, ... of the live list,
+// as a small state machine so that a caller can put other work between the
+// first copies being issued and their consumption:
+//   begin()  barriers, first round's scan, first pass resolved, its copies issued
+//   finish() consume that pass, then every further pass and round
 // ring: ring_bytes of shared memory; rank_tab: staged ranks (if use_tab).
-// Returns false if a bounded wait expired (the status word records it).
+// finish() returns false if a bounded wait expired (the status word records it).
 template <bool WIDE>
-static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsigned char *ring, const int *rank_tab,
-                             int cta, int ncta)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d_in = a.pool.d_in, r_max = a.pool.r_max;
-    int32_t *status = a.m.hdr + HDR_STATUS;
-    const int RING = a.ring_bytes;
-
-    if (tid == 0) {
-        for (int s = 0; s < SHR_MAXE; ++s)
-            mbar_init(&sh.bar[s], 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-
+struct ShrinkRun {
+    const ShrinkArgs &a;
+    ShrinkShared &sh;
+    unsigned char *ring;
+    const int *rank_tab;
+    int cta, ncta;
+    // round / pass
+    int rbase = 0, ntr = 0, total_r = 0, cap_rows = 1, pass = 0, total = 0;
+    bool has_pass = false;
+    // ring producer (uniform across threads)
+    int p_next = 0, p_e = 0, p_ch = 0, head = 0;
+    int my_off[SHR_MAXE];
     uint32_t e_base = 0;  // entry sequence number (drives barrier slot and parity)
     int unit_parity = 0;
-    for (int rbase = 0; rbase < a.tile_bound; rbase += SHRINK_ROUND_TILES) {
-        // ---- units of every tile of the round.  Rows per unit: the tile shape's
-        // maximum, capped by the largest cap in {32, 16, 8, 4, 2, 1} that still
-        // gives at least one unit per CTA (small batches spread over all SMs).
-        const int ntr = min(SHRINK_ROUND_TILES, a.tile_bound - rbase);
+
+    __device__ ShrinkRun(const ShrinkArgs &a_, ShrinkShared &sh_, unsigned char *ring_, const int *rank_tab_,
+                         int cta_, int ncta_)
+        : a(a_), sh(sh_), ring(ring_), rank_tab(rank_tab_), cta(cta_), ncta(ncta_)
+    {
+    }
+
+    // Units of every tile of the round at rbase.  Rows per unit: the tile
+    // shape's maximum, capped by the largest cap in {32, 16, 8, 4, 2, 1} that
+    // still gives at least one unit per CTA (small batches spread over all SMs).
+    __device__ void scan()
+    {
+        const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        int32_t *status = a.m.hdr + HDR_STATUS;
+        ntr = min(SHRINK_ROUND_TILES, a.tile_bound - rbase);
         int part[6] = {0, 0, 0, 0, 0, 0};
         for (int i = tid; i < ntr; i += SHRINK_THREADS) {
             const int4 t = a.m.tile[rbase + i];  // {adapter, q0, n, segment}; n = 0: empty slot
@@ -241,7 +254,7 @@ static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsig
                 sh.capsum[ci][warp] = v;
         }
         __syncthreads();
-        int cap_rows = 1;
+        cap_rows = 1;
 #pragma unroll
         for (int ci = 5; ci >= 0; --ci) {
             int tot = 0;
@@ -259,203 +272,273 @@ static __device__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsig
         }
         __syncthreads();
         shrink_scan(sh.prefix, ntr, sh.wsum);
-        const int total_r = sh.prefix[ntr];
-        __syncthreads();  // every thread has read total_r before the next round rewrites it
+        total_r = sh.prefix[ntr];
+        __syncthreads();  // every thread has read total_r before anything rewrites it
+    }
 
-        for (int pass = cta; pass < total_r; pass += ncta * SHR_LIST) {
-            // ---- resolve this pass's units
-            const int u = pass + tid * ncta;
-            int my_nch = 0;
-            if (u < total_r) {
-                int lo = 0, hi = ntr;  // last tile with prefix <= u
-                while (hi - lo > 1) {
-                    const int mid = (lo + hi) >> 1;
-                    if (sh.prefix[mid] <= u)
-                        lo = mid;
+    // Moves to the next pass with work, scanning later rounds as needed.
+    __device__ bool next_pass(bool first)
+    {
+        if (first) {
+            rbase = 0;
+            scan();
+            pass = cta;
+        } else {
+            pass += ncta * SHR_LIST;
+        }
+        while (pass >= total_r) {
+            rbase += SHRINK_ROUND_TILES;
+            if (rbase >= a.tile_bound)
+                return false;
+            scan();
+            pass = cta;
+        }
+        return true;
+    }
+
+    // Resolves this pass's units (unit record, tokens, pair weights, chunking)
+    // and counts its entries.
+    __device__ void resolve()
+    {
+        const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        const int d_in = a.pool.d_in;
+        const int u = pass + tid * ncta;
+        int my_nch = 0;
+        if (u < total_r) {
+            int lo = 0, hi = ntr;  // last tile with prefix <= u
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (sh.prefix[mid] <= u)
+                    lo = mid;
+                else
+                    hi = mid;
+            }
+            const int2 tc = sh.tcache[lo];
+            const int adapter = tc.x & 0xffff, n = (tc.x >> 16) & 0xf, k = (tc.x >> 20) & 0x7f;
+            const int rows = min(shrink_rows_for<WIDE>(n), cap_rows);
+            const int j0 = (u - sh.prefix[lo]) * rows;
+            const int R = min(rows, k - j0);
+            sh.unit[tid] = make_int4(adapter, tc.y, n, (j0 << 8) | R);
+            const int4 tk0 = reinterpret_cast<const int4 *>(a.m.tile_tok)[2 * (rbase + lo)];
+            const int4 tk1 = reinterpret_cast<const int4 *>(a.m.tile_tok)[2 * (rbase + lo) + 1];
+            sh.tok[tid][0] = tk0.x;
+            sh.tok[tid][1] = tk0.y;
+            sh.tok[tid][2] = tk0.z;
+            sh.tok[tid][3] = tk0.w;
+            sh.tok[tid][4] = tk1.x;
+            sh.tok[tid][5] = tk1.y;
+            sh.tok[tid][6] = tk1.z;
+            sh.tok[tid][7] = tk1.w;
+#pragma unroll
+            for (int i = 0; i < SHRINK_TT; ++i)
+                sh.alpha[tid][i] = i < n ? a.m.alpha[tc.y + i] : 0.f;
+            // longest chunk (multiple of 64 elements) whose rows fit one entry
+            const int clen = min(d_in, max(64, (a.entry_bytes / (2 * (R + n))) & ~63));
+            sh.clen[tid] = (short)clen;
+            my_nch = (d_in + clen - 1) / clen;
+        }
+        const unsigned nb = __reduce_add_sync(0xffffffffu, (unsigned)my_nch);
+        if (lane == 0)
+            sh.wsum[warp] = (int)nb;
+        __syncthreads();
+        total = 0;
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            total += sh.wsum[w];
+        p_next = p_e = p_ch = head = 0;
+    }
+
+    // Entries (unit, chunk) in order through the byte ring.  Every thread runs
+    // the same allocation (uniform state); thread 0 issues the bulk copies.
+    __device__ void issue_more(int c_done)
+    {
+        const int d_in = a.pool.d_in, r_max = a.pool.r_max, RING = a.ring_bytes;
+        while (p_next < total && p_next - c_done < SHR_MAXE) {
+            const int4 r = sh.unit[p_e];
+            const int n = r.z, R = r.w & 0xff, j0 = r.w >> 8;
+            const int clen_u = sh.clen[p_e];
+            const int c0 = p_ch * clen_u, clen = min(clen_u, d_in - c0);
+            const int size = (R + n) * clen * 2;
+            int pos;
+            if (p_next == c_done) {
+                pos = 0;  // ring empty
+            } else {
+                const int tail = my_off[(e_base + c_done) % SHR_MAXE];
+                if (head > tail) {
+                    if (head + size <= RING)
+                        pos = head;
+                    else if (size < tail)
+                        pos = 0;
                     else
-                        hi = mid;
-                }
-                const int2 tc = sh.tcache[lo];
-                const int adapter = tc.x & 0xffff, n = (tc.x >> 16) & 0xf, k = (tc.x >> 20) & 0x7f;
-                const int rows = min(shrink_rows_for<WIDE>(n), cap_rows);
-                const int j0 = (u - sh.prefix[lo]) * rows;
-                const int R = min(rows, k - j0);
-                sh.unit[tid] = make_int4(adapter, tc.y, n, (j0 << 8) | R);
-                const int4 tk0 = reinterpret_cast<const int4 *>(a.m.tile_tok)[2 * (rbase + lo)];
-                const int4 tk1 = reinterpret_cast<const int4 *>(a.m.tile_tok)[2 * (rbase + lo) + 1];
-                sh.tok[tid][0] = tk0.x;
-                sh.tok[tid][1] = tk0.y;
-                sh.tok[tid][2] = tk0.z;
-                sh.tok[tid][3] = tk0.w;
-                sh.tok[tid][4] = tk1.x;
-                sh.tok[tid][5] = tk1.y;
-                sh.tok[tid][6] = tk1.z;
-                sh.tok[tid][7] = tk1.w;
-                // longest chunk (multiple of 64 elements) whose rows fit one entry
-                const int clen = min(d_in, max(64, (a.entry_bytes / (2 * (R + n))) & ~63));
-                sh.clen[tid] = (short)clen;
-                my_nch = (d_in + clen - 1) / clen;
-            }
-            const int L = min(SHR_LIST, (total_r - pass + ncta - 1) / ncta);
-            const unsigned nb = __reduce_add_sync(0xffffffffu, (unsigned)my_nch);
-            if (lane == 0)
-                sh.wsum[warp] = (int)nb;
-            __syncthreads();
-            int total = 0;
-#pragma unroll
-            for (int w = 0; w < 8; ++w)
-                total += sh.wsum[w];
-            (void)L;
-
-            // ---- entries (unit, chunk) in order through the byte ring.  Every
-            // thread runs the same allocation (uniform state); thread 0 issues
-            // the entry's bulk copies.
-            int my_off[SHR_MAXE];
-            int p_next = 0, p_e = 0, p_ch = 0, head = 0;
-            auto issue_more = [&](int c_done) {
-                while (p_next < total && p_next - c_done < SHR_MAXE) {
-                    const int4 r = sh.unit[p_e];
-                    const int n = r.z, R = r.w & 0xff, j0 = r.w >> 8;
-                    const int clen_u = sh.clen[p_e];
-                    const int c0 = p_ch * clen_u, clen = min(clen_u, d_in - c0);
-                    const int size = (R + n) * clen * 2;
-                    int pos;
-                    if (p_next == c_done) {
-                        pos = 0;  // ring empty
-                    } else {
-                        const int tail = my_off[(e_base + c_done) % SHR_MAXE];
-                        if (head > tail) {
-                            if (head + size <= RING)
-                                pos = head;
-                            else if (size < tail)
-                                pos = 0;
-                            else
-                                break;
-                        } else {
-                            if (head + size < tail)
-                                pos = head;
-                            else
-                                break;
-                        }
-                    }
-                    const int slot = (e_base + p_next) % SHR_MAXE;
-                    my_off[slot] = pos;
-                    if (tid == 0) {
-                        const uint32_t row_bytes = (uint32_t)clen * 2u;
-                        unsigned char *dst = ring + pos;
-                        mbar_arrive_expect_tx(&sh.bar[slot], row_bytes * (uint32_t)(R + n));
-                        const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
-                        if (clen == d_in) {  // whole rows: the unit's A rows are one contiguous run
-                            bulk_g2s(dst, Abase, row_bytes * (uint32_t)R, &sh.bar[slot]);
-                        } else {
-                            for (int rr = 0; rr < R; ++rr)
-                                bulk_g2s(dst + rr * row_bytes, Abase + (size_t)rr * d_in, row_bytes, &sh.bar[slot]);
-                        }
-                        for (int i = 0; i < n; ++i)
-                            bulk_g2s(dst + (R + i) * row_bytes, a.x + (size_t)sh.tok[p_e][i] * d_in + c0, row_bytes,
-                                     &sh.bar[slot]);
-                    }
-                    head = pos + size;
-                    ++p_next;
-                    if (c0 + clen >= d_in) {
-                        ++p_e;
-                        p_ch = 0;
-                    } else {
-                        ++p_ch;
-                    }
-                }
-            };
-            issue_more(0);
-
-            float acc[32];
-            float alpha_i = 0.f;
-            int c_e = 0, c_ch = 0;  // consumer: unit and chunk of entry c
-            for (int c = 0; c < total; ++c) {
-                const uint32_t g = e_base + c;
-                const int slot = g % SHR_MAXE;
-                const bool ok = mbar_wait_bounded(&sh.bar[slot], (g / SHR_MAXE) & 1u, status);
-                const int e = c_e, ch = c_ch;
-                const int4 r = sh.unit[e];
-                const int n = r.z, R = r.w & 0xff;
-                const int rows = shrink_rows_for<WIDE>(n);  // accumulator shape (R <= rows)
-                const int clen_u = sh.clen[e];
-                const int clen = min(clen_u, d_in - ch * clen_u);
-                const bool last = (ch * clen_u + clen >= d_in);
-                if (last) {
-                    ++c_e;
-                    c_ch = 0;
+                        break;
                 } else {
-                    ++c_ch;
-                }
-                if (ch == 0) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        acc[i] = 0.f;
-                    if (warp == 0) {  // this lane's pair weight, needed at the end of the unit
-                        const int i = lane / rows;
-                        alpha_i = i < n ? a.m.alpha[r.y + i] : 0.f;
-                    }
-                }
-                const __nv_bfloat16 *sA = reinterpret_cast<const __nv_bfloat16 *>(ring + my_off[slot]);
-                if (ok) {
-                    if constexpr (WIDE) {
-                        switch (rows) {
-                        case 32:
-                            shrink_entry<1, 32>(sA, clen, n, R, acc);
-                            break;
-                        case 16:
-                            shrink_entry<2, 16>(sA, clen, n, R, acc);
-                            break;
-                        case 8:
-                            shrink_entry<4, 8>(sA, clen, n, R, acc);
-                            break;
-                        default:
-                            shrink_entry<8, 4>(sA, clen, n, R, acc);
-                            break;
-                        }
-                    } else {
-                        if (rows == 8)
-                            shrink_entry<4, 8>(sA, clen, n, R, acc);
-                        else
-                            shrink_entry<8, 4>(sA, clen, n, R, acc);
-                    }
-                }
-                if (last) {
-                    // reduce-scatter: lane l ends with the warp sum of value l
-#pragma unroll
-                    for (int off = 16; off >= 1; off >>= 1) {
-                        const bool upper = (lane & off) != 0;
-#pragma unroll
-                        for (int i = 0; i < off; ++i) {
-                            const float send = upper ? acc[i] : acc[i + off];
-                            const float keep = upper ? acc[i + off] : acc[i];
-                            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                        }
-                    }
-                    sh.red[unit_parity][warp][lane] = acc[0];
-                }
-                const int any_bad = __syncthreads_or(!ok);
-                if (any_bad)
-                    return false;
-                issue_more(c + 1);
-                if (last) {
-                    if (warp == 0) {
-                        float s = 0.f;
-#pragma unroll
-                        for (int w = 0; w < 8; ++w)
-                            s += sh.red[unit_parity][w][lane];
-                        const int i = lane / rows, rr = lane % rows, j0 = r.w >> 8;
-                        if (i < n && rr < R)
-                            a.m.z[(size_t)(r.y + i) * a.zs + j0 + rr] = alpha_i * s;
-                    }
-                    unit_parity ^= 1;
+                    if (head + size < tail)
+                        pos = head;
+                    else
+                        break;
                 }
             }
-            e_base += (uint32_t)total;
-            __syncthreads();
+            const int slot = (e_base + p_next) % SHR_MAXE;
+            my_off[slot] = pos;
+            if (threadIdx.x == 0) {
+                const uint32_t row_bytes = (uint32_t)clen * 2u;
+                unsigned char *dst = ring + pos;
+                mbar_arrive_expect_tx(&sh.bar[slot], row_bytes * (uint32_t)(R + n));
+                const __nv_bfloat16 *Abase = a.pool.At + ((size_t)r.x * r_max + j0) * d_in + c0;
+                if (clen == d_in) {  // whole rows: the unit's A rows are one contiguous run
+                    bulk_g2s(dst, Abase, row_bytes * (uint32_t)R, &sh.bar[slot]);
+                } else {
+                    for (int rr = 0; rr < R; ++rr)
+                        bulk_g2s(dst + rr * row_bytes, Abase + (size_t)rr * d_in, row_bytes, &sh.bar[slot]);
+                }
+                for (int i = 0; i < n; ++i)
+                    bulk_g2s(dst + (R + i) * row_bytes, a.x + (size_t)sh.tok[p_e][i] * d_in + c0, row_bytes,
+                             &sh.bar[slot]);
+            }
+            head = pos + size;
+            ++p_next;
+            if (c0 + clen >= d_in) {
+                ++p_e;
+                p_ch = 0;
+            } else {
+                ++p_ch;
+            }
         }
     }
-    return true;
+
+    // Consumes the current pass's entries (issuing more as space frees up).
+    __device__ bool consume()
+    {
+        const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+        const int d_in = a.pool.d_in;
+        int32_t *status = a.m.hdr + HDR_STATUS;
+        float acc[32];
+        float alpha_i = 0.f;
+        int c_e = 0, c_ch = 0;  // unit and chunk of entry c
+        for (int c = 0; c < total; ++c) {
+            const uint32_t g = e_base + c;
+            const int slot = g % SHR_MAXE;
+            const bool ok = mbar_wait_bounded(&sh.bar[slot], (g / SHR_MAXE) & 1u, status);
+            const int e = c_e, ch = c_ch;
+            const int4 r = sh.unit[e];
+            const int n = r.z, R = r.w & 0xff;
+            const int rows = shrink_rows_for<WIDE>(n);  // accumulator shape (R <= rows)
+            const int clen_u = sh.clen[e];
+            const int clen = min(clen_u, d_in - ch * clen_u);
+            const bool last = (ch * clen_u + clen >= d_in);
+            if (last) {
+                ++c_e;
+                c_ch = 0;
+            } else {
+                ++c_ch;
+            }
+            if (ch == 0) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    acc[i] = 0.f;
+                const int i = lane / rows;  // this lane's pair, needed at the end of the unit
+                alpha_i = i < SHRINK_TT ? sh.alpha[e][i] : 0.f;
+            }
+            const __nv_bfloat16 *sA = reinterpret_cast<const __nv_bfloat16 *>(ring + my_off[slot]);
+            if (ok) {
+                if constexpr (WIDE) {
+                    switch (rows) {
+                    case 32:
+                        shrink_entry<1, 32>(sA, clen, n, R, acc);
+                        break;
+                    case 16:
+                        shrink_entry<2, 16>(sA, clen, n, R, acc);
+                        break;
+                    case 8:
+                        shrink_entry<4, 8>(sA, clen, n, R, acc);
+                        break;
+                    default:
+                        shrink_entry<8, 4>(sA, clen, n, R, acc);
+                        break;
+                    }
+                } else {
+                    if (rows == 8)
+                        shrink_entry<4, 8>(sA, clen, n, R, acc);
+                    else
+                        shrink_entry<8, 4>(sA, clen, n, R, acc);
+                }
+            }
+            if (last) {
+                // reduce-scatter: lane l ends with the warp sum of value l
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) {
+                    const bool upper = (lane & off) != 0;
+#pragma unroll
+                    for (int i = 0; i < off; ++i) {
+                        const float send = upper ? acc[i] : acc[i + off];
+                        const float keep = upper ? acc[i + off] : acc[i];
+                        acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                sh.red[unit_parity][warp][lane] = acc[0];
+            }
+            const int any_bad = __syncthreads_or(!ok);
+            if (any_bad)
+                return false;
+            issue_more(c + 1);
+            if (last) {
+                if (warp == 0) {
+                    float s = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        s += sh.red[unit_parity][w][lane];
+                    const int i = lane / rows, rr = lane % rows, j0 = r.w >> 8;
+                    if (i < n && rr < R)
+                        a.m.z[(size_t)(r.y + i) * a.zs + j0 + rr] = alpha_i * s;
+                }
+                unit_parity ^= 1;
+            }
+        }
+        e_base += (uint32_t)total;
+        __syncthreads();
+        return true;
+    }
+
+    // Barriers, the first pass resolved and its first copies issued.
+    __device__ void begin()
+    {
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < SHR_MAXE; ++s)
+                mbar_init(&sh.bar[s], 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        has_pass = next_pass(true);
+        if (has_pass) {
+            resolve();
+            issue_more(0);
+        }
+    }
+
+    // Everything else; false if a bounded wait expired.
+    __device__ bool finish()
+    {
+        while (has_pass) {
+            if (!consume())
+                return false;
+            has_pass = next_pass(false);
+            if (has_pass) {
+                resolve();
+                issue_more(0);
+            }
+        }
+        return true;
+    }
+};
+
+// The whole shrink of this CTA in one call.
+template <bool WIDE>
+__device__ __forceinline__ bool shrink_phase(const ShrinkArgs &a, ShrinkShared &sh, unsigned char *ring,
+                                             const int *rank_tab, int cta, int ncta)
+{
+    ShrinkRun<WIDE> run(a, sh, ring, rank_tab, cta, ncta);
+    run.begin();
+    return run.finish();
 }
 
 }  // namespace tcl
