@@ -184,8 +184,8 @@ lora_status run_fused(const void *x, void *y, const lora_pool *pool, const int32
     const ExpandPlan plan = choose_expand_plan(m->T, pool->d_out);
     const cudaError_t e = launch_fused(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
                                        pool_dev(pool), ranks, m->dev, m->T, m->P, plan, sm_count(), st);
-    if (e == cudaErrorInvalidValue)
-        return LORA_ERR_NOT_SUPPORTED;
+    if (e == cudaErrorNotSupported)
+        return LORA_ERR_NOT_SUPPORTED;  // the shape does not fit this kernel
     return from_cuda(e);
 }
 

@@ -188,14 +188,39 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_fused(FusedArgs a)
     (void)ok;
 }
 
+// Largest dynamic shared memory k_fused<CPT> may take on this device.
 template <int CPT>
-cudaError_t launch_fused_cpt(const FusedArgs &a, int grid, size_t smem, cudaStream_t st)
+int fused_dynamic_limit()
 {
+    static int cached = -1, cached_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cached_dev != dev) {
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        cudaFuncAttributes fa{};
+        cudaFuncGetAttributes(&fa, k_fused<CPT>);
+        cached = optin - (int)fa.sharedSizeBytes;
+        cached_dev = dev;
+    }
+    return cached;
+}
+
+template <int CPT>
+cudaError_t launch_fused_cpt(FusedArgs a, int grid, size_t exp_bytes, cudaStream_t st)
+{
+    const int dyn_max = fused_dynamic_limit<CPT>();
+    const long long room = (long long)dyn_max - (long long)exp_bytes;
+    const int ring = (int)((room < FUSED_RING_MAX ? room : FUSED_RING_MAX) & ~1023LL);
+    if (ring < 2 * SHRINK_MIN_ENTRY)
+        return cudaErrorNotSupported;
+    a.s.ring_bytes = ring;
+    a.s.entry_bytes = ring / 2;
     static int attr_done = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_fused<CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, FUSED_SMEM_MAX);
+        cudaError_t e = cudaFuncSetAttribute(k_fused<CPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_fused<CPT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
@@ -206,7 +231,7 @@ cudaError_t launch_fused_cpt(const FusedArgs &a, int grid, size_t smem, cudaStre
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(EXP_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = exp_bytes + (size_t)ring;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeCooperative;
@@ -228,31 +253,24 @@ cudaError_t launch_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev
 {
     const int use_tab = pool.capacity <= RANK_TAB_MAX ? 1 : 0;
     const size_t exp_bytes = (expand_smem_bytes(plan.tb, plan.w, pool.capacity) + 127) & ~(size_t)127;
-    // static shared memory of k_fused (ShrinkShared + ExpandShared) is outside this budget
-    const long long room = (long long)FUSED_SMEM_MAX - (long long)exp_bytes;
-    const int ring = (int)((room < FUSED_RING_MAX ? room : FUSED_RING_MAX) & ~1023LL);
-    if (ring < 2 * SHRINK_MIN_ENTRY)
-        return cudaErrorInvalidValue;
     FusedArgs a;
-    a.s = ShrinkArgs{x, pool, ranks, m, z_stride(pool.r_max), shrink_tile_bound(P, pool.capacity), use_tab,
-                     ring, ring / 2};
+    a.s = ShrinkArgs{x, pool, ranks, m, z_stride(pool.r_max), shrink_tile_bound(P, pool.capacity), use_tab, 0, 0};
     a.e = ExpandArgs{y, pool, ranks, m, T, plan.tb, z_stride(pool.r_max), plan.w, plan.ng, use_tab};
     a.n_exp = (pool.d_out / plan.w) * plan.ng;
     a.partial = m.partial;
     if (a.n_exp > grid || (plan.ng > 1 && a.n_exp > m.partial_ctas) || plan.tb * plan.w > EXP_TILE_ELEMS)
-        return cudaErrorInvalidValue;
-    const size_t smem = exp_bytes + (size_t)ring;
+        return cudaErrorNotSupported;
     switch (expand_cpt(plan.tb, plan.w)) {
     case 2:
-        return launch_fused_cpt<2>(a, grid, smem, st);
+        return launch_fused_cpt<2>(a, grid, exp_bytes, st);
     case 4:
-        return launch_fused_cpt<4>(a, grid, smem, st);
+        return launch_fused_cpt<4>(a, grid, exp_bytes, st);
     case 8:
-        return launch_fused_cpt<8>(a, grid, smem, st);
+        return launch_fused_cpt<8>(a, grid, exp_bytes, st);
     case 16:
-        return launch_fused_cpt<16>(a, grid, smem, st);
+        return launch_fused_cpt<16>(a, grid, exp_bytes, st);
     case 32:
-        return launch_fused_cpt<32>(a, grid, smem, st);
+        return launch_fused_cpt<32>(a, grid, exp_bytes, st);
     default:
         return cudaErrorInvalidValue;
     }

@@ -14,7 +14,7 @@ constexpr int SHRINK_TT = 8;
 constexpr int SHRINK_THREADS = 256;
 constexpr int SHRINK_RING_BYTES = 64 * 1024;   // split path (beside an expand CTA)
 constexpr int SHRINK_MIN_ENTRY = 12 * 64 * 2;  // a 64-element chunk of the largest unit
-constexpr int SHRINK_ROUND_TILES = 2048;       // tile records scanned per round
+constexpr int SHRINK_ROUND_TILES = 1024;       // tile records scanned per round
 constexpr int SHRINK_MAX_INFLIGHT = 8;
 
 // Expand (RowExpand) tile: W in {32, 64, 128} output columns x a token block
@@ -46,8 +46,8 @@ enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR
        HDR_EXIT = 7, HDR_WORDS = 8 };
 
 // Fused decode kernel: one CTA per SM; dynamic shared memory = the expand
-// layout + an entry ring of at most FUSED_RING_MAX bytes.
-constexpr int FUSED_SMEM_MAX = 184 * 1024;  // + ~42 KB static <= 227 KB
+// layout + an entry ring of at most FUSED_RING_MAX bytes (less if the
+// device's per-block limit minus the kernel's static shared memory is lower).
 constexpr int FUSED_RING_MAX = 96 * 1024;
 
 struct PoolDev {
