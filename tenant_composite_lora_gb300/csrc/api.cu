@@ -10,6 +10,7 @@ struct lora_pool {
     __nv_bfloat16 *At;  // [capacity][r_max][d_in]
     __nv_bfloat16 *B;   // [capacity][r_max][d_out]
     int32_t *reg_rank;  // [capacity]
+    tcl::MmaMaps maps;  // TMA descriptors of At and B (tensor-core path)
 };
 
 struct lora_mapping {
@@ -118,8 +119,9 @@ cudaError_t dalloc(T **p, size_t count)
 void free_mapping(lora_mapping *m)
 {
     MapDev &d = m->dev;
-    void *ptrs[] = {d.tok, d.adapter, d.src, d.pos, d.alpha, d.seg_adapter, d.seg_start, d.tile, d.tile_tok,
-                    d.tmp_tok, d.hdr, d.z, d.partial, m->sx, m->sy, m->soff, m->sids, m->salpha};
+    void *ptrs[] = {d.tok,  d.adapter, d.src, d.pos,     d.alpha, d.seg_adapter, d.seg_start,
+                    d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.z,
+                    d.partial, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -128,13 +130,15 @@ void free_mapping(lora_mapping *m)
 
 // Dispatch table (LoRAForge page, "Approach" (5): native path or a special
 // kernel, fixed by phase, rank and shape).
+// Long batches (prefill) go to the tensor cores: a 128-token tile then
+// touches few adapters and a segment holds many tokens.
 int choose_path(int T, int P, int r_max, int d_in, int d_out)
 {
     (void)P;
-    (void)r_max;
-    (void)d_in;
     if (fused_supported(T, d_out))
         return LORA_PATH_FUSED;  // decode: one launch
+    if (T >= MMA_MIN_TOKENS && mma_supported(d_in, d_out, r_max))
+        return LORA_PATH_MMA;
     return LORA_PATH_SPLIT;
 }
 
@@ -186,6 +190,18 @@ lora_status run_fused(const void *x, void *y, const lora_pool *pool, const int32
                                        pool_dev(pool), ranks, m->dev, m->T, m->P, plan, sm_count(), st);
     if (e == cudaErrorNotSupported)
         return LORA_ERR_NOT_SUPPORTED;  // the shape does not fit this kernel
+    return from_cuda(e);
+}
+
+lora_status run_mma(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
+                    cudaStream_t st)
+{
+    if (!pool->maps.ready || !mma_supported(pool->d_in, pool->d_out, pool->r_max))
+        return LORA_ERR_NOT_SUPPORTED;
+    const cudaError_t e = launch_mma(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
+                                     pool_dev(pool), pool->maps, ranks, m->dev, m->T, m->P, st);
+    if (e == cudaErrorNotSupported)
+        return LORA_ERR_NOT_SUPPORTED;
     return from_cuda(e);
 }
 
@@ -265,6 +281,8 @@ lora_status lora_pool_create(int d_in, int d_out, int r_max, int capacity, lora_
         e = cudaMemset(p->reg_rank, 0xff, (size_t)capacity * sizeof(int32_t));  // -1: unregistered
     if (e == cudaSuccess)
         e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        mma_encode_maps(pool_dev(p), p->maps);  // without it the tensor-core path reports NOT_SUPPORTED
     if (e != cudaSuccess) {
         if (p->At)
             cudaFree(p->At);
@@ -346,6 +364,8 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.tile_tok, P * SHRINK_TT);
     if (e == cudaSuccess) e = dalloc(&d.tmp_tok, P);
     if (e == cudaSuccess) e = dalloc(&d.hdr, (size_t)HDR_WORDS);
+    if (e == cudaSuccess) e = dalloc(&d.mtile, (size_t)mma_tile_bound(max_pairs, capacity));
+    if (e == cudaSuccess) e = dalloc(&d.toff, (size_t)max_tokens + 1);
     if (e == cudaSuccess) e = dalloc(&d.z, P * LORA_MAX_RANK);
     d.partial_ctas = sm_count();
     if (e == cudaSuccess) e = dalloc(&d.partial, (size_t)d.partial_ctas * EXP_TILE_ELEMS);
@@ -396,6 +416,8 @@ lora_status lora_delta_apply_path(const void *x_dev, void *y_dev, const lora_poo
         return run_split(x_dev, y_dev, pool, ranks_dev, m, st);
     case LORA_PATH_FUSED:
         return run_fused(x_dev, y_dev, pool, ranks_dev, m, st);
+    case LORA_PATH_MMA:
+        return run_mma(x_dev, y_dev, pool, ranks_dev, m, st);
     default:
         return LORA_ERR_NOT_SUPPORTED;
     }

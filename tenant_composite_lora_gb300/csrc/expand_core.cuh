@@ -132,31 +132,6 @@ __device__ __forceinline__ int4 block_scan4(int4 v, int4 &total, int4 *sh /* [NW
                      before.w + inc.w - v.w);
 }
 
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ float4 ld_dsmem_f4(const void *local, uint32_t rank)
-{
-    uint32_t raddr;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(raddr)
-                 : "memory");
-    return v;
-}
-
 // CPT: columns of the tile owned by one thread (2, 4, 8, 16 or 32); the
 // tile width W and the threads per token TPT = W / CPT are runtime values.
 

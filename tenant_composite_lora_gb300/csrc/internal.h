@@ -42,8 +42,15 @@ constexpr int RANK_TAB_MAX = 2048;
 
 // Header words of the mapping (device int32).
 // HDR_BAR, HDR_BAR_BASE, HDR_EXIT: grid-barrier counters of the fused kernel.
+// HDR_NMTILES: tensor-core shrink tiles (MMA_TM pairs of one segment).
 enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_BAR = 5, HDR_BAR_BASE = 6,
-       HDR_EXIT = 7, HDR_WORDS = 8 };
+       HDR_EXIT = 7, HDR_NMTILES = 8, HDR_WORDS = 9 };
+
+// Tensor-core (tcgen05) prefill path: tiles of MMA_TM rows (pairs of one
+// segment for the shrink, consecutive tokens for the expand).
+constexpr int MMA_TM = 128;
+// Dispatch: batches of at least this many tokens take the tensor-core path.
+constexpr int MMA_MIN_TOKENS = 512;
 
 // Fused decode kernel: one CTA per SM; dynamic shared memory = the expand
 // layout + an entry ring of at most FUSED_RING_MAX bytes (less if the
@@ -65,6 +72,8 @@ struct MapDev {
     int32_t *tile_tok;                   // [max_pairs][SHRINK_TT] tokens of each tile's pairs
     int32_t *tmp_tok;                    // [max_pairs] scratch
     int32_t *hdr;                        // [HDR_WORDS]
+    int4 *mtile;                         // [mma_tile_bound] tensor-core shrink tiles {adapter, q0, n, segment}
+    int32_t *toff;                       // [max_tokens+1] copy of the batch's CSR offsets
     float *z;                            // [max_pairs][LORA_MAX_RANK] shrink output
     float *partial;                      // [partial_ctas][EXP_TILE_ELEMS] fused-kernel tiles
     int partial_ctas;
@@ -93,8 +102,24 @@ int sm_count();
 // (host-computable; the mapping fills unused tile slots with empty records).
 int shrink_tile_bound(int P, int capacity);
 
+// Upper bound of the number of tensor-core shrink tiles (MMA_TM pairs of one segment).
+int mma_tile_bound(int P, int capacity);
+
 bool fused_supported(int T, int d_out);
 cudaError_t launch_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
                          const MapDev &m, int T, int P, const ExpandPlan &plan, int grid, cudaStream_t st);
+
+// Tensor-core prefill path (tcgen05): segment shrink with the K dimension
+// split over a cluster, then a token-tile expand; chained with programmatic
+// dependent launch.  Tensor maps of the pool are encoded once per pool.
+struct MmaMaps {
+    alignas(64) unsigned char At[128];  // CUtensorMap over At: [capacity * r_max][d_in]
+    alignas(64) unsigned char B[128];   // CUtensorMap over B:  [capacity * r_max][d_out]
+    bool ready;
+};
+cudaError_t mma_encode_maps(const PoolDev &pool, MmaMaps &maps);
+bool mma_supported(int d_in, int d_out, int r_max);
+cudaError_t launch_mma(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const MmaMaps &maps,
+                       const int32_t *ranks, const MapDev &m, int T, int P, cudaStream_t st);
 
 }  // namespace tcl

@@ -15,8 +15,9 @@
 //      histograms of the ids over contiguous chunks of the pairs (warp-level
 //      match + popcount, no atomics; layout [warp][bin], conflict-free);
 //   3. block scans over the bins give every warp's first output slot per
-//      bin, the segments, and the shrink tiles (<= SHRINK_TT pairs of one
-//      segment; slots up to the host-known bound get empty sentinels);
+//      bin, the segments, the shrink tiles (<= SHRINK_TT pairs of one
+//      segment) and the tensor-core shrink tiles (<= MMA_TM pairs of one
+//      segment); slots up to the host-known bounds get empty sentinels;
 //   4. each warp rescans its chunk and scatters: rank among equal keys =
 //      earlier lanes with the same key + the warp's running cursor; the
 //      token also goes to its shrink tile's token list.
@@ -30,79 +31,69 @@ namespace tcl {
 
 namespace {
 
-struct Scan3 {
-    int a, b, c;
+struct Scan4 {
+    int a, b, c, d;
 };
 
-// Block-wide exclusive scan of three ints (MAP_THREADS threads); returns the
+// Block-wide exclusive scan of four ints (MAP_THREADS threads); returns the
 // exclusive prefix and writes the block totals.
-__device__ Scan3 block_exclusive_scan3(Scan3 v, Scan3 &total, int *sh /* [3 * 32 + 3] */)
+__device__ Scan4 block_exclusive_scan4(Scan4 v, Scan4 &total, int *sh /* [4 * 32 + 4] */)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    Scan3 inc = v;
+    int in[4] = {v.a, v.b, v.c, v.d};
+    int inc[4] = {v.a, v.b, v.c, v.d};
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int a = __shfl_up_sync(0xffffffffu, inc.a, off);
-        const int b = __shfl_up_sync(0xffffffffu, inc.b, off);
-        const int c = __shfl_up_sync(0xffffffffu, inc.c, off);
-        if (lane >= off) {
-            inc.a += a;
-            inc.b += b;
-            inc.c += c;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int o = __shfl_up_sync(0xffffffffu, inc[j], off);
+            if (lane >= off)
+                inc[j] += o;
         }
     }
-    if (lane == 31) {
-        sh[warp] = inc.a;
-        sh[32 + warp] = inc.b;
-        sh[64 + warp] = inc.c;
-    }
+    if (lane == 31)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            sh[32 * j + warp] = inc[j];
     __syncthreads();
     if (warp == 0) {
-        const int a = sh[lane], b = sh[32 + lane], c = sh[64 + lane];
-        int ia = a, ib = b, ic = c;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int xa = __shfl_up_sync(0xffffffffu, ia, off);
-            const int xb = __shfl_up_sync(0xffffffffu, ib, off);
-            const int xc = __shfl_up_sync(0xffffffffu, ic, off);
-            if (lane >= off) {
-                ia += xa;
-                ib += xb;
-                ic += xc;
+        for (int j = 0; j < 4; ++j) {
+            const int x = sh[32 * j + lane];
+            int ix = x;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, ix, off);
+                if (lane >= off)
+                    ix += o;
             }
-        }
-        sh[lane] = ia - a;
-        sh[32 + lane] = ib - b;
-        sh[64 + lane] = ic - c;
-        if (lane == 31) {
-            sh[96] = ia;
-            sh[97] = ib;
-            sh[98] = ic;
+            sh[32 * j + lane] = ix - x;
+            if (lane == 31)
+                sh[128 + j] = ix;
         }
     }
     __syncthreads();
-    Scan3 r;
-    r.a = sh[warp] + inc.a - v.a;
-    r.b = sh[32 + warp] + inc.b - v.b;
-    r.c = sh[64 + warp] + inc.c - v.c;
-    total.a = sh[96];
-    total.b = sh[97];
-    total.c = sh[98];
+    int r[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        r[j] = sh[32 * j + warp] + inc[j] - in[j];
+    total = {sh[128], sh[129], sh[130], sh[131]};
     __syncthreads();
-    return r;
+    return {r[0], r[1], r[2], r[3]};
 }
 
 struct MapArgs {
     MapDev m;
     const int32_t *off, *ids;
     const float *alpha;
-    int T, P, cap, nw, staged, tile_bound;
+    int T, P, cap, nw, staged, tile_bound, mtile_bound;
 };
+
 
 __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
 {
     extern __shared__ int32_t sh[];
-    __shared__ int s_scan[3 * 32 + 3];
+    __shared__ int s_scan[4 * 32 + 4];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, P = a.P, cap = a.cap, nw = a.nw;
     MapDev &m = a.m;
@@ -151,10 +142,13 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
             m.pos[p] = -1;
         for (int i = tid; i < a.tile_bound; i += MAP_THREADS)
             m.tile[i] = make_int4(0, 0, 0, -1);
+        for (int i = tid; i < a.mtile_bound; i += MAP_THREADS)
+            m.mtile[i] = make_int4(0, 0, 0, -1);
         if (tid == 0) {
             m.hdr[HDR_U] = 0;
             m.hdr[HDR_PVALID] = 0;
             m.hdr[HDR_NTILES] = 0;
+            m.hdr[HDR_NMTILES] = 0;
             m.hdr[HDR_T] = T;
             m.hdr[HDR_STATUS] = LORA_DEV_BAD_OFFSETS;
             m.seg_start[0] = 0;
@@ -162,7 +156,10 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         return;
     }
 
-    // 2. token of each pair; per-warp histograms
+    // 2. token of each pair (and a copy of the offsets for the token-tile
+    // expand); per-warp histograms
+    for (int t = tid; t <= T; t += MAP_THREADS)
+        m.toff[t] = off[t];
     for (int t = tid; t < T; t += MAP_THREADS) {
         const int p0 = off[t], p1 = off[t + 1];
         for (int p = p0; p < p1; ++p)
@@ -189,16 +186,16 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
     __syncthreads();
 
     // 3. scan over bins, 1024 bins per round, bin-ascending
-    Scan3 carry = {0, 0, 0};
+    Scan4 carry = {0, 0, 0, 0};
     for (int base = 0; base < cap; base += MAP_THREADS) {
         const int b = base + tid;
         int c = 0;
         if (b < cap)
             for (int w = 0; w < nw; ++w)
                 c += hist[w * cap + b];
-        const Scan3 mine = {c, c > 0 ? 1 : 0, (c + SHRINK_TT - 1) / SHRINK_TT};
-        Scan3 tot;
-        const Scan3 ex = block_exclusive_scan3(mine, tot, s_scan);
+        const Scan4 mine = {c, c > 0 ? 1 : 0, (c + SHRINK_TT - 1) / SHRINK_TT, (c + MMA_TM - 1) / MMA_TM};
+        Scan4 tot;
+        const Scan4 ex = block_exclusive_scan4(mine, tot, s_scan);
         if (c > 0) {
             int run = carry.a + ex.a;
             const int sidx = carry.b + ex.b, tix = carry.c + ex.c;
@@ -208,6 +205,8 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
             bin_tile[b] = tix;
             for (int i = 0; i < mine.c; ++i)
                 m.tile[tix + i] = make_int4(b, run + i * SHRINK_TT, min(SHRINK_TT, c - i * SHRINK_TT), sidx);
+            for (int i = 0, mix = carry.d + ex.d; i < mine.d; ++i)
+                m.mtile[mix + i] = make_int4(b, run + i * MMA_TM, min(MMA_TM, c - i * MMA_TM), sidx);
             for (int w = 0; w < nw; ++w) {
                 const int v = hist[w * cap + b];
                 hist[w * cap + b] = run;
@@ -217,13 +216,17 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         carry.a += tot.a;
         carry.b += tot.b;
         carry.c += tot.c;
+        carry.d += tot.d;
     }
     for (int i = carry.c + tid; i < a.tile_bound; i += MAP_THREADS)
         m.tile[i] = make_int4(0, 0, 0, -1);  // empty slots up to the host-known bound
+    for (int i = carry.d + tid; i < a.mtile_bound; i += MAP_THREADS)
+        m.mtile[i] = make_int4(0, 0, 0, -1);
     if (tid == 0) {
         m.hdr[HDR_U] = carry.b;
         m.hdr[HDR_PVALID] = carry.a;
         m.hdr[HDR_NTILES] = carry.c;
+        m.hdr[HDR_NMTILES] = carry.d;
         m.hdr[HDR_T] = T;
         m.seg_start[carry.b] = carry.a;
     }
@@ -272,6 +275,14 @@ int shrink_tile_bound(int P, int capacity)
     return (int)(b < P ? b : P);
 }
 
+int mma_tile_bound(int P, int capacity)
+{
+    if (P <= 0)
+        return 0;
+    const long long b = (long long)(P + MMA_TM - 1) / MMA_TM + (P < capacity ? P : capacity);
+    return (int)(b < P ? b : P);
+}
+
 cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const int32_t *ids,
                                  const float *alpha, int T, int P, int capacity, int max_pairs,
                                  cudaStream_t st)
@@ -306,7 +317,8 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
             return e;
         attr_done = dev;
     }
-    MapArgs a{m, offsets, ids, alpha, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity)};
+    MapArgs a{m, offsets, ids, alpha, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity),
+              mma_tile_bound(P, capacity)};
     k_build_mapping<<<1, MAP_THREADS, smem, st>>>(a);
     return cudaGetLastError();
 }

@@ -127,6 +127,7 @@ def test_mapping_bad_offsets_and_degenerate():
 APPLY_CASES = ["tiny", "distinct", "zipf", "sweep1", "sweep8", "sweep64", "sweep256"]
 PATH_AUTO, PATH_SPLIT, PATH_FUSED, PATH_MMA = 0, 1, 2, 3
 DECODE_PATHS = [PATH_AUTO, PATH_SPLIT, PATH_FUSED]
+ALL_PATHS = [PATH_AUTO, PATH_SPLIT, PATH_FUSED, PATH_MMA]
 
 
 @pytest.mark.parametrize("name", APPLY_CASES)
@@ -138,7 +139,7 @@ def test_apply_matches_oracle(name):
     stated_gate(y, yref)
 
 
-@pytest.mark.parametrize("path", DECODE_PATHS)
+@pytest.mark.parametrize("path", ALL_PATHS)
 @pytest.mark.parametrize("name", APPLY_CASES)
 def test_apply_delta_only(name, path):
     wl = W.make(name, y_zero=True)
@@ -148,9 +149,10 @@ def test_apply_delta_only(name, path):
     delta_gate(y, acc)
 
 
-def test_prefill_small_delta_only():
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_SPLIT, PATH_MMA])
+def test_prefill_small_delta_only(path):
     wl = W.sparse_prefill(n_requests=3, y_zero=True)
-    y, st = run_gpu(wl)
+    y, st = run_gpu(wl, path=path)
     _, acc, ost = oracle.apply_workload(wl, threads=0)
     assert st == ost == 0
     delta_gate(y, acc)
@@ -170,12 +172,13 @@ def test_paths_agree_bitwise_where_order_matches():
         np.testing.assert_array_equal(r, runs[0])
 
 
-def test_prefill_full_size_sampled():
-    """The full sparse-prefill batch in the benchmark's launch configuration;
-    the oracle checks sampled tokens (first/last of the batch, request
-    boundaries, random)."""
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_SPLIT])
+def test_prefill_full_size_sampled(path):
+    """The full sparse-prefill batch in the benchmark's launch configuration
+    (the dispatch table sends it to the tensor-core path); the oracle checks
+    sampled tokens (first/last of the batch, random)."""
     wl = W.sparse_prefill(y_zero=True)
-    y, st = run_gpu(wl)
+    y, st = run_gpu(wl, path=path)
     assert st == 0
     rng = np.random.default_rng(0)
     toks = sorted(set([0, 1, wl.T - 1, wl.T // 2] + list(rng.choice(wl.T, 40, replace=False))))
@@ -185,26 +188,28 @@ def test_prefill_full_size_sampled():
 
 
 # ---------------------------------------------------------------- contracts
-def test_garbage_padding_is_inert():
+@pytest.mark.parametrize("path", ALL_PATHS)
+def test_garbage_padding_is_inert(path):
     zero = W.rank_sweep(64)
     garb = W.rank_sweep(64, garbage_padding=True)
-    y0, _ = run_gpu(zero)
-    y1, _ = run_gpu(garb)
+    y0, _ = run_gpu(zero, path=path)
+    y1, _ = run_gpu(garb, path=path)
     np.testing.assert_array_equal(y0, y1)
 
 
-def test_rank_override_and_bad_rank():
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA])
+def test_rank_override_and_bad_rank(path):
     wl = W.rank_sweep(64, y_zero=True)
     rng = np.random.default_rng(5)
     ranks = np.minimum(wl.ranks, rng.integers(0, 65, size=wl.capacity)).astype(np.int32)
-    y, st = run_gpu(wl, ranks=ranks)
+    y, st = run_gpu(wl, ranks=ranks, path=path)
     _, acc, _ = oracle.apply_workload(wl, ranks=ranks)
     assert st == 0
     delta_gate(y, acc)
     bad = ranks.copy()
     victim = int(wl.ids[0])
     bad[victim] = wl.r_max + 5
-    y, st = run_gpu(wl, ranks=bad)
+    y, st = run_gpu(wl, ranks=bad, path=path)
     assert st & 8
     ok = bad.copy()
     ok[victim] = 0
@@ -212,14 +217,15 @@ def test_rank_override_and_bad_rank():
     delta_gate(y, acc)
 
 
-def test_unregistered_slot():
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA])
+def test_unregistered_slot(path):
     wl = W.zipf_decode(y_zero=True)
     victim = int(wl.ids[1])
     reg = wl.ranks.copy()
     reg[victim] = -1
     dw = DeviceWorkload(wl, register_ranks=reg)
     try:
-        y = dw.apply(y=torch.zeros_like(dw.y0))
+        y = dw.apply(y=torch.zeros_like(dw.y0), path=path)
         st = dw.mapping.status()
     finally:
         dw.close()
@@ -229,7 +235,7 @@ def test_unregistered_slot():
     delta_gate(bf16_to_numpy_bits(y), acc)
 
 
-@pytest.mark.parametrize("path", DECODE_PATHS)
+@pytest.mark.parametrize("path", ALL_PATHS)
 def test_deterministic(path):
     wl = W.rank_sweep(256)
     dw = DeviceWorkload(wl)
@@ -241,13 +247,14 @@ def test_deterministic(path):
     np.testing.assert_array_equal(a, b)
 
 
-def test_noops():
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA])
+def test_noops(path):
     wl = W.tiny()
     wl.alpha[:] = 0
-    y, _ = run_gpu(wl)
+    y, _ = run_gpu(wl, path=path)
     np.testing.assert_array_equal(bf16_bits_to_f32(y), bf16_bits_to_f32(wl.y))
     wl = W.tiny()
-    y, _ = run_gpu(wl, ranks=np.zeros(wl.capacity, np.int32))
+    y, _ = run_gpu(wl, ranks=np.zeros(wl.capacity, np.int32), path=path)
     np.testing.assert_array_equal(bf16_bits_to_f32(y), bf16_bits_to_f32(wl.y))
 
 
@@ -293,20 +300,21 @@ def _custom(rng, d_in, d_out, r, cap, lists, ranks=None):
                          alpha_lists=alpha_lists, ranks=ranks, y_sigma=0.0)
 
 
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA])
 @pytest.mark.parametrize("ntok", [300, 200])
-def test_big_segments_and_many_pairs_per_token(ntok):
+def test_big_segments_and_many_pairs_per_token(ntok, path):
     """Segments far longer than a shrink tile or an expand job, one token with
     40 pairs, an empty token; 200 tokens also runs the fused path."""
     rng = np.random.default_rng(21)
     lists = [[0, 1, 2] for _ in range(ntok)] + [list(rng.permutation(64)[:40])] + [[]] + [[5]]
     wl = _custom(rng, 128, 192, 16, 64, lists)
-    y, st = run_gpu(wl)
+    y, st = run_gpu(wl, path=path)
     _, acc, _ = oracle.apply_workload(wl)
     assert st == 0
     delta_gate(y, acc)
 
 
-@pytest.mark.parametrize("path", DECODE_PATHS)
+@pytest.mark.parametrize("path", ALL_PATHS)
 @pytest.mark.parametrize("d_in,d_out,r,k", [(64, 128, 1, 1), (6208, 64, 5, 3), (14336, 4096, 8, 8),
                                             (256, 256, 64, 64), (192, 320, 13, 7)])
 def test_shapes(d_in, d_out, r, k, path):
@@ -319,6 +327,24 @@ def test_shapes(d_in, d_out, r, k, path):
     y, st = run_gpu(wl, path=path)
     _, acc, _ = oracle.apply_workload(wl)
     delta_gate(y, acc)
+
+
+def test_mma_many_adapters_and_pairs_per_tile():
+    """Tensor-core path: a 128-token tile whose pairs name more adapters than
+    one listing window holds (8 distinct of 2048 per token) and more pairs
+    than the tile's pair cache; duplicates of one adapter within a token;
+    token tiles with no pair; a ragged last tile."""
+    rng = np.random.default_rng(33)
+    cap = 2048
+    lists = [list(rng.permutation(cap)[:8]) for _ in range(130)]
+    lists += [[] for _ in range(140)]
+    lists += [[7, 7, 9] for _ in range(3)]
+    wl = _custom(rng, 64, 128, 4, cap, lists)
+    for path in (PATH_MMA, PATH_SPLIT):
+        y, st = run_gpu(wl, path=path)
+        _, acc, _ = oracle.apply_workload(wl)
+        assert st == 0
+        delta_gate(y, acc)
 
 
 def test_no_pairs_leaves_y():
