@@ -224,6 +224,40 @@ const char *lora_status_string(lora_status s);
 /* lora_version: the library version string. */
 const char *lora_version(void);
 
+/*
+ * lora_delta_apply_noalloc: one whole batch -- the mapping, then the
+ * segment shrink and the token-block RowExpand (the split path) -- with
+ * every scratch array in one fixed, statically allocated device buffer of
+ * LORA_NOALLOC_SCRATCH_BYTES, so the call allocates no device memory and
+ * needs no lora_mapping.  The pages describe no such interface: it is an
+ * operational variant of lora_build_mapping + lora_delta_apply_path(SPLIT).
+ *
+ * For callers that cannot allocate per call: a serving loop whose caching
+ * allocator already holds the spare device memory (cudaMalloc would fail),
+ * or code that must not call cudaMalloc / cudaFree, which may synchronise
+ * the device.
+ *   x_dev, y_dev, pool, ranks_dev : as for lora_delta_apply
+ *   offsets_dev, ids_dev, alpha_dev, T, P : as for lora_build_mapping
+ *   status_dev : NULL, or a device int32 that receives this call's
+ *                LORA_DEV_* bits (stream-ordered)
+ * Scratch for a batch: about P * (30 + 4 * round4(r_max)) + 64 * min(P,
+ * capacity) + 8 * capacity + 4 * T bytes, in 256-byte aligned pieces.  A batch whose layout
+ * exceeds LORA_NOALLOC_SCRATCH_BYTES returns LORA_ERR_NOT_SUPPORTED before
+ * launching anything.  The scratch header (status word and counters) is
+ * zeroed on the stream at the start of every call; every other scratch
+ * array is written before it is read.
+ * The first call on a device does set-up (looks up the buffer's device
+ * address, sets kernel attributes); make it before any stream capture.
+ * There is one buffer per device: calls whose work overlaps in time (on
+ * different streams, or from several host threads) race on it and must be
+ * serialised, e.g. by issuing them on one stream.
+ */
+#define LORA_NOALLOC_SCRATCH_BYTES (4 << 20)
+lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, const lora_pool *pool,
+                                     const int32_t *ranks_dev, const int32_t *offsets_dev,
+                                     const int32_t *ids_dev, const float *alpha_dev, int T, int P,
+                                     int32_t *status_dev, lora_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -545,3 +545,116 @@ lora_status lora_mapping_destroy(lora_mapping *m)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation variant
+namespace {
+
+// The fixed scratch of lora_delta_apply_noalloc (one per device).
+__device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
+
+struct NoallocLayout {
+    size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, z;
+    size_t total;
+};
+
+NoallocLayout noalloc_layout(int T, int P, int capacity, int r_max)
+{
+    NoallocLayout L;
+    size_t off = 0;
+    auto take = [&off](size_t bytes) {
+        const size_t o = off;
+        off += (bytes + 255) & ~static_cast<size_t>(255);
+        return o;
+    };
+    const size_t p = P > 0 ? (size_t)P : 1;
+    const size_t tiles = (size_t)(P > 0 ? shrink_tile_bound(P, capacity) : 1);
+    const size_t mtiles = (size_t)(P > 0 ? mma_tile_bound(P, capacity) : 1);
+    L.tok = take(4 * p);
+    L.adapter = take(4 * p);
+    L.src = take(4 * p);
+    L.pos = take(4 * p);
+    L.alpha = take(4 * p);
+    L.tmp_tok = take(4 * p);
+    L.seg_adapter = take(4 * (size_t)capacity);
+    L.seg_start = take(4 * ((size_t)capacity + 1));
+    L.tile = take(16 * tiles);
+    L.tile_tok = take(4 * tiles * SHRINK_TT);
+    L.hdr = take(4 * (size_t)HDR_WORDS);
+    L.mtile = take(16 * mtiles);
+    L.toff = take(4 * ((size_t)T + 1));
+    L.z = take(4 * p * (size_t)z_stride(r_max));
+    L.total = off;
+    return L;
+}
+
+// Device address of the scratch on the current device (looked up once per device).
+unsigned char *noalloc_base()
+{
+    constexpr int MAX_DEVICES = 64;
+    static unsigned char *base[MAX_DEVICES] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
+        return nullptr;
+    if (!base[dev]) {
+        unsigned char *ptr = nullptr;
+        if (cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch) != cudaSuccess)
+            return nullptr;
+        base[dev] = ptr;
+    }
+    return base[dev];
+}
+
+}  // namespace
+
+extern "C" lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, const lora_pool *pool,
+                                                const int32_t *ranks_dev, const int32_t *offsets_dev,
+                                                const int32_t *ids_dev, const float *alpha_dev, int T, int P,
+                                                int32_t *status_dev, lora_stream_t stream)
+{
+    if (!x_dev || !y_dev || !pool || !offsets_dev || x_dev == y_dev || T < 0 || P < 0)
+        return LORA_ERR_INVALID_ARG;
+    if (P > 0 && (!ids_dev || !alpha_dev))
+        return LORA_ERR_INVALID_ARG;
+    if (!aligned16(x_dev) || !aligned16(y_dev))
+        return LORA_ERR_INVALID_ARG;
+    if (T > LORA_MAX_TOKENS || P > LORA_MAX_PAIRS)
+        return LORA_ERR_NOT_SUPPORTED;
+    const NoallocLayout L = noalloc_layout(T, P, pool->capacity, pool->r_max);
+    if (L.total > (size_t)LORA_NOALLOC_SCRATCH_BYTES)
+        return LORA_ERR_NOT_SUPPORTED;  // batch too large for the fixed scratch
+    unsigned char *base = noalloc_base();
+    if (!base)
+        return LORA_ERR_CUDA;
+    MapDev d = {};
+    d.tok = reinterpret_cast<int32_t *>(base + L.tok);
+    d.adapter = reinterpret_cast<int32_t *>(base + L.adapter);
+    d.src = reinterpret_cast<int32_t *>(base + L.src);
+    d.pos = reinterpret_cast<int32_t *>(base + L.pos);
+    d.alpha = reinterpret_cast<float *>(base + L.alpha);
+    d.tmp_tok = reinterpret_cast<int32_t *>(base + L.tmp_tok);
+    d.seg_adapter = reinterpret_cast<int32_t *>(base + L.seg_adapter);
+    d.seg_start = reinterpret_cast<int32_t *>(base + L.seg_start);
+    d.tile = reinterpret_cast<int4 *>(base + L.tile);
+    d.tile_tok = reinterpret_cast<int32_t *>(base + L.tile_tok);
+    d.hdr = reinterpret_cast<int32_t *>(base + L.hdr);
+    d.mtile = reinterpret_cast<int4 *>(base + L.mtile);
+    d.toff = reinterpret_cast<int32_t *>(base + L.toff);
+    d.z = reinterpret_cast<float *>(base + L.z);
+    d.partial = nullptr;  // used by the fused kernel only
+    d.partial_ctas = 0;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(d.hdr, 0, HDR_WORDS * sizeof(int32_t), st);
+    if (e == cudaSuccess)
+        e = launch_build_mapping(d, offsets_dev, ids_dev, alpha_dev, T, P, pool->capacity, P, st);
+    if (e == cudaSuccess && T > 0 && P > 0) {
+        const PoolDev pd = pool_dev(pool);
+        e = launch_shrink(static_cast<const __nv_bfloat16 *>(x_dev), pd, ranks_dev, d, P, sm_count(), st);
+        if (e == cudaSuccess)
+            e = launch_expand(static_cast<__nv_bfloat16 *>(y_dev), pd, ranks_dev, d, T,
+                              choose_expand_plan(T, pool->d_out), /*pdl=*/true, st);
+    }
+    if (e == cudaSuccess && status_dev)
+        e = cudaMemcpyAsync(status_dev, d.hdr + HDR_STATUS, sizeof(int32_t), cudaMemcpyDeviceToDevice, st);
+    return from_cuda(e);
+}

@@ -41,8 +41,10 @@ EXPORTS = [
     "lora_pool_create", "lora_pool_register", "lora_pool_unregister", "lora_pool_destroy",
     "lora_mapping_create", "lora_build_mapping", "lora_delta_apply", "lora_delta_apply_path",
     "lora_dispatch_choose", "lora_delta_apply_host", "lora_mapping_status", "lora_mapping_export",
-    "lora_mapping_destroy", "lora_status_string", "lora_version",
+    "lora_mapping_destroy", "lora_status_string", "lora_version", "lora_delta_apply_noalloc",
 ]
+
+LORA_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class LoraError(RuntimeError):
@@ -78,6 +80,7 @@ def load(path: str | None = None):
         "lora_delta_apply_path": ([V, V, V, V, V, I, V], I),
         "lora_dispatch_choose": ([I, I, I, I, I], I),
         "lora_delta_apply_host": ([V, V, V, V, V, I, I, V, V, V, V], I),
+        "lora_delta_apply_noalloc": ([V, V, V, V, V, V, V, I, I, V, V], I),
         "lora_mapping_status": ([V, V, ctypes.POINTER(ctypes.c_int)], I),
         "lora_mapping_export": ([V, V, V, V, V, V, V, V, V, V], I),
         "lora_mapping_destroy": ([V], I),
@@ -174,6 +177,13 @@ def lora_delta_apply_host(x_host, y_host, offsets_host, ids_host, alpha_host, T:
     _check("lora_delta_apply_host",
            load().lora_delta_apply_host(_ptr(x_host), _ptr(y_host), _ptr(offsets_host), _ptr(ids_host),
                                         _ptr(alpha_host), T, P, pool, _ptr(ranks), m, _stream(stream)))
+
+
+def lora_delta_apply_noalloc(x, y, pool: int, ranks, offsets, ids, alpha, T: int, P: int,
+                             status=None, stream=None):
+    _check("lora_delta_apply_noalloc",
+           load().lora_delta_apply_noalloc(_ptr(x), _ptr(y), pool, _ptr(ranks), _ptr(offsets), _ptr(ids),
+                                           _ptr(alpha), T, P, _ptr(status), _stream(stream)))
 
 
 def lora_mapping_status(m: int, stream=None) -> int:
