@@ -114,7 +114,7 @@ cudaError_t launch_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev
 // dependent launch.  Tensor maps of the pool are encoded once per pool.
 struct MmaMaps {
     alignas(64) unsigned char At[128];  // CUtensorMap over At: [capacity * r_max][d_in]
-    alignas(64) unsigned char B[128];   // CUtensorMap over B:  [capacity * r_max][d_out]
+    alignas(64) unsigned char B[128];   // CUtensorMap over B:  {64, capacity * r_max, d_out / 64}
     bool ready;
 };
 cudaError_t mma_encode_maps(const PoolDev &pool, MmaMaps &maps);

@@ -14,8 +14,9 @@
 //    the cluster adds them in rank order through distributed shared memory
 //    (deterministic), scales by alpha and writes z[q][j], j < k.
 //
-// 2. Token-tile expand (RowExpand as a dense product): a CTA owns MMA_TM
-//    consecutive tokens x BN output columns.  Its pairs' adapters, in
+// 2. Token-tile expand (RowExpand as a dense product): a unit is MMA_TM
+//    consecutive tokens x BN output columns; a persistent CTA per SM takes a
+//    contiguous run of units (mostly of one token tile).  The tile's adapters, in
 //    ascending id order, each give ceil(k / 16) "slots" of 16 rank rows; the
 //    A operand holds, per token and slot, the sum of the token's z rows for
 //    that adapter (zero elsewhere), split into a bf16 high part and a bf16
@@ -23,9 +24,11 @@
 //    B operand is B_a[16c .. 16c + 15, columns] loaded by TMA in the
 //    MN-major 128-byte swizzled layout (B is stored row-major, d_out
 //    contiguous).  D (128 x BN fp32) accumulates in tensor memory over all
-//    slots; the epilogue adds y and rounds once to bf16.  Rank rows at or
-//    beyond k of a partial chunk are zeroed in shared memory before use, so
-//    padding never reaches the sum.
+//    slots, in two buffers so that one unit's epilogue (y + D, rounded once
+//    to bf16) overlaps the next unit's MMAs; one warp streams B and issues
+//    the MMAs, eight build the operand and run the epilogue.  Rank rows at
+//    or beyond k of a partial chunk are zeroed in shared memory before use,
+//    so padding never reaches the sum.
 //
 // LoRAForge page, "Approach" (5) (a path fixed per phase and shape) and the
 // DyMerge-LoRA page, "Core idea" (tuples reordered by adapter so that one CTA
@@ -231,13 +234,14 @@ __global__ void __launch_bounds__(MS_THREADS, 1)
 
 // ---------------------------------------------------------------- expand
 
-constexpr int ME_THREADS = 256;
-constexpr int ME_SP = 8;                            // slots (16 rank rows each) per pass
-constexpr int ME_Z_BYTES = MMA_TM * ME_SP * 16 * 2;  // one of hi / lo: 128 rows x 128 bf16
-constexpr int ME_STAGES = 4;
-constexpr int ME_B_BYTES = 16 * 256 * 2;            // 16 rank rows x up to 256 columns
-constexpr int ME_PT_MAX = 512;                      // pairs of a tile cached in shared memory
-constexpr int ME_NU_MAX = 512;                      // adapters listed per window
+constexpr int ME_WORKERS = 256;                        // warps 0-7: lists, A operand, epilogue
+constexpr int ME_THREADS = ME_WORKERS + 64;            // warp 8: MMA issue; warp 9: B chunks by TMA
+constexpr int ME_SMAX = 16;                            // slots per A-operand build
+constexpr int ME_Z_BYTES = MMA_TM * ME_SMAX * 16 * 2;  // one of hi / lo: 128 rows x 256 bf16
+constexpr int ME_STAGES = 8;
+constexpr int ME_B_BYTES = 16 * 256 * 2;               // 16 rank rows x up to 256 columns
+constexpr int ME_PT_MAX = 512;                         // pairs of a tile cached in shared memory
+constexpr int ME_NU_MAX = 512;                         // adapters listed per window
 
 struct MmaExpandArgs {
     __nv_bfloat16 *y;
@@ -245,28 +249,44 @@ struct MmaExpandArgs {
     const int32_t *ranks;
     MapDev m;
     int T, zs;
+    int n_nt;   // column tiles: d_out / BN
+    int units;  // token tiles x column tiles
 };
 
 // Dynamic shared memory of the expand kernel (offsets from a 1024-aligned base).
 struct MeLayout {
-    int zhi, zlo, b, cache, list, lrank, sbase, toff, bitmap, total;
+    int zhi, zlo, b, cache, list, lrank, sbase, toff, bitmap, wpre, total;
     __host__ __device__ explicit MeLayout(int capacity)
     {
+        const int words = (((capacity + 31) / 32) + 3) & ~3;
         zhi = 0;
         zlo = zhi + ME_Z_BYTES;
         b = zlo + ME_Z_BYTES;
-        cache = b + ME_STAGES * ME_B_BYTES;      // int2 [ME_PT_MAX]: sorted position, adapter
-        list = cache + ME_PT_MAX * 8;            // int [ME_NU_MAX]: adapters of the window
-        lrank = list + ME_NU_MAX * 4;            // int [ME_NU_MAX]: their ranks
-        sbase = lrank + ME_NU_MAX * 4;           // int [ME_NU_MAX + 1]: first slot of each
-        toff = sbase + (ME_NU_MAX + 4) * 4;      // int [MMA_TM + 1]: pair offsets of the tile's tokens
-        bitmap = toff + (MMA_TM + 4) * 4;        // uint32 [ceil(capacity / 32)]
-        total = bitmap + ((capacity + 31) / 32) * 4 + 1024;
+        cache = b + ME_STAGES * ME_B_BYTES;  // int2 [ME_PT_MAX]: sorted position, adapter (-1: none)
+        list = cache + ME_PT_MAX * 8;        // int [ME_NU_MAX]: adapters of the window, ascending
+        lrank = list + ME_NU_MAX * 4;        // int [ME_NU_MAX]: their ranks
+        sbase = lrank + ME_NU_MAX * 4;       // int [ME_NU_MAX + 1]: first slot of each
+        toff = sbase + (ME_NU_MAX + 4) * 4;  // int [MMA_TM + 1]: pair offsets of the tile's tokens
+        bitmap = toff + (MMA_TM + 4) * 4;    // uint32 [words]: adapters of the tile with k > 0
+        wpre = bitmap + words * 4;           // int [words]: set bits before each word
+        total = wpre + words * 4 + 1024;
     }
 };
 
-// Block-wide exclusive scan of one int over ME_THREADS threads.
-__device__ __forceinline__ int me_scan(int v, int &total, int *sh /* [ME_THREADS / 32 + 1] */)
+// One A-operand build, handed from the workers to the MMA warp.
+struct MeBuild {
+    int u0, u1;       // units [u0, u1) take their slots [s0, s1) from this build
+    int s0, s1;       // window slots held (operand column block jj = s - s0)
+    int nu;           // adapters in the window lists
+    int first, last;  // the build starts / ends each unit's sum
+    int gi0;          // running index (in this CTA) of unit u0; accumulator buffer = index % 2
+    int done;         // no further builds
+};
+
+__device__ __forceinline__ void me_bar() { asm volatile("bar.sync 1, %0;" ::"n"(ME_WORKERS) : "memory"); }
+
+// Exclusive scan of one int over the ME_WORKERS worker threads.
+__device__ __forceinline__ int me_scan(int v, int &total, int *sh /* [ME_WORKERS / 32 + 1] */)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int inc = v;
@@ -278,20 +298,20 @@ __device__ __forceinline__ int me_scan(int v, int &total, int *sh /* [ME_THREADS
     }
     if (lane == 31)
         sh[warp] = inc;
-    __syncthreads();
+    me_bar();
     if (threadIdx.x == 0) {
         int run = 0;
-        for (int w = 0; w < ME_THREADS / 32; ++w) {
+        for (int w = 0; w < ME_WORKERS / 32; ++w) {
             const int t = sh[w];
             sh[w] = run;
             run += t;
         }
-        sh[ME_THREADS / 32] = run;
+        sh[ME_WORKERS / 32] = run;
     }
-    __syncthreads();
+    me_bar();
     const int r = sh[warp] + inc - v;
-    total = sh[ME_THREADS / 32];
-    __syncthreads();
+    total = sh[ME_WORKERS / 32];
+    me_bar();
     return r;
 }
 
@@ -309,101 +329,265 @@ __device__ __forceinline__ int me_slot_owner(const int *sbase, int nu, int j)
     return lo;
 }
 
+// Token row of the tile owning pair offset i (last row with toff[row] - p0 <= i).
+__device__ __forceinline__ int me_pair_row(const int *toff, int nrows, int p0, int i)
+{
+    int lo = 0, hi = nrows;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (toff[mid] - p0 <= i)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// The B producer warp (lane 0): for each build, streams the B chunks of its
+// (unit, slot) sequence through a ring of ME_STAGES stages -- one 3-D TMA box
+// {64 columns, 16 rank rows, BN / 64 column blocks} per chunk, which lands in
+// the MN-major swizzled operand layout -- refilling a stage as soon as the
+// MMAs that read it complete.  Per-slot rows are resolved once per build.
 template <int BN>
-__global__ void __launch_bounds__(ME_THREADS, 2)
+__device__ __forceinline__ void me_producer_warp(const CUtensorMap &map_b, const MmaExpandArgs &a,
+                                                 unsigned char *smem, const MeLayout &L, uint64_t *full_b,
+                                                 uint64_t *empty_b, uint64_t *zready, const MeBuild *s_build,
+                                                 int32_t *status)
+{
+    if ((threadIdx.x & 31) != 0)
+        return;
+    unsigned char *sb = smem + L.b;
+    const int *list = reinterpret_cast<const int *>(smem + L.list);
+    const int *sbase = reinterpret_cast<const int *>(smem + L.sbase);
+    const int r_max = a.pool.r_max;
+    int g = 0;  // ring sequence
+    for (int nb = 0;; ++nb) {
+        if (!mbar_wait_bounded(zready, nb & 1, status))
+            return;
+        const MeBuild bd = *s_build;
+        if (bd.done)
+            return;
+        const int nsl = bd.s1 - bd.s0;
+        int rows[ME_SMAX];
+#pragma unroll
+        for (int j = 0; j < ME_SMAX; ++j) {
+            rows[j] = 0;
+            if (j < nsl) {
+                const int s = bd.s0 + j, ui = me_slot_owner(sbase, bd.nu, s);
+                rows[j] = list[ui] * r_max + 16 * (s - sbase[ui]);
+            }
+        }
+        for (int uu = bd.u0; uu < bd.u1; ++uu) {
+            const int z0 = (uu % a.n_nt) * (BN / 64);
+#pragma unroll
+            for (int j = 0; j < ME_SMAX; ++j) {
+                if (j < nsl) {
+                    const int gs = g++, st = gs % ME_STAGES;
+                    if (gs >= ME_STAGES && !mbar_wait_bounded(&empty_b[st], ((gs / ME_STAGES) - 1) & 1, status))
+                        return;
+                    mbar_arrive_expect_tx(&full_b[st], 16 * BN * 2);
+                    tma_load_3d(sb + st * ME_B_BYTES, &map_b, 0, rows[j], z0, &full_b[st]);
+                }
+            }
+        }
+    }
+}
+
+// The MMA warp: waits for each build, then per (unit, slot) for its B chunk,
+// masks rank rows >= k of a partial chunk, issues the hi and lo MMAs, frees
+// the stage, and commits a unit's accumulator once its last slot is issued.
+template <int BN>
+__device__ __forceinline__ void me_mma_warp(unsigned char *smem, const MeLayout &L, uint64_t *full_b,
+                                            uint64_t *empty_b, uint64_t *zready, uint64_t *zfree,
+                                            uint64_t *acc_full, uint64_t *acc_empty, const MeBuild *s_build,
+                                            uint32_t taddr, int32_t *status)
+{
+    const int lane = threadIdx.x & 31;
+    unsigned char *sb = smem + L.b;
+    const uint32_t zhi = smem_u32(smem + L.zhi), zlo = smem_u32(smem + L.zlo);
+    const int *lrank = reinterpret_cast<const int *>(smem + L.lrank);
+    const int *sbase = reinterpret_cast<const int *>(smem + L.sbase);
+    const uint32_t idesc = umma_idesc_bf16(MMA_TM, BN) | (1u << 16);  // B operand MN-major
+    int g = 0;                                                         // ring sequence
+    for (int nb = 0;; ++nb) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(zready, nb & 1, status)))
+            return;
+        const MeBuild bd = *s_build;
+        if (bd.done)
+            return;
+        const int nsl = bd.s1 - bd.s0;
+        int krs[ME_SMAX];  // rank rows of each slot's chunk (16 = full)
+#pragma unroll
+        for (int j = 0; j < ME_SMAX; ++j) {
+            krs[j] = 16;
+            if (j < nsl) {
+                const int s = bd.s0 + j, ui = me_slot_owner(sbase, bd.nu, s);
+                krs[j] = min(16, lrank[ui] - 16 * (s - sbase[ui]));
+            }
+        }
+        bool ok = true;
+        for (int uu = bd.u0; uu < bd.u1 && ok; ++uu) {
+            const int gi = bd.gi0 + (uu - bd.u0), b = gi & 1;
+            if (bd.first && gi >= 2) {
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&acc_empty[b], ((gi >> 1) - 1) & 1, status));
+                if (!ok)
+                    break;
+            }
+            const uint32_t dt = taddr + (uint32_t)(b * BN);
+#pragma unroll
+            for (int j = 0; j < ME_SMAX; ++j) {
+                if (j < nsl && ok) {
+                    const int gs = g++, st = gs % ME_STAGES;
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full_b[st], (gs / ME_STAGES) & 1, status));
+                    if (ok) {
+                        unsigned char *bs = sb + st * ME_B_BYTES;
+                        const int kr = krs[j];
+                        if (kr < 16) {
+                            const int nz = (16 - kr) * (BN / 64) * 8;  // 16-byte pieces of rank rows kr..15
+                            for (int e = lane; e < nz; e += 32) {
+                                const int piece = e & 7, rest = e >> 3;
+                                const int at = rest % (BN / 64), rr = kr + rest / (BN / 64);
+                                *reinterpret_cast<uint4 *>(bs + at * 2048 + (rr >> 3) * 1024 + (rr & 7) * 128 +
+                                                           piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            fence_proxy_async_smem();
+                        }
+                        __syncwarp();
+                        if (lane == 0) {
+                            tc_fence_after();
+                            const uint64_t bdesc = umma_desc_sw128_mn(smem_u32(bs), 2048, 1024);
+                            const uint32_t zo = (uint32_t)((j >> 2) * (MMA_TM * 128) + (j & 3) * 32);
+                            umma_bf16(dt, umma_desc_sw128(zhi + zo), bdesc, idesc, !(bd.first && j == 0));
+                            umma_bf16(dt, umma_desc_sw128(zlo + zo), bdesc, idesc, true);
+                            umma_commit(&empty_b[st]);
+                            if (bd.last && j == nsl - 1)
+                                umma_commit(&acc_full[b]);
+                        }
+                        __syncwarp();
+                    }
+                }
+            }
+        }
+        if (lane == 0)
+            umma_commit(zfree);  // the operand may be rebuilt once these MMAs complete
+        __syncwarp();
+        if (!ok)
+            return;
+    }
+}
+
+template <int BN>
+__global__ void __launch_bounds__(ME_THREADS, 1)
     k_mma_expand(const __grid_constant__ CUtensorMap map_b, const MmaExpandArgs a)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                             ~static_cast<uintptr_t>(1023));
     const MeLayout L(a.pool.capacity);
-    unsigned char *zhi = smem + L.zhi, *zlo = smem + L.zlo, *sb = smem + L.b;
+    __shared__ uint64_t full_b[ME_STAGES], empty_b[ME_STAGES], zready, zfree, acc_full[2], acc_empty[2];
+    __shared__ uint32_t s_taddr;
+    __shared__ int s_scan[ME_WORKERS / 32 + 1];
+    __shared__ MeBuild s_build;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int32_t *status = a.m.hdr + HDR_STATUS;
+    if (a.m.hdr[HDR_PVALID] == 0)
+        return;  // nothing valid in this batch (uniform)
+    const int G = gridDim.x;
+    const int u_begin = (int)((long long)blockIdx.x * a.units / G);
+    const int u_end = (int)((long long)(blockIdx.x + 1) * a.units / G);
+    if (tid == 0) {
+        for (int s = 0; s < ME_STAGES; ++s) {
+            mbar_init(&full_b[s], 1);
+            mbar_init(&empty_b[s], 1);
+        }
+        mbar_init(&zready, ME_WORKERS);
+        mbar_init(&zfree, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], ME_WORKERS);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == ME_WORKERS / 32) {
+        // z is written by the shrink: wait for it; tensor memory only after that
+        // (the shrink's CTAs hold tensor memory until they finish)
+        pdl_wait();
+        tmem_alloc(&s_taddr, 2 * BN);
+        tc_fence_before();
+        __syncthreads();  // (A) accumulator address visible
+        tc_fence_after();
+        const uint32_t taddr = s_taddr;
+        me_mma_warp<BN>(smem, L, full_b, empty_b, &zready, &zfree, acc_full, acc_empty, &s_build, taddr, status);
+        __syncwarp();
+        __syncthreads();  // (B) every epilogue has read its accumulator
+        tc_fence_after();
+        tmem_dealloc(taddr, 2 * BN);
+        return;
+    }
+    if (warp == ME_WORKERS / 32 + 1) {
+        __syncthreads();  // (A)
+        me_producer_warp<BN>(map_b, a, smem, L, full_b, empty_b, &zready, &s_build, status);
+        __syncwarp();
+        __syncthreads();  // (B)
+        return;
+    }
+
+    // ------------------------------------------------------------ workers
+    unsigned char *zhi = smem + L.zhi, *zlo = smem + L.zlo;
     int2 *cache = reinterpret_cast<int2 *>(smem + L.cache);
     int *list = reinterpret_cast<int *>(smem + L.list);
     int *lrank = reinterpret_cast<int *>(smem + L.lrank);
     int *sbase = reinterpret_cast<int *>(smem + L.sbase);
     int *toff = reinterpret_cast<int *>(smem + L.toff);
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem + L.bitmap);
-    __shared__ uint64_t full_b[ME_STAGES], empty_b[ME_STAGES], pass_done;
-    __shared__ uint32_t s_taddr;
-    __shared__ int s_scan[ME_THREADS / 32 + 1];
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int n0 = blockIdx.x * BN, t0 = blockIdx.y * MMA_TM;
-    const int nrows = min(MMA_TM, a.T - t0);
-    const int d_out = a.pool.d_out, r_max = a.pool.r_max;
+    int *wpre = reinterpret_cast<int *>(smem + L.wpre);
     const int nwords = (a.pool.capacity + 31) / 32;
-    int32_t *status = a.m.hdr + HDR_STATUS;
-    if (a.m.hdr[HDR_PVALID] == 0)
-        return;  // nothing valid in this batch (uniform)
+    const int d_out = a.pool.d_out;
 
-    // ---- the tile's pairs (mapping data: complete before the shrink started)
-    for (int i = tid; i <= nrows; i += ME_THREADS)
-        toff[i] = a.m.toff[t0 + i];
-    for (int i = tid; i < nwords; i += ME_THREADS)
-        bitmap[i] = 0u;
-    if (tid == 0) {
-        for (int s = 0; s < ME_STAGES; ++s) {
-            mbar_init(&full_b[s], 1);
-            mbar_init(&empty_b[s], 1);
-        }
-        mbar_init(&pass_done, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    const int p0 = toff[0], np = toff[nrows] - p0;
-    for (int i = tid; i < np; i += ME_THREADS) {
-        const int q = a.m.pos[p0 + i];
-        int ad = q >= 0 ? a.m.adapter[q] : -1;
-        if (ad >= 0 && effective_rank(a.pool, a.ranks, ad) <= 0)
-            ad = -1;  // contributes nothing
-        if (ad >= 0)
-            atomicOr(&bitmap[ad >> 5], 1u << (ad & 31));
-        if (i < ME_PT_MAX)
-            cache[i] = make_int2(q, ad);
-    }
-    __syncthreads();
-    int nu_total;
-    {
-        int c = 0;
-        for (int i = tid; i < nwords; i += ME_THREADS)
-            c += __popc(bitmap[i]);
-        me_scan(c, nu_total, s_scan);
-    }
-    if (nu_total == 0)
-        return;  // uniform: y stays as it is
-
-    const uint32_t idesc = umma_idesc_bf16(MMA_TM, BN) | (1u << 16);  // B operand MN-major
+    bool synced = false;
     uint32_t taddr = 0;
-    int gs_base = 0, gp = 0;
-    bool first_mma = true, ok = true;
-    for (int w0 = 0; w0 < nu_total; w0 += ME_NU_MAX) {
-        // ---- the window's adapters (ascending id), their ranks and first slots
-        int carry = 0;
-        for (int base = 0; base < nwords; base += ME_THREADS) {
-            const int wi = base + tid;
-            uint32_t word = wi < nwords ? bitmap[wi] : 0u;
-            int tot;
-            int ord = carry + me_scan(__popc(word), tot, s_scan);
+    int nb = 0, freed = 0, gi = 0;
+    auto wait_free = [&]() {  // every build handed over so far has been consumed
+        while (freed < nb) {
+            mbar_wait_bounded(&zfree, freed & 1, status);
+            ++freed;
+        }
+    };
+    auto publish = [&](int u0, int u1, int s0, int s1, int nu, int first, int last, int done) {
+        if (tid == 0)
+            s_build = MeBuild{u0, u1, s0, s1, nu, first, last, gi, done};
+        fence_proxy_async_smem();
+        mbar_arrive(&zready);
+        ++nb;
+    };
+    int t0 = 0, nrows = 0, p0 = 0, np = 0, nu_total = 0;
+
+    // lists of window w0: adapters of ordinals [w0, w0 + ME_NU_MAX), ranks, first slots; returns the slot count
+    auto build_lists = [&](int w0) -> int {
+        for (int wi = tid; wi < nwords; wi += ME_WORKERS) {
+            uint32_t word = bitmap[wi];
+            int ord = wpre[wi];
             while (word) {
-                const int b = __ffs(word) - 1;
+                const int bit = __ffs(word) - 1;
                 word &= word - 1u;
                 if (ord >= w0 && ord < w0 + ME_NU_MAX)
-                    list[ord - w0] = wi * 32 + b;
+                    list[ord - w0] = wi * 32 + bit;
                 ++ord;
             }
-            carry += tot;
         }
+        me_bar();
         const int nu = min(ME_NU_MAX, nu_total - w0);
-        __syncthreads();
         int scarry = 0;
-        for (int ub = 0; ub < nu; ub += ME_THREADS) {
+        for (int ub = 0; ub < nu; ub += ME_WORKERS) {
             const int u = ub + tid;
             int nch = 0;
             if (u < nu) {
@@ -419,76 +603,63 @@ __global__ void __launch_bounds__(ME_THREADS, 2)
         }
         if (tid == 0)
             sbase[nu] = scarry;
-        __syncthreads();
-        const int ns = scarry;
+        me_bar();
+        return scarry;
+    };
 
-        // ---- B chunks by TMA (warp 0, lane 0): slot j -> stage (gs_base + j) % ME_STAGES
-        int issued = 0;
-        auto issue_b = [&](int j) -> bool {
-            const int gs = gs_base + j, st = gs % ME_STAGES;
-            if (gs >= ME_STAGES && !mbar_wait_bounded(&empty_b[st], ((gs / ME_STAGES) - 1) & 1, status))
-                return false;
-            const int u = me_slot_owner(sbase, nu, j);
-            const int row = list[u] * r_max + 16 * (j - sbase[u]);
-            mbar_arrive_expect_tx(&full_b[st], 16 * BN * 2);
-#pragma unroll
-            for (int at = 0; at < BN / 64; ++at)
-                tma_load_2d(sb + st * ME_B_BYTES + at * 2048, &map_b, n0 + 64 * at, row, &full_b[st]);
-            return true;
-        };
-        if (warp == 0 && lane == 0)
-            while (ok && issued < ns && issued < ME_STAGES)
-                ok = issue_b(issued++);
-        __syncwarp();
-
-        if (w0 == 0) {
-            // z comes from the shrink: wait for it; tensor memory only after that
-            // (the shrink's CTAs hold tensor memory until they finish)
-            pdl_wait();
-            if (warp == 0)
-                tmem_alloc(&s_taddr, BN);
-            tc_fence_before();
-            __syncthreads();
-            tc_fence_after();
-            taddr = s_taddr;
+    // A operand for window slots [s0, s1): per token row and slot, the summed z as bf16 hi + lo
+    auto build_zsel = [&](int w0, int nu, int s0, int s1) {
+        const int nkb = (s1 - s0 + 3) >> 2;  // 64-column blocks in use
+        uint4 *zh4 = reinterpret_cast<uint4 *>(zhi), *zl4 = reinterpret_cast<uint4 *>(zlo);
+        for (int i = tid; i < nkb * (MMA_TM * 128 / 16); i += ME_WORKERS) {
+            zh4[i] = make_uint4(0u, 0u, 0u, 0u);
+            zl4[i] = make_uint4(0u, 0u, 0u, 0u);
         }
-
-        for (int j0 = 0; j0 < ns; j0 += ME_SP, ++gp) {
-            const int npass = min(ME_SP, ns - j0);
-            if (gp > 0 && !mbar_wait_bounded(&pass_done, (gp - 1) & 1, status))
-                ok = false;
-            // ---- A operand: per token row and slot, the summed z, as bf16 hi + lo
-            for (int idx = tid; idx < MMA_TM * npass; idx += ME_THREADS) {
-                const int row = idx & (MMA_TM - 1), jj = idx / MMA_TM, j = j0 + jj;
-                const int u = me_slot_owner(sbase, nu, j);
-                const int ad = list[u], c = j - sbase[u];
-                const int kk = min(16, lrank[u] - 16 * c);
+        me_bar();
+        auto pair_at = [&](int i) -> int2 {
+            if (i < ME_PT_MAX)
+                return cache[i];
+            const int q = a.m.pos[p0 + i];
+            return make_int2(q, q >= 0 ? a.m.adapter[q] : -1);
+        };
+        for (int i = tid; i < np; i += ME_WORKERS) {
+            const int2 qa = pair_at(i);
+            const int ad = qa.y;
+            if (ad < 0 || !((bitmap[ad >> 5] >> (ad & 31)) & 1u))
+                continue;
+            const int u = wpre[ad >> 5] + __popc(bitmap[ad >> 5] & ((1u << (ad & 31)) - 1u)) - w0;
+            if (u < 0 || u >= nu)
+                continue;
+            const int row = me_pair_row(toff, nrows, p0, i);
+            const int i_lo = toff[row] - p0, i_hi = toff[row + 1] - p0;
+            bool dup = false;  // an earlier pair of the token with the same adapter sums this one
+            for (int j = i_lo; j < i && !dup; ++j)
+                dup = pair_at(j).y == ad;
+            if (dup)
+                continue;
+            const int k = lrank[u], sb0 = sbase[u];
+            for (int c = 0; c < (k + 15) >> 4; ++c) {
+                const int s = sb0 + c;
+                if (s < s0 || s >= s1)
+                    continue;
+                const int jj = s - s0, kk = min(16, k - 16 * c);
                 float acc[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     acc[e] = 0.f;
-                if (row < nrows) {
-                    const int i0 = toff[row] - p0, i1 = toff[row + 1] - p0;
-                    for (int i = i0; i < i1; ++i) {
-                        int2 qa;
-                        if (i < ME_PT_MAX) {
-                            qa = cache[i];
-                        } else {
-                            const int q = a.m.pos[p0 + i];
-                            qa = make_int2(q, q >= 0 ? a.m.adapter[q] : -1);
-                        }
-                        if (qa.y != ad)
-                            continue;
-                        const float *zr = a.m.z + (size_t)qa.x * a.zs + 16 * c;
+                for (int j = i; j < i_hi; ++j) {
+                    const int2 qb = j == i ? qa : pair_at(j);
+                    if (qb.y != ad)
+                        continue;
+                    const float *zr = a.m.z + (size_t)qb.x * a.zs + 16 * c;
 #pragma unroll
-                        for (int j4 = 0; j4 < 16; j4 += 4) {
-                            if (j4 < kk) {
-                                const float4 v = __ldcg(reinterpret_cast<const float4 *>(zr + j4));
-                                acc[j4] += v.x;
-                                acc[j4 + 1] += j4 + 1 < kk ? v.y : 0.f;
-                                acc[j4 + 2] += j4 + 2 < kk ? v.z : 0.f;
-                                acc[j4 + 3] += j4 + 3 < kk ? v.w : 0.f;
-                            }
+                    for (int j4 = 0; j4 < 16; j4 += 4) {
+                        if (j4 < kk) {
+                            const float4 v = __ldcg(reinterpret_cast<const float4 *>(zr + j4));
+                            acc[j4] += v.x;
+                            acc[j4 + 1] += j4 + 1 < kk ? v.y : 0.f;
+                            acc[j4 + 2] += j4 + 2 < kk ? v.z : 0.f;
+                            acc[j4 + 3] += j4 + 3 < kk ? v.w : 0.f;
                         }
                     }
                 }
@@ -505,88 +676,143 @@ __global__ void __launch_bounds__(ME_THREADS, 2)
                 *reinterpret_cast<uint4 *>(zlo + o0) = make_uint4(l[0], l[1], l[2], l[3]);
                 *reinterpret_cast<uint4 *>(zlo + o1) = make_uint4(l[4], l[5], l[6], l[7]);
             }
-            fence_proxy_async_smem();
-            __syncthreads();
+        }
+    };
 
-            // ---- warp 0: per slot, wait for its B chunk, mask rank rows >= k, issue hi and lo MMAs
-            if (warp == 0) {
-                for (int jj = 0; jj < npass && ok; ++jj) {
-                    const int j = j0 + jj, gs = gs_base + j, st = gs % ME_STAGES;
-                    ok = mbar_wait_bounded(&full_b[st], (gs / ME_STAGES) & 1, status);
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                    if (!ok)
-                        break;
-                    const int u = me_slot_owner(sbase, nu, j);
-                    const int kr = lrank[u] - 16 * (j - sbase[u]);
-                    unsigned char *bs = sb + st * ME_B_BYTES;
-                    if (kr < 16) {
-                        const int nz = (16 - kr) * (BN / 64) * 8;  // 16-byte pieces of rows kr..15
-                        for (int e = lane; e < nz; e += 32) {
-                            const int piece = e & 7, rest = e >> 3;
-                            const int at = rest % (BN / 64), rr = kr + rest / (BN / 64);
-                            *reinterpret_cast<uint4 *>(bs + at * 2048 + (rr >> 3) * 1024 + (rr & 7) * 128 +
-                                                       piece * 16) = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        fence_proxy_async_smem();
-                    }
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc_fence_after();
-                        const uint64_t bd = umma_desc_sw128_mn(smem_u32(bs), 2048, 1024);
-                        const uint32_t zo = (uint32_t)((jj >> 2) * (MMA_TM * 128) + (jj & 3) * 32);
-                        umma_bf16(taddr, umma_desc_sw128(smem_u32(zhi) + zo), bd, idesc, !first_mma);
-                        umma_bf16(taddr, umma_desc_sw128(smem_u32(zlo) + zo), bd, idesc, true);
-                        first_mma = false;
-                        umma_commit(&empty_b[st]);
-                        while (ok && issued < ns && issued <= j + ME_STAGES - 1)
-                            ok = issue_b(issued++);
-                    }
-                    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    // epilogue of unit uu (running index gi): y + D, rounded once; warp w reads
+    // lanes 32 (w % 4).. of the accumulator, column half w / 4
+    auto epilogue = [&](int uu) {
+        constexpr int HALF = BN / 2, NV = HALF / 8;
+        const int b = gi & 1;
+        const int lq = warp & 3, hf = warp >> 2;
+        const int row = lq * 32 + lane;
+        const bool live = row < nrows;
+        __nv_bfloat16 *yr = a.y + (size_t)(t0 + (live ? row : 0)) * d_out + (uu % a.n_nt) * BN + hf * HALF;
+        uint4 yv[NV];
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+            yv[v] = live ? *reinterpret_cast<const uint4 *>(yr + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+        const bool ok = mbar_wait_bounded(&acc_full[b], (gi >> 1) & 1, status);
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < HALF; c += 16) {
+            float v[16];
+            tmem_ld16(taddr + ((uint32_t)(lq * 32) << 16) + (uint32_t)(b * BN + hf * HALF + c), v);
+            if (live && ok) {
+                uint4 o[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint4 w = yv[c / 8 + hh];
+                    const float *d = v + 8 * hh;
+                    o[hh] = make_uint4(pack_bf16x2(bf16lo(w.x) + d[0], bf16hi(w.x) + d[1]),
+                                       pack_bf16x2(bf16lo(w.y) + d[2], bf16hi(w.y) + d[3]),
+                                       pack_bf16x2(bf16lo(w.z) + d[4], bf16hi(w.z) + d[5]),
+                                       pack_bf16x2(bf16lo(w.w) + d[6], bf16hi(w.w) + d[7]));
                 }
-                if (lane == 0)
-                    umma_commit(&pass_done);
-                __syncwarp();
+                *reinterpret_cast<uint4 *>(yr + c) = o[0];
+                *reinterpret_cast<uint4 *>(yr + c + 8) = o[1];
             }
         }
-        gs_base += ns;
-    }
+        tc_fence_before();
+        mbar_arrive(&acc_empty[b]);
+        ++gi;
+    };
 
-    // ---- epilogue: y (prefetched) + D, rounded once; warp w: lanes 32 (w % 4).., column half w / 4
-    constexpr int HALF = BN / 2, NV = HALF / 8;
-    const int lq = warp & 3, hf = warp >> 2;
-    const int row = lq * 32 + lane;
-    const bool live = row < nrows;
-    __nv_bfloat16 *yr = a.y + (size_t)(t0 + (live ? row : 0)) * d_out + n0 + hf * HALF;
-    uint4 yv[NV];
-#pragma unroll
-    for (int v = 0; v < NV; ++v)
-        yv[v] = live ? *reinterpret_cast<const uint4 *>(yr + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
-    ok = mbar_wait_bounded(&pass_done, (gp - 1) & 1, status) && ok;
-    tc_fence_after();
-#pragma unroll
-    for (int c = 0; c < HALF; c += 16) {
-        float v[16];
-        tmem_ld16(taddr + ((uint32_t)(lq * 32) << 16) + hf * HALF + c, v);
-        if (live && ok) {
-            uint4 o[2];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const uint4 w = yv[c / 8 + hh];
-                const float *d = v + 8 * hh;
-                o[hh] = make_uint4(pack_bf16x2(bf16lo(w.x) + d[0], bf16hi(w.x) + d[1]),
-                                   pack_bf16x2(bf16lo(w.y) + d[2], bf16hi(w.y) + d[3]),
-                                   pack_bf16x2(bf16lo(w.z) + d[4], bf16hi(w.z) + d[5]),
-                                   pack_bf16x2(bf16lo(w.w) + d[6], bf16hi(w.w) + d[7]));
-            }
-            *reinterpret_cast<uint4 *>(yr + c) = o[0];
-            *reinterpret_cast<uint4 *>(yr + c + 8) = o[1];
+    for (int u = u_begin; u < u_end;) {
+        const int tile = u / a.n_nt;
+        const int ut_end = min(u_end, (tile + 1) * a.n_nt);
+        t0 = tile * MMA_TM;
+        nrows = min(MMA_TM, a.T - t0);
+        wait_free();  // the lists and the operand are rewritten below
+        // ---- the tile's pairs (mapping data: complete before the shrink started)
+        for (int i = tid; i <= nrows; i += ME_WORKERS)
+            toff[i] = a.m.toff[t0 + i];
+        for (int i = tid; i < nwords; i += ME_WORKERS)
+            bitmap[i] = 0u;
+        me_bar();
+        p0 = toff[0];
+        np = toff[nrows] - p0;
+        for (int i = tid; i < np; i += ME_WORKERS) {
+            const int q = a.m.pos[p0 + i];
+            int ad = q >= 0 ? a.m.adapter[q] : -1;
+            if (ad >= 0 && effective_rank(a.pool, a.ranks, ad) <= 0)
+                ad = -1;  // contributes nothing
+            if (ad >= 0)
+                atomicOr(&bitmap[ad >> 5], 1u << (ad & 31));
+            if (i < ME_PT_MAX)
+                cache[i] = make_int2(q, ad);
         }
+        me_bar();
+        nu_total = 0;
+        for (int base = 0; base < nwords; base += ME_WORKERS) {
+            const int wi = base + tid;
+            const int c = wi < nwords ? __popc(bitmap[wi]) : 0;
+            int tot;
+            const int ex = me_scan(c, tot, s_scan);
+            if (wi < nwords)
+                wpre[wi] = nu_total + ex;
+            nu_total += tot;
+        }
+        me_bar();
+        if (!synced) {
+            pdl_wait();  // z of the shrink is complete from here on
+            __syncthreads();  // (A)
+            tc_fence_after();
+            taddr = s_taddr;
+            synced = true;
+        }
+        if (nu_total > 0) {
+            const int nwin = (nu_total + ME_NU_MAX - 1) / ME_NU_MAX;
+            if (nwin == 1) {
+                const int ns = build_lists(0);
+                const int nu = nu_total;
+                const int npass = (ns + ME_SMAX - 1) / ME_SMAX;
+                if (npass == 1) {
+                    build_zsel(0, nu, 0, ns);  // one operand for every column tile of the token tile
+                    publish(u, ut_end, 0, ns, nu, 1, 1, 0);
+                    for (int uu = u; uu < ut_end; ++uu)
+                        epilogue(uu);
+                } else {
+                    for (int uu = u; uu < ut_end; ++uu) {
+                        for (int p = 0; p < npass; ++p) {
+                            const int s0 = p * ME_SMAX, s1 = min(ns, s0 + ME_SMAX);
+                            wait_free();
+                            build_zsel(0, nu, s0, s1);
+                            publish(uu, uu + 1, s0, s1, nu, p == 0, p == npass - 1, 0);
+                        }
+                        epilogue(uu);
+                    }
+                }
+            } else {
+                for (int uu = u; uu < ut_end; ++uu) {
+                    for (int w = 0; w < nwin; ++w) {
+                        const int w0 = w * ME_NU_MAX;
+                        wait_free();
+                        const int ns = build_lists(w0);
+                        const int nu = min(ME_NU_MAX, nu_total - w0);
+                        const int npass = (ns + ME_SMAX - 1) / ME_SMAX;
+                        for (int p = 0; p < npass; ++p) {
+                            const int s0 = p * ME_SMAX, s1 = min(ns, s0 + ME_SMAX);
+                            wait_free();
+                            build_zsel(w0, nu, s0, s1);
+                            publish(uu, uu + 1, s0, s1, nu, w == 0 && p == 0, w == nwin - 1 && p == npass - 1, 0);
+                        }
+                    }
+                    epilogue(uu);
+                }
+            }
+        }
+        u = ut_end;
     }
+    if (!synced) {
+        pdl_wait();
+        __syncthreads();  // (A)
+        synced = true;
+    }
+    wait_free();
+    publish(0, 0, 0, 0, 0, 0, 0, 1);
     tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 0)
-        tmem_dealloc(taddr, BN);
+    __syncthreads();  // (B)
 }
 
 }  // namespace
@@ -630,6 +856,28 @@ cudaError_t encode_rows(unsigned char *out, const void *base, int cols, long lon
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// B as a 3-D tensor {64 columns, rows, d_out / 64 column blocks} (strides: the
+// row pitch, then 128 bytes), boxes {64, 16, bn / 64}: one box is a 16-row
+// chunk of bn columns, landing column block after column block (2 KB each).
+cudaError_t encode_b_blocks(unsigned char *out, const void *base, int d_out, long long rows, int bn)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(d_out / 64)};
+    const cuuint64_t strides[2] = {(cuuint64_t)d_out * 2, 128};
+    const cuuint32_t box[3] = {64, 16, (cuuint32_t)(bn / 64)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = fn(reinterpret_cast<CUtensorMap *>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                          const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Output columns per expand unit.
+int expand_bn(int d_out) { return d_out % 256 == 0 ? 256 : (d_out % 128 == 0 ? 128 : 64); }
+
 // Cluster size of the shrink: the K blocks of d_in split over ck CTAs.
 int shrink_cluster(int d_in)
 {
@@ -655,9 +903,12 @@ cudaError_t launch_expand_bn(__nv_bfloat16 *y, const PoolDev &pool, const CUtens
             return e;
         attr_dev = dev;
     }
-    MmaExpandArgs a{y, pool, ranks, m, T, z_stride(pool.r_max)};
+    const int n_nt = pool.d_out / BN;
+    const int units = n_nt * ((T + MMA_TM - 1) / MMA_TM);
+    MmaExpandArgs a{y, pool, ranks, m, T, z_stride(pool.r_max), n_nt, units};
+    const int grid = units < sm_count() ? units : sm_count();  // persistent: one CTA per SM
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pool.d_out / BN, (T + MMA_TM - 1) / MMA_TM, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(ME_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L.total;
     cfg.stream = st;
@@ -682,7 +933,7 @@ cudaError_t mma_encode_maps(const PoolDev &pool, MmaMaps &maps)
     const long long rows = (long long)pool.capacity * pool.r_max;
     cudaError_t e = encode_rows(maps.At, pool.At, pool.d_in, rows);
     if (e == cudaSuccess)
-        e = encode_rows(maps.B, pool.B, pool.d_out, rows);
+        e = encode_b_blocks(maps.B, pool.B, pool.d_out, rows, expand_bn(pool.d_out));
     maps.ready = e == cudaSuccess;
     return e;
 }
@@ -730,11 +981,14 @@ cudaError_t launch_mma(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &
     // 2. token-tile expand, PDL-chained to the shrink
     if (T <= 0)
         return cudaSuccess;
-    if (pool.d_out % 256 == 0)
+    switch (expand_bn(pool.d_out)) {
+    case 256:
         return launch_expand_bn<256>(y, pool, map_b, ranks, m, T, st);
-    if (pool.d_out % 128 == 0)
+    case 128:
         return launch_expand_bn<128>(y, pool, map_b, ranks, m, T, st);
-    return launch_expand_bn<64>(y, pool, map_b, ranks, m, T, st);
+    default:
+        return launch_expand_bn<64>(y, pool, map_b, ranks, m, T, st);
+    }
 }
 
 }  // namespace tcl
