@@ -327,10 +327,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--max-replicas", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="auto", choices=["auto", "split", "fused", "mma"],
+    ap.add_argument("--path", default="auto", choices=["auto", "split", "fused", "mma", "decode"],
                     help="force an execution path (default: the library's dispatch table)")
     args = ap.parse_args()
-    args.path_id = {"auto": 0, "split": 1, "fused": 2, "mma": 3}[args.path]
+    args.path_id = {"auto": 0, "split": 1, "fused": 2, "mma": 3, "decode": 4}[args.path]
     args.warmup = max(3, args.warmup)
     rank, world, dist = dist_setup(args.gpus)
 

@@ -120,7 +120,7 @@ void free_mapping(lora_mapping *m)
 {
     MapDev &d = m->dev;
     void *ptrs[] = {d.tok,  d.adapter, d.src, d.pos,     d.alpha, d.seg_adapter, d.seg_start,
-                    d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.z,
+                    d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.pq, d.z,
                     d.partial, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
@@ -130,13 +130,14 @@ void free_mapping(lora_mapping *m)
 
 // Dispatch table (LoRAForge page, "Approach" (5): native path or a special
 // kernel, fixed by phase, rank and shape).
-// Long batches (prefill) go to the tensor cores: a 128-token tile then
-// touches few adapters and a segment holds many tokens.
+// Short batches (decode) take the per-pair decode kernels; long batches
+// (prefill) go to the tensor cores, where a 128-token tile touches few
+// adapters and a segment holds many tokens.
 int choose_path(int T, int P, int r_max, int d_in, int d_out)
 {
     (void)P;
-    if (fused_supported(T, d_out))
-        return LORA_PATH_FUSED;  // decode: one launch
+    if (T <= DECODE_MAX_TOKENS && decode_supported(d_in, d_out))
+        return LORA_PATH_DECODE;
     if (T >= MMA_MIN_TOKENS && mma_supported(d_in, d_out, r_max))
         return LORA_PATH_MMA;
     return LORA_PATH_SPLIT;
@@ -200,6 +201,16 @@ lora_status run_mma(const void *x, void *y, const lora_pool *pool, const int32_t
         return LORA_ERR_NOT_SUPPORTED;
     const cudaError_t e = launch_mma(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
                                      pool_dev(pool), pool->maps, ranks, m->dev, m->T, m->P, st);
+    if (e == cudaErrorNotSupported)
+        return LORA_ERR_NOT_SUPPORTED;
+    return from_cuda(e);
+}
+
+lora_status run_decode(const void *x, void *y, const lora_pool *pool, const int32_t *ranks,
+                       const lora_mapping *m, cudaStream_t st)
+{
+    const cudaError_t e = launch_decode(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
+                                        pool_dev(pool), ranks, m->dev, m->T, m->P, st);
     if (e == cudaErrorNotSupported)
         return LORA_ERR_NOT_SUPPORTED;
     return from_cuda(e);
@@ -366,6 +377,7 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.hdr, (size_t)HDR_WORDS);
     if (e == cudaSuccess) e = dalloc(&d.mtile, (size_t)mma_tile_bound(max_pairs, capacity));
     if (e == cudaSuccess) e = dalloc(&d.toff, (size_t)max_tokens + 1);
+    if (e == cudaSuccess) e = dalloc(&d.pq, P);
     if (e == cudaSuccess) e = dalloc(&d.z, P * LORA_MAX_RANK);
     d.partial_ctas = sm_count();
     if (e == cudaSuccess) e = dalloc(&d.partial, (size_t)d.partial_ctas * EXP_TILE_ELEMS);
@@ -418,6 +430,8 @@ lora_status lora_delta_apply_path(const void *x_dev, void *y_dev, const lora_poo
         return run_fused(x_dev, y_dev, pool, ranks_dev, m, st);
     case LORA_PATH_MMA:
         return run_mma(x_dev, y_dev, pool, ranks_dev, m, st);
+    case LORA_PATH_DECODE:
+        return run_decode(x_dev, y_dev, pool, ranks_dev, m, st);
     default:
         return LORA_ERR_NOT_SUPPORTED;
     }
@@ -553,7 +567,7 @@ namespace {
 __device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
 
 struct NoallocLayout {
-    size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, z;
+    size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, pq, z;
     size_t total;
 };
 
@@ -582,6 +596,7 @@ NoallocLayout noalloc_layout(int T, int P, int capacity, int r_max)
     L.hdr = take(4 * (size_t)HDR_WORDS);
     L.mtile = take(16 * mtiles);
     L.toff = take(4 * ((size_t)T + 1));
+    L.pq = take(8 * p);
     L.z = take(4 * p * (size_t)z_stride(r_max));
     L.total = off;
     return L;
@@ -639,6 +654,7 @@ extern "C" lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, 
     d.hdr = reinterpret_cast<int32_t *>(base + L.hdr);
     d.mtile = reinterpret_cast<int4 *>(base + L.mtile);
     d.toff = reinterpret_cast<int32_t *>(base + L.toff);
+    d.pq = reinterpret_cast<int2 *>(base + L.pq);
     d.z = reinterpret_cast<float *>(base + L.z);
     d.partial = nullptr;  // used by the fused kernel only
     d.partial_ctas = 0;

@@ -1,0 +1,293 @@
+// Decode path: short batches, where every pair has its own x row and the
+// adapters' factors are read once.  Two launches chained with programmatic
+// dependent launch, every global access a 16-byte coalesced vector:
+//
+// 1. Shrink (LoRAForge page, "Approach" (4): direct reduction for short
+//    decode batches; DyMerge-LoRA page, "Core idea": the weight alpha folded
+//    in).  A CTA owns one sorted pair q and 8 consecutive rank rows; its x row
+//    is staged once in shared memory and each warp streams one row of A_a
+//    (stored transposed, contiguous along d_in) against it, reducing with
+//    warp shuffles:  z[q][j] = alpha_q * sum_d x[tok_q][d] * A_a[d][j].
+//
+// 2. Expand (RowExpand, LoRAForge page, "Approach" (4)): a warp owns one
+//    token and 256 output columns (8 per lane).  Before waiting for the
+//    shrink it reads the token's pair list and issues the loads of y and of
+//    the first B rows (they do not depend on z; rows are fetched before the
+//    rank is known and used only below it); then it adds
+//    sum_pairs sum_j z[q][j] * B_a[j][cols] in fp32, 8 rows in flight at a
+//    time, and rounds once to bf16.
+//
+// Both kernels order their loads so that each waits on as few dependent
+// round trips to memory as possible: a decode batch moves little data, and
+// its time is the chain of latencies.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace tcl {
+
+namespace {
+
+constexpr int DS_THREADS = 256;  // 8 warps: one rank row each
+
+struct DecShrinkArgs {
+    const __nv_bfloat16 *x;
+    PoolDev pool;
+    const int32_t *ranks;
+    MapDev m;
+    int zs;
+};
+
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
+{
+    acc = fmaf(bf16lo(a.x), bf16lo(b.x), acc);
+    acc = fmaf(bf16hi(a.x), bf16hi(b.x), acc);
+    acc = fmaf(bf16lo(a.y), bf16lo(b.y), acc);
+    acc = fmaf(bf16hi(a.y), bf16hi(b.y), acc);
+    acc = fmaf(bf16lo(a.z), bf16lo(b.z), acc);
+    acc = fmaf(bf16hi(a.z), bf16hi(b.z), acc);
+    acc = fmaf(bf16lo(a.w), bf16lo(b.w), acc);
+    acc = fmaf(bf16hi(a.w), bf16hi(b.w), acc);
+    return acc;
+}
+
+__global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a)
+{
+    extern __shared__ __align__(16) uint4 xs[];  // the pair's x row
+    pdl_launch_dependents();
+    const int q = blockIdx.x;
+    // one round trip: the pair (its adapter is used only once q is known valid)
+    const int pvalid = a.m.hdr[HDR_PVALID];
+    const int ad = a.m.adapter[q], tk = a.m.tok[q];
+    const float al = a.m.alpha[q];
+    if (q >= pvalid)
+        return;  // pairs left out of the mapping (and every pair when its offsets were malformed)
+    const int r_max = a.pool.r_max;
+    const int j0 = blockIdx.y * (DS_THREADS / 32);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = j0 + warp;
+    const bool row = j < r_max;  // rows are fetched before the rank is known
+    const int d_in = a.pool.d_in, nv = d_in / 8;  // 16-byte vectors per row
+    // second round trip: x row (to shared memory), the A row, the rank
+    const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)tk * d_in);
+    for (int i = threadIdx.x; i < nv; i += DS_THREADS)
+        cp_async16(&xs[i], &xr[i]);
+    cp_async_commit();
+    const uint4 *ar = reinterpret_cast<const uint4 *>(a.pool.At + ((size_t)ad * r_max + (row ? j : 0)) * d_in);
+    uint4 av[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int i = u * 32 + lane;
+        av[u] = row && i < nv ? __ldcs(&ar[i]) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    const int k = effective_rank(a.pool, a.ranks, ad);
+    if (k <= 0) {
+        if (k < 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            atomicOr(a.m.hdr + HDR_STATUS, k == -1 ? LORA_DEV_UNREGISTERED : LORA_DEV_BAD_RANK);
+        cp_async_wait_all();
+        return;
+    }
+    if (j0 >= k) {
+        cp_async_wait_all();
+        return;
+    }
+    const bool live = j < k;
+    cp_async_wait_all();
+    __syncthreads();
+    float acc = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+        const int i = u * 32 + lane;
+        if (i < nv)
+            acc = dot8(av[u], xs[i], acc);
+    }
+    // longer rows: further batches of 16 vectors per lane
+    for (int base = 32 * 16; base < nv; base += 32 * 16) {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int i = base + u * 32 + lane;
+            av[u] = live && i < nv ? __ldcs(&ar[i]) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int i = base + u * 32 + lane;
+            if (i < nv)
+                acc = dot8(av[u], xs[i], acc);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && lane == 0)
+        a.m.z[(size_t)q * a.zs + j] = al * acc;
+}
+
+struct DecExpandArgs {
+    __nv_bfloat16 *y;
+    PoolDev pool;
+    const int32_t *ranks;
+    MapDev m;
+    int T, zs, nc;  // nc: 256-column chunks per row (the last may be partial)
+};
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float z, uint4 b)
+{
+    acc[0] = fmaf(z, bf16lo(b.x), acc[0]);
+    acc[1] = fmaf(z, bf16hi(b.x), acc[1]);
+    acc[2] = fmaf(z, bf16lo(b.y), acc[2]);
+    acc[3] = fmaf(z, bf16hi(b.y), acc[3]);
+    acc[4] = fmaf(z, bf16lo(b.z), acc[4]);
+    acc[5] = fmaf(z, bf16hi(b.z), acc[5]);
+    acc[6] = fmaf(z, bf16lo(b.w), acc[6]);
+    acc[7] = fmaf(z, bf16hi(b.w), acc[7]);
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+constexpr int DE_PP = 2;  // pairs of a token whose B rows are fetched before the dependency wait
+constexpr int DE_PR = 8;  // rows fetched per such pair
+
+// Retained rank of adapter ad for this call, 0 when it contributes nothing.
+__device__ __forceinline__ int dec_rank(const PoolDev &pool, const int32_t *ranks, int ad)
+{
+    const int k = effective_rank(pool, ranks, ad);
+    return k > 0 ? k : 0;
+}
+
+// acc += sum_{j in [jb, k)} z[j] * B row j, 8 rows in flight at a time.
+__device__ __forceinline__ void dec_rows(float (&acc)[8], const __nv_bfloat16 *br, const float *zr, int jb, int k,
+                                         int d_out, bool on)
+{
+    for (int j = jb; j < k; j += 8) {
+        uint4 bb[8];
+        float zz[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool v = j + u < k;
+            bb[u] = v && on ? __ldcs(reinterpret_cast<const uint4 *>(br + (size_t)(j + u) * d_out))
+                            : make_uint4(0u, 0u, 0u, 0u);
+            zz[u] = v ? __ldcg(zr + j + u) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            fma8(acc, zz[u], bb[u]);
+    }
+}
+
+__global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (g >= a.T * a.nc)
+        return;
+    const int t = g / a.nc, c = g % a.nc;
+    const int d_out = a.pool.d_out, r_max = a.pool.r_max;
+    const int col = c * 256 + lane * 8;
+    const bool on = col < d_out;  // the last chunk of a row may be partial
+    // round trip 1: y, the token's pair range, the batch's validity
+    __nv_bfloat16 *yp = a.y + (size_t)t * d_out + (on ? col : 0);
+    const uint4 yv = on ? *reinterpret_cast<const uint4 *>(yp) : make_uint4(0u, 0u, 0u, 0u);
+    const int pvalid = a.m.hdr[HDR_PVALID];
+    const int p0 = a.m.toff[t], p1 = a.m.toff[t + 1];
+    if (pvalid == 0)
+        return;  // nothing valid (also: offsets malformed, the pair range is not defined)
+    // round trip 2: {sorted position, adapter} of the first pairs
+    int2 pq[DE_PP];
+#pragma unroll
+    for (int i = 0; i < DE_PP; ++i)
+        pq[i] = p0 + i < p1 ? a.m.pq[p0 + i] : make_int2(-1, -1);
+    // round trip 3: their first B rows (whatever the rank turns out to be) and ranks
+    uint4 bpre[DE_PP][DE_PR];
+    int kk[DE_PP];
+#pragma unroll
+    for (int i = 0; i < DE_PP; ++i) {
+        const int ad = pq[i].y;
+        const __nv_bfloat16 *br = a.pool.B + (size_t)(ad < 0 ? 0 : ad) * r_max * d_out + col;
+#pragma unroll
+        for (int j = 0; j < DE_PR; ++j)
+            bpre[i][j] = ad >= 0 && on && j < r_max ? __ldcs(reinterpret_cast<const uint4 *>(br + (size_t)j * d_out))
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+        kk[i] = ad >= 0 ? dec_rank(a.pool, a.ranks, ad) : 0;
+    }
+    pdl_wait();  // z of the shrink
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < DE_PP; ++i) {
+        const int k = kk[i];
+        if (k > 0) {
+            const float *zr = a.m.z + (size_t)pq[i].x * a.zs;
+            float zz[DE_PR];
+#pragma unroll
+            for (int j = 0; j < DE_PR; ++j)
+                zz[j] = j < k ? __ldcg(zr + j) : 0.f;
+#pragma unroll
+            for (int j = 0; j < DE_PR; ++j)
+                fma8(acc, zz[j], bpre[i][j]);
+            if (k > DE_PR)
+                dec_rows(acc, a.pool.B + (size_t)pq[i].y * r_max * d_out + col, zr, DE_PR, k, d_out, on);
+        }
+    }
+    for (int p = p0 + DE_PP; p < p1; ++p) {
+        const int2 v = a.m.pq[p];
+        if (v.y < 0)
+            continue;
+        const int k = dec_rank(a.pool, a.ranks, v.y);
+        if (k > 0)
+            dec_rows(acc, a.pool.B + (size_t)v.y * r_max * d_out + col, a.m.z + (size_t)v.x * a.zs, 0, k, d_out, on);
+    }
+    uint4 o;
+    o.x = pack2(bf16lo(yv.x) + acc[0], bf16hi(yv.x) + acc[1]);
+    o.y = pack2(bf16lo(yv.y) + acc[2], bf16hi(yv.y) + acc[3]);
+    o.z = pack2(bf16lo(yv.z) + acc[4], bf16hi(yv.z) + acc[5]);
+    o.w = pack2(bf16lo(yv.w) + acc[6], bf16hi(yv.w) + acc[7]);
+    if (on)
+        *reinterpret_cast<uint4 *>(yp) = o;
+}
+
+}  // namespace
+
+// The x row is staged in shared memory: d_in * 2 bytes of at most 200 KB.
+bool decode_supported(int d_in, int d_out) { return d_in % 8 == 0 && d_out % 8 == 0 && d_in <= 100 * 1024; }
+
+cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
+                          const MapDev &m, int T, int P, cudaStream_t st)
+{
+    if (!decode_supported(pool.d_in, pool.d_out))
+        return cudaErrorNotSupported;
+    static int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(k_dec_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess)
+            return e;
+        attr_dev = dev;
+    }
+    DecShrinkArgs sa{x, pool, ranks, m, z_stride(pool.r_max)};
+    const dim3 sgrid(P, (pool.r_max + 7) / 8, 1);
+    k_dec_shrink<<<sgrid, DS_THREADS, (size_t)pool.d_in * 2, st>>>(sa);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const int nc = (pool.d_out + 255) / 256;
+    const long long warps = (long long)T * nc;
+    int wpc = 8;  // warps per CTA: the most that still gives a CTA per SM
+    while (wpc > 1 && (warps + wpc - 1) / wpc < sm_count())
+        wpc >>= 1;
+    DecExpandArgs ea{y, pool, ranks, m, T, z_stride(pool.r_max), nc};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + wpc - 1) / wpc), 1, 1);
+    cfg.blockDim = dim3(32 * wpc, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_dec_expand, ea);
+}
+
+}  // namespace tcl

@@ -74,6 +74,7 @@ struct MapDev {
     int32_t *hdr;                        // [HDR_WORDS]
     int4 *mtile;                         // [mma_tile_bound] tensor-core shrink tiles {adapter, q0, n, segment}
     int32_t *toff;                       // [max_tokens+1] copy of the batch's CSR offsets
+    int2 *pq;                            // [max_pairs] per CSR pair: {sorted position, adapter}, -1s if left out
     float *z;                            // [max_pairs][LORA_MAX_RANK] shrink output
     float *partial;                      // [partial_ctas][EXP_TILE_ELEMS] fused-kernel tiles
     int partial_ctas;
@@ -106,6 +107,13 @@ int shrink_tile_bound(int P, int capacity);
 int mma_tile_bound(int P, int capacity);
 
 bool fused_supported(int T, int d_out);
+
+// Decode path: per-pair shrink, then a warp per (token, 256 columns) expand.
+bool decode_supported(int d_in, int d_out);
+cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
+                          const MapDev &m, int T, int P, cudaStream_t st);
+// Dispatch: batches of at most this many tokens take the decode path.
+constexpr int DECODE_MAX_TOKENS = 256;
 cudaError_t launch_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
                          const MapDev &m, int T, int P, const ExpandPlan &plan, int grid, cudaStream_t st);
 

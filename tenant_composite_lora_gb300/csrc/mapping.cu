@@ -254,8 +254,10 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
                 reinterpret_cast<int32_t *>(m.alpha)[dst] = alb[p];
                 m.src[dst] = p;
                 m.pos[p] = dst;
+                m.pq[p] = make_int2(dst, id);
             } else if (valid) {
                 m.pos[p] = -1;
+                m.pq[p] = make_int2(-1, -1);
             }
             __syncwarp();
             if (ok && lane == __ffs(peers) - 1)

@@ -32,6 +32,7 @@ LORA_PATH_AUTO = 0
 LORA_PATH_SPLIT = 1
 LORA_PATH_FUSED = 2
 LORA_PATH_MMA = 3
+LORA_PATH_DECODE = 4
 
 LORA_MAX_RANK = 64
 LORA_MAX_CAPACITY = 49152

@@ -45,8 +45,11 @@ def test_host_only_calls(lib):
     assert native.status_string(0) == "ok"
     assert "not supported" in native.status_string(5)
     assert "sm_103a" in native.lora_version()
-    p = native.lora_dispatch_choose(32, 96, 8, 4096, 4096)
-    assert p in (native.LORA_PATH_SPLIT, native.LORA_PATH_FUSED, native.LORA_PATH_MMA)
+    # the dispatch table: decode batches, long prefill batches, the middle
+    assert native.lora_dispatch_choose(32, 96, 8, 4096, 4096) == native.LORA_PATH_DECODE
+    assert native.lora_dispatch_choose(256, 512, 64, 4096, 1024) == native.LORA_PATH_DECODE
+    assert native.lora_dispatch_choose(3250, 6500, 16, 4096, 4096) == native.LORA_PATH_MMA
+    assert native.lora_dispatch_choose(300, 900, 16, 4096, 4096) == native.LORA_PATH_SPLIT
 
 
 def test_bad_arguments_rejected_before_device(lib):

@@ -125,9 +125,9 @@ def test_mapping_bad_offsets_and_degenerate():
 
 # ---------------------------------------------------------------- delta, element-wise
 APPLY_CASES = ["tiny", "distinct", "zipf", "sweep1", "sweep8", "sweep64", "sweep256"]
-PATH_AUTO, PATH_SPLIT, PATH_FUSED, PATH_MMA = 0, 1, 2, 3
-DECODE_PATHS = [PATH_AUTO, PATH_SPLIT, PATH_FUSED]
-ALL_PATHS = [PATH_AUTO, PATH_SPLIT, PATH_FUSED, PATH_MMA]
+PATH_AUTO, PATH_SPLIT, PATH_FUSED, PATH_MMA, PATH_DECODE = 0, 1, 2, 3, 4
+DECODE_PATHS = [PATH_AUTO, PATH_SPLIT, PATH_FUSED, PATH_DECODE]
+ALL_PATHS = [PATH_AUTO, PATH_SPLIT, PATH_FUSED, PATH_MMA, PATH_DECODE]
 
 
 @pytest.mark.parametrize("name", APPLY_CASES)
@@ -197,7 +197,7 @@ def test_garbage_padding_is_inert(path):
     np.testing.assert_array_equal(y0, y1)
 
 
-@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA])
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA, PATH_SPLIT])
 def test_rank_override_and_bad_rank(path):
     wl = W.rank_sweep(64, y_zero=True)
     rng = np.random.default_rng(5)
@@ -217,7 +217,7 @@ def test_rank_override_and_bad_rank(path):
     delta_gate(y, acc)
 
 
-@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA])
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA, PATH_SPLIT])
 def test_unregistered_slot(path):
     wl = W.zipf_decode(y_zero=True)
     victim = int(wl.ids[1])
@@ -247,7 +247,7 @@ def test_deterministic(path):
     np.testing.assert_array_equal(a, b)
 
 
-@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA])
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA, PATH_SPLIT])
 def test_noops(path):
     wl = W.tiny()
     wl.alpha[:] = 0
@@ -300,7 +300,7 @@ def _custom(rng, d_in, d_out, r, cap, lists, ranks=None):
                          alpha_lists=alpha_lists, ranks=ranks, y_sigma=0.0)
 
 
-@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA])
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA, PATH_SPLIT])
 @pytest.mark.parametrize("ntok", [300, 200])
 def test_big_segments_and_many_pairs_per_token(ntok, path):
     """Segments far longer than a shrink tile or an expand job, one token with
