@@ -42,7 +42,14 @@ CONFIG_NAMES = {
     "sweep64": "rank sweep k_i~U{1..64}, k/v_proj 4096->1024, r_max=64, pool 1000, T=64",
     "sweep256": "rank sweep k_i~U{1..64}, k/v_proj 4096->1024, r_max=64, pool 1000, T=256",
 }
-KERNEL_SOURCES = ["shrink.cu", "expand.cu", "mapping.cu", "api.cu", "internal.h", "ptx.cuh"]
+PATH_NAMES = {0: "auto", 1: "split", 2: "fused", 3: "mma", 4: "decode"}
+# kernels of lora_delta_apply per path (the mapping kernel adds one launch per step)
+PATH_KERNELS = {
+    "split": (2, "k_shrink + k_expand (PDL)"),
+    "fused": (1, "k_fused (cooperative, one launch)"),
+    "mma": (2, "k_mma_shrink + k_mma_expand (tcgen05, PDL)"),
+    "decode": (2, "k_dec_shrink + k_dec_expand (PDL)"),
+}
 
 
 def peaks():
@@ -54,18 +61,23 @@ def peaks():
 
 
 def sources_digest() -> str:
+    """Digest of every kernel source and the ABI header: a traffic figure taken
+    with other sources no longer describes the kernels."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
-        fp = os.path.join(ROOT, "tenant_composite_lora_gb300", "csrc", f)
-        if os.path.exists(fp):
-            h.update(open(fp, "rb").read())
+    csrc = os.path.join(ROOT, "tenant_composite_lora_gb300", "csrc")
+    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
+    for f in files:
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "lora.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(config: str):
-    """dram bytes per lora_delta_apply from a committed ncu summary, valid
-    only while the kernel sources are unchanged."""
-    fp = os.path.join(ROOT, "profiles", f"traffic_{config}.txt")
+def ncu_traffic(config: str, path: str):
+    """dram bytes (read + write) per lora_delta_apply, summed over the apply's
+    kernels, from a committed ncu summary; valid only while the kernel sources
+    are unchanged."""
+    fp = os.path.join(ROOT, "profiles", f"traffic_{config}_{path}.txt")
     if not os.path.exists(fp):
         return None
     kv = {}
@@ -257,6 +269,9 @@ def bench_ours(args, rank, world, dist):
         d2h = wl.y.nbytes
 
     peak, peak_kind = peaks()
+    path_taken = args.path if args.path_id != 0 else PATH_NAMES[
+        native.lora_dispatch_choose(wl.T, wl.P, wl.r_max, wl.d_in, wl.d_out)]
+    n_apply_kernels, kernel_desc = PATH_KERNELS[path_taken]
     achieved = ab["total"] / (ms_apply * 1e-3) / 1e9
     value = world * wl.T / (ms_per_step * 1e-3)
     line = {
@@ -277,22 +292,22 @@ def bench_ours(args, rank, world, dist):
             "T": wl.T, "P": wl.P, "d_in": wl.d_in, "d_out": wl.d_out, "r_max": wl.r_max,
             "pool": wl.capacity, "distinct_adapters": ab["U"], "sum_k": ab["sum_k"],
             "step": "lora_build_mapping + lora_delta_apply",
-            "path": args.path,
+            "path": path_taken if args.path_id != 0 else f"auto -> {path_taken}",
             "l2_protocol": f"inputs larger than L2: {R} rotating replicas, {R * ab['total'] / 1e6:.0f} MB "
                            f"touched per pass vs {l2 / 1e6:.0f} MB L2",
             "parallelism": "replicas only" if world > 1 else "single GPU",
         },
         "roofline": {
-            "bound": "hbm", "kernel": "lora_delta_apply (shrink + expand, PDL-overlapped)",
+            "bound": "hbm", "kernel": f"lora_delta_apply = {kernel_desc}",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
             "algorithmic_bytes": ab["total"], "apply_us": round(ms_apply * 1e3, 3),
-            "traffic": ncu_traffic(args.config),
+            "traffic": ncu_traffic(args.config, path_taken),
         },
         "e2e": {"value": round(world * wl.T / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 6),
                 "api": "lora_delta_apply_host"},
-        "gpu_launches": 3 * steps_done,
+        "gpu_launches": (1 + n_apply_kernels) * steps_done,
         "clocks": clocks,
     }
     return line, wl
