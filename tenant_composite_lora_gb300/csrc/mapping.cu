@@ -315,6 +315,9 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
     if (attr_done != dev) {
         cudaError_t e =
             cudaFuncSetAttribute(k_build_mapping, cudaFuncAttributeMaxDynamicSharedMemorySize, MAP_SMEM_BYTES);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_build_mapping, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         attr_done = dev;

@@ -899,6 +899,9 @@ cudaError_t launch_expand_bn(__nv_bfloat16 *y, const PoolDev &pool, const CUtens
     if (attr_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(k_mma_expand<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              MeLayout(LORA_MAX_CAPACITY).total);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_mma_expand<BN>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess)
             return e;
         attr_dev = dev;
@@ -956,6 +959,9 @@ cudaError_t launch_mma(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &
         cudaGetDevice(&dev);
         if (attr_dev != dev) {
             cudaError_t e = cudaFuncSetAttribute(k_mma_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, MS_SMEM);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(k_mma_shrink, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         cudaSharedmemCarveoutMaxShared);
             if (e != cudaSuccess)
                 return e;
             attr_dev = dev;
