@@ -19,7 +19,9 @@
 //
 // Both kernels order their loads so that each waits on as few dependent
 // round trips to memory as possible: a decode batch moves little data, and
-// its time is the chain of latencies.
+// its time is the chain of latencies.  The shrink is itself a programmatic
+// dependent of the mapping kernel (its CTAs are resident when the mapping
+// ends), and the expand lets the next kernel in the stream start early.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -54,6 +56,7 @@ __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a
 {
     extern __shared__ __align__(16) uint4 xs[];  // the pair's x row
     pdl_launch_dependents();
+    pdl_wait();  // launched as a programmatic dependent of the mapping
     const int q = blockIdx.x;
     // one round trip: the pair (its adapter is used only once q is known valid)
     const int pvalid = a.m.hdr[HDR_PVALID];
@@ -179,6 +182,7 @@ __device__ __forceinline__ void dec_rows(float (&acc)[8], const __nv_bfloat16 *b
 
 __global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
 {
+    pdl_launch_dependents();  // the next kernel in the stream may start its prologue
     const int lane = threadIdx.x & 31;
     const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (g >= a.T * a.nc)
@@ -267,9 +271,17 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
         attr_dev = dev;
     }
     DecShrinkArgs sa{x, pool, ranks, m, z_stride(pool.r_max)};
-    const dim3 sgrid(P, (pool.r_max + 7) / 8, 1);
-    k_dec_shrink<<<sgrid, DS_THREADS, (size_t)pool.d_in * 2, st>>>(sa);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t scfg = {};
+    scfg.gridDim = dim3(P, (pool.r_max + 7) / 8, 1);
+    scfg.blockDim = dim3(DS_THREADS, 1, 1);
+    scfg.dynamicSmemBytes = (size_t)pool.d_in * 2;
+    scfg.stream = st;
+    scfg.attrs = attr;
+    scfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&scfg, k_dec_shrink, sa);
     if (e != cudaSuccess)
         return e;
     const int nc = (pool.d_out + 255) / 256;
@@ -282,9 +294,6 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     cfg.gridDim = dim3((unsigned)((warps + wpc - 1) / wpc), 1, 1);
     cfg.blockDim = dim3(32 * wpc, 1, 1);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_dec_expand, ea);

@@ -97,6 +97,11 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, P = a.P, cap = a.cap, nw = a.nw;
     MapDev &m = a.m;
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream: the CTA starts and stages the batch's inputs (which no kernel of
+    // the library writes) while that kernel finishes, and waits for it before
+    // writing anything.  Its own dependents may launch at once: they wait too.
+    pdl_launch_dependents();
 
     const int32_t *off, *ids, *alb;
     int32_t *tok, *hist;
@@ -125,6 +130,7 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
     int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
     for (int i = tid; i < nw * cap; i += MAP_THREADS)
         hist[i] = 0;
+    pdl_wait();  // the previous kernel (which may still read this mapping) is done
     if (tid == 0) {
         m.hdr[HDR_STATUS] = 0;
         m.hdr[HDR_BAR] = 0;  // fused-kernel barrier counters start over with every mapping
@@ -324,8 +330,17 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
     }
     MapArgs a{m, offsets, ids, alpha, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity),
               mma_tile_bound(P, capacity)};
-    k_build_mapping<<<1, MAP_THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(MAP_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_build_mapping, a);
 }
 
 }  // namespace tcl
