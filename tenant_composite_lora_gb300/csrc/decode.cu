@@ -4,13 +4,15 @@
 //
 // 1. Shrink (LoRAForge page, "Approach" (4): direct reduction for short
 //    decode batches; DyMerge-LoRA page, "Core idea": the weight alpha folded
-//    in).  A CTA owns one sorted pair q and 8 consecutive rank rows; its x row
+//    in).  A CTA owns one sorted pair q and 4 or 8 consecutive rank rows; its x row
 //    is staged once in shared memory and each warp streams one row of A_a
 //    (stored transposed, contiguous along d_in) against it, reducing with
 //    warp shuffles:  z[q][j] = alpha_q * sum_d x[tok_q][d] * A_a[d][j].
 //
 // 2. Expand (RowExpand, LoRAForge page, "Approach" (4)): a warp owns one
-//    token and 256 output columns (8 per lane).  Before waiting for the
+//    token and 256 output columns (8 per lane); a CTA's warps are
+//    consecutive tokens on one column chunk, sharing B rows through L1.
+//    Before waiting for the
 //    shrink it reads the token's pair list and issues the loads of y and of
 //    the first B rows (they do not depend on z; rows are fetched before the
 //    rank is known and used only below it); then it adds
@@ -29,7 +31,7 @@ namespace tcl {
 
 namespace {
 
-constexpr int DS_THREADS = 256;  // 8 warps: one rank row each
+constexpr int DS_THREADS = 256;  // at most 8 warps: one rank row each
 
 struct DecShrinkArgs {
     const __nv_bfloat16 *x;
@@ -65,14 +67,14 @@ __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a
     if (q >= pvalid)
         return;  // pairs left out of the mapping (and every pair when its offsets were malformed)
     const int r_max = a.pool.r_max;
-    const int j0 = blockIdx.y * (DS_THREADS / 32);
+    const int j0 = blockIdx.y * (blockDim.x >> 5);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = j0 + warp;
     const bool row = j < r_max;  // rows are fetched before the rank is known
     const int d_in = a.pool.d_in, nv = d_in / 8;  // 16-byte vectors per row
     // second round trip: x row (to shared memory), the A row, the rank
     const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)tk * d_in);
-    for (int i = threadIdx.x; i < nv; i += DS_THREADS)
+    for (int i = threadIdx.x; i < nv; i += blockDim.x)
         cp_async16(&xs[i], &xr[i]);
     cp_async_commit();
     const uint4 *ar = reinterpret_cast<const uint4 *>(a.pool.At + ((size_t)ad * r_max + (row ? j : 0)) * d_in);
@@ -150,7 +152,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi)
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-constexpr int DE_PP = 2;  // pairs of a token whose B rows are fetched before the dependency wait
+constexpr int DE_PP = 3;  // pairs of a token whose B rows are fetched before the dependency wait
 constexpr int DE_PR = 8;  // rows fetched per such pair
 
 // Retained rank of adapter ad for this call, 0 when it contributes nothing.
@@ -170,7 +172,7 @@ __device__ __forceinline__ void dec_rows(float (&acc)[8], const __nv_bfloat16 *b
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const bool v = j + u < k;
-            bb[u] = v && on ? __ldcs(reinterpret_cast<const uint4 *>(br + (size_t)(j + u) * d_out))
+            bb[u] = v && on ? __ldg(reinterpret_cast<const uint4 *>(br + (size_t)(j + u) * d_out))
                             : make_uint4(0u, 0u, 0u, 0u);
             zz[u] = v ? __ldcg(zr + j + u) : 0.f;
         }
@@ -187,7 +189,9 @@ __global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
     const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (g >= a.T * a.nc)
         return;
-    const int t = g / a.nc, c = g % a.nc;
+    // consecutive warps: consecutive tokens on one column chunk, so the B rows
+    // of an adapter several of them use come from L1 after the first
+    const int t = g % a.T, c = g / a.T;
     const int d_out = a.pool.d_out, r_max = a.pool.r_max;
     const int col = c * 256 + lane * 8;
     const bool on = col < d_out;  // the last chunk of a row may be partial
@@ -212,7 +216,7 @@ __global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
         const __nv_bfloat16 *br = a.pool.B + (size_t)(ad < 0 ? 0 : ad) * r_max * d_out + col;
 #pragma unroll
         for (int j = 0; j < DE_PR; ++j)
-            bpre[i][j] = ad >= 0 && on && j < r_max ? __ldcs(reinterpret_cast<const uint4 *>(br + (size_t)j * d_out))
+            bpre[i][j] = ad >= 0 && on && j < r_max ? __ldg(reinterpret_cast<const uint4 *>(br + (size_t)j * d_out))
                                                     : make_uint4(0u, 0u, 0u, 0u);
         kk[i] = ad >= 0 ? dec_rank(a.pool, a.ranks, ad) : 0;
     }
@@ -274,9 +278,12 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    // rows per CTA: 8, or 4 when r_max is small, so that a short batch's A
+    // rows spread over more SMs
+    const int rpc = pool.r_max <= 8 ? 4 : 8;
     cudaLaunchConfig_t scfg = {};
-    scfg.gridDim = dim3(P, (pool.r_max + 7) / 8, 1);
-    scfg.blockDim = dim3(DS_THREADS, 1, 1);
+    scfg.gridDim = dim3(P, (pool.r_max + rpc - 1) / rpc, 1);
+    scfg.blockDim = dim3(32 * rpc, 1, 1);
     scfg.dynamicSmemBytes = (size_t)pool.d_in * 2;
     scfg.stream = st;
     scfg.attrs = attr;
