@@ -6,7 +6,8 @@
 // processes the tokens of one adapter back to back and each adapter's A and
 // B are read once.
 //
-// One CTA of 1024 threads performs a stable counting sort on the adapter id
+// One CTA (1024 threads; 256 for short batches over small pools) performs a
+// stable counting sort on the adapter id
 // (the key range is the pool capacity):
 //   0. stage the offsets, ids and alpha bits in shared memory when they fit
 //      (one coalesced read; every later step works on shared memory);
@@ -35,7 +36,7 @@ struct Scan4 {
     int a, b, c, d;
 };
 
-// Block-wide exclusive scan of four ints (MAP_THREADS threads); returns the
+// Block-wide exclusive scan of four ints (blockDim.x threads, a multiple of 32); returns the
 // exclusive prefix and writes the block totals.
 __device__ Scan4 block_exclusive_scan4(Scan4 v, Scan4 &total, int *sh /* [4 * 32 + 4] */)
 {
@@ -59,7 +60,7 @@ __device__ Scan4 block_exclusive_scan4(Scan4 v, Scan4 &total, int *sh /* [4 * 32
     if (warp == 0) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int x = sh[32 * j + lane];
+            const int x = lane < (int)(blockDim.x >> 5) ? sh[32 * j + lane] : 0;
             int ix = x;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
     __shared__ int s_scan[4 * 32 + 4];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, P = a.P, cap = a.cap, nw = a.nw;
+    const int nthr = blockDim.x;  // 1024, or 256 for short batches
     MapDev &m = a.m;
     // Launched as a programmatic dependent of the previous kernel in the
     // stream: the CTA starts and stages the batch's inputs (which no kernel of
@@ -109,10 +111,10 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         int32_t *s_off = sh, *s_ids = sh + (T + 1), *s_al = s_ids + P;
         tok = s_al + P;
         hist = tok + P;
-        for (int i = tid; i <= T; i += MAP_THREADS)
+        for (int i = tid; i <= T; i += nthr)
             s_off[i] = a.off[i];
         const int32_t *alg = reinterpret_cast<const int32_t *>(a.alpha);
-        for (int p = tid; p < P; p += MAP_THREADS) {
+        for (int p = tid; p < P; p += nthr) {
             s_ids[p] = a.ids[p];
             s_al[p] = alg[p];
         }
@@ -128,7 +130,7 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
     }
     // per bin: first sorted position and first shrink tile of its segment
     int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
-    for (int i = tid; i < nw * cap; i += MAP_THREADS)
+    for (int i = tid; i < nw * cap; i += nthr)
         hist[i] = 0;
     pdl_wait();  // the previous kernel (which may still read this mapping) is done
     if (tid == 0) {
@@ -141,14 +143,14 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
 
     // 1. CSR check
     int bad = (tid == 0) && (off[0] != 0 || off[T] != P);
-    for (int t = tid; t < T; t += MAP_THREADS)
+    for (int t = tid; t < T; t += nthr)
         bad |= off[t + 1] < off[t];
     if (__syncthreads_or(bad)) {
-        for (int p = tid; p < P; p += MAP_THREADS)
+        for (int p = tid; p < P; p += nthr)
             m.pos[p] = -1;
-        for (int i = tid; i < a.tile_bound; i += MAP_THREADS)
+        for (int i = tid; i < a.tile_bound; i += nthr)
             m.tile[i] = make_int4(0, 0, 0, -1);
-        for (int i = tid; i < a.mtile_bound; i += MAP_THREADS)
+        for (int i = tid; i < a.mtile_bound; i += nthr)
             m.mtile[i] = make_int4(0, 0, 0, -1);
         if (tid == 0) {
             m.hdr[HDR_U] = 0;
@@ -164,9 +166,9 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
 
     // 2. token of each pair (and a copy of the offsets for the token-tile
     // expand); per-warp histograms
-    for (int t = tid; t <= T; t += MAP_THREADS)
+    for (int t = tid; t <= T; t += nthr)
         m.toff[t] = off[t];
-    for (int t = tid; t < T; t += MAP_THREADS) {
+    for (int t = tid; t < T; t += nthr) {
         const int p0 = off[t], p1 = off[t + 1];
         for (int p = p0; p < p1; ++p)
             tok[p] = t;
@@ -191,9 +193,9 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_ID);
     __syncthreads();
 
-    // 3. scan over bins, 1024 bins per round, bin-ascending
+    // 3. scan over bins, a CTA's worth of bins per round, bin-ascending
     Scan4 carry = {0, 0, 0, 0};
-    for (int base = 0; base < cap; base += MAP_THREADS) {
+    for (int base = 0; base < cap; base += nthr) {
         const int b = base + tid;
         int c = 0;
         if (b < cap)
@@ -224,9 +226,9 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         carry.c += tot.c;
         carry.d += tot.d;
     }
-    for (int i = carry.c + tid; i < a.tile_bound; i += MAP_THREADS)
+    for (int i = carry.c + tid; i < a.tile_bound; i += nthr)
         m.tile[i] = make_int4(0, 0, 0, -1);  // empty slots up to the host-known bound
-    for (int i = carry.d + tid; i < a.mtile_bound; i += MAP_THREADS)
+    for (int i = carry.d + tid; i < a.mtile_bound; i += nthr)
         m.mtile[i] = make_int4(0, 0, 0, -1);
     if (tid == 0) {
         m.hdr[HDR_U] = carry.b;
@@ -298,8 +300,11 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
     (void)max_pairs;
     const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
     const long long staged_words = (long long)(T + 1) + 3LL * P;
+    // short batches over small pools: one CTA of 256 threads (cheaper
+    // block-wide phases, the bins still one scan round); otherwise 1024
+    const int threads = (P <= 512 && capacity <= 256) ? 256 : MAP_THREADS;
     int nw = (P + 63) / 64;
-    nw = nw < 1 ? 1 : (nw > 32 ? 32 : nw);
+    nw = nw < 1 ? 1 : (nw > threads / 32 ? threads / 32 : nw);
     int staged = 0;
     // words: [staged arrays] + nw histograms + two per-bin arrays
     if (staged_words + 3LL * capacity <= budget) {
@@ -332,7 +337,7 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
               mma_tile_bound(P, capacity)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
-    cfg.blockDim = dim3(MAP_THREADS, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
