@@ -241,7 +241,7 @@ const char *lora_version(void);
  *   offsets_dev, ids_dev, alpha_dev, T, P : as for lora_build_mapping
  *   status_dev : NULL, or a device int32 that receives this call's
  *                LORA_DEV_* bits (stream-ordered)
- * Scratch for a batch: about P * (38 + 4 * round4(r_max)) + 64 * min(P,
+ * Scratch for a batch: about P * (42 + 4 * round4(r_max)) + 64 * min(P,
  * capacity) + 8 * capacity + 4 * T bytes, in 256-byte aligned pieces.  A batch whose layout
  * exceeds LORA_NOALLOC_SCRATCH_BYTES returns LORA_ERR_NOT_SUPPORTED before
  * launching anything.  The scratch header (status word and counters) is

@@ -120,7 +120,7 @@ void free_mapping(lora_mapping *m)
 {
     MapDev &d = m->dev;
     void *ptrs[] = {d.tok,  d.adapter, d.src, d.pos,     d.alpha, d.seg_adapter, d.seg_start,
-                    d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.pq, d.z,
+                    d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.pq, d.zcnt, d.z,
                     d.partial, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
@@ -184,6 +184,13 @@ ExpandPlan choose_expand_plan(int T, int d_out)
 lora_status run_fused(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
                       cudaStream_t st)
 {
+    if (decode_supported(pool->d_in, pool->d_out)) {
+        const cudaError_t e = launch_decode_fused(static_cast<const __nv_bfloat16 *>(x),
+                                                  static_cast<__nv_bfloat16 *>(y), pool_dev(pool), ranks, m->dev,
+                                                  m->T, m->P, st);
+        if (e != cudaErrorNotSupported)
+            return from_cuda(e);
+    }
     if (!fused_supported(m->T, pool->d_out))
         return LORA_ERR_NOT_SUPPORTED;
     const ExpandPlan plan = choose_expand_plan(m->T, pool->d_out);
@@ -378,6 +385,7 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.mtile, (size_t)mma_tile_bound(max_pairs, capacity));
     if (e == cudaSuccess) e = dalloc(&d.toff, (size_t)max_tokens + 1);
     if (e == cudaSuccess) e = dalloc(&d.pq, P);
+    if (e == cudaSuccess) e = dalloc(&d.zcnt, P);
     if (e == cudaSuccess) e = dalloc(&d.z, P * LORA_MAX_RANK);
     d.partial_ctas = sm_count();
     if (e == cudaSuccess) e = dalloc(&d.partial, (size_t)d.partial_ctas * EXP_TILE_ELEMS);
@@ -567,7 +575,8 @@ namespace {
 __device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
 
 struct NoallocLayout {
-    size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, pq, z;
+    size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, pq, zcnt,
+        z;
     size_t total;
 };
 
@@ -597,6 +606,7 @@ NoallocLayout noalloc_layout(int T, int P, int capacity, int r_max)
     L.mtile = take(16 * mtiles);
     L.toff = take(4 * ((size_t)T + 1));
     L.pq = take(8 * p);
+    L.zcnt = take(4 * p);
     L.z = take(4 * p * (size_t)z_stride(r_max));
     L.total = off;
     return L;
@@ -655,6 +665,7 @@ extern "C" lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, 
     d.mtile = reinterpret_cast<int4 *>(base + L.mtile);
     d.toff = reinterpret_cast<int32_t *>(base + L.toff);
     d.pq = reinterpret_cast<int2 *>(base + L.pq);
+    d.zcnt = reinterpret_cast<int32_t *>(base + L.zcnt);
     d.z = reinterpret_cast<float *>(base + L.z);
     d.partial = nullptr;  // used by the fused kernel only
     d.partial_ctas = 0;

@@ -54,12 +54,11 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
     return acc;
 }
 
-__global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a)
+// One shrink item: pair q, rank rows [j0, j0 + warps of the CTA).  Every
+// thread of the CTA calls it; it returns once the CTA's copies have landed.
+// report: set the status bit of an unusable adapter (one item per pair does).
+__device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *xs, int q, int j0, bool report)
 {
-    extern __shared__ __align__(16) uint4 xs[];  // the pair's x row
-    pdl_launch_dependents();
-    pdl_wait();  // launched as a programmatic dependent of the mapping
-    const int q = blockIdx.x;
     // one round trip: the pair (its adapter is used only once q is known valid)
     const int pvalid = a.m.hdr[HDR_PVALID];
     const int ad = a.m.adapter[q], tk = a.m.tok[q];
@@ -67,7 +66,6 @@ __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a
     if (q >= pvalid)
         return;  // pairs left out of the mapping (and every pair when its offsets were malformed)
     const int r_max = a.pool.r_max;
-    const int j0 = blockIdx.y * (blockDim.x >> 5);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = j0 + warp;
     const bool row = j < r_max;  // rows are fetched before the rank is known
@@ -85,13 +83,9 @@ __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a
         av[u] = row && i < nv ? __ldcs(&ar[i]) : make_uint4(0u, 0u, 0u, 0u);
     }
     const int k = effective_rank(a.pool, a.ranks, ad);
-    if (k <= 0) {
-        if (k < 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    if (k <= 0 || j0 >= k) {
+        if (k < 0 && report && threadIdx.x == 0)
             atomicOr(a.m.hdr + HDR_STATUS, k == -1 ? LORA_DEV_UNREGISTERED : LORA_DEV_BAD_RANK);
-        cp_async_wait_all();
-        return;
-    }
-    if (j0 >= k) {
         cp_async_wait_all();
         return;
     }
@@ -124,6 +118,14 @@ __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (live && lane == 0)
         a.m.z[(size_t)q * a.zs + j] = al * acc;
+}
+
+__global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a)
+{
+    extern __shared__ __align__(16) uint4 xs[];  // the pair's x row
+    pdl_launch_dependents();
+    pdl_wait();  // launched as a programmatic dependent of the mapping
+    dec_shrink_item(a, xs, blockIdx.x, blockIdx.y * (blockDim.x >> 5), blockIdx.y == 0);
 }
 
 struct DecExpandArgs {
@@ -182,16 +184,12 @@ __device__ __forceinline__ void dec_rows(float (&acc)[8], const __nv_bfloat16 *b
     }
 }
 
-__global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
+// One expand item: token t, 256-column chunk c, on one warp.  wait_pair(q)
+// is called before the first read of pair q's z (the shrink's output).
+template <class WaitPair>
+__device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, int c, WaitPair wait_pair)
 {
-    pdl_launch_dependents();  // the next kernel in the stream may start its prologue
     const int lane = threadIdx.x & 31;
-    const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (g >= a.T * a.nc)
-        return;
-    // consecutive warps: consecutive tokens on one column chunk, so the B rows
-    // of an adapter several of them use come from L1 after the first
-    const int t = g % a.T, c = g / a.T;
     const int d_out = a.pool.d_out, r_max = a.pool.r_max;
     const int col = c * 256 + lane * 8;
     const bool on = col < d_out;  // the last chunk of a row may be partial
@@ -220,12 +218,12 @@ __global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
                                                     : make_uint4(0u, 0u, 0u, 0u);
         kk[i] = ad >= 0 ? dec_rank(a.pool, a.ranks, ad) : 0;
     }
-    pdl_wait();  // z of the shrink
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < DE_PP; ++i) {
         const int k = kk[i];
         if (k > 0) {
+            wait_pair(pq[i].x);
             const float *zr = a.m.z + (size_t)pq[i].x * a.zs;
             float zz[DE_PR];
 #pragma unroll
@@ -243,8 +241,11 @@ __global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
         if (v.y < 0)
             continue;
         const int k = dec_rank(a.pool, a.ranks, v.y);
-        if (k > 0)
-            dec_rows(acc, a.pool.B + (size_t)v.y * r_max * d_out + col, a.m.z + (size_t)v.x * a.zs, 0, k, d_out, on);
+        if (k > 0) {
+            wait_pair(v.x);
+            dec_rows(acc, a.pool.B + (size_t)v.y * r_max * d_out + col, a.m.z + (size_t)v.x * a.zs, 0, k, d_out,
+                     on);
+        }
     }
     uint4 o;
     o.x = pack2(bf16lo(yv.x) + acc[0], bf16hi(yv.x) + acc[1]);
@@ -255,10 +256,105 @@ __global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
         *reinterpret_cast<uint4 *>(yp) = o;
 }
 
+__global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
+{
+    pdl_launch_dependents();  // the next kernel in the stream may start its prologue
+    const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (g >= a.T * a.nc)
+        return;
+    // consecutive warps: consecutive tokens on one column chunk, so the B rows
+    // of an adapter several of them use come from L1 after the first
+    bool waited = false;
+    dec_expand_item(a, g % a.T, g / a.T, [&](int) {
+        if (!waited) {
+            pdl_wait();  // z of the shrink
+            waited = true;
+        }
+    });
+}
+
+// ------------------------------------------------------------ fused (one launch)
+
+struct DecFusedArgs {
+    DecShrinkArgs s;
+    DecExpandArgs e;
+    int ng;  // shrink items per pair: rank rows in groups of 8
+};
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until *cnt >= target, for at most WAIT_LIMIT_NS (then LORA_DEV_TIMEOUT).
+__device__ __forceinline__ bool wait_count(const int32_t *cnt, int target, int32_t *status)
+{
+    if (ld_acquire_gpu(cnt) >= target)
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        for (int i = 0; i < 16; ++i) {
+            if (ld_acquire_gpu(cnt) >= target)
+                return true;
+            __nanosleep(32);
+        }
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            atomicOr(status, LORA_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// A cooperative launch, every CTA resident: each CTA first runs shrink items
+// (pair, 8 rank rows) and counts them per pair, then its warps run expand
+// items, each waiting only on the counters of its token's pairs.  The CTAs
+// never wait on one another during the shrink phase, so every counter is
+// reached.  The launch's epoch (launches since the mapping was built) sets
+// the counters' target; the last CTA to exit advances it.
+__global__ void __launch_bounds__(256, 1) k_dec_fused(const DecFusedArgs a)
+{
+    extern __shared__ __align__(16) uint4 xs[];
+    pdl_launch_dependents();
+    const MapDev &m = a.s.m;
+    int32_t *status = m.hdr + HDR_STATUS;
+    const int epoch = m.hdr[HDR_EPOCH];
+    const int pvalid = m.hdr[HDR_PVALID];
+    const int G = gridDim.x;
+    for (int it = blockIdx.x; it < pvalid * a.ng; it += G) {
+        const int q = it / a.ng, g = it % a.ng;
+        dec_shrink_item(a.s, xs, q, g * (blockDim.x >> 5), g == 0);
+        __syncthreads();  // z rows written, x row consumed
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicAdd(m.zcnt + q, 1);
+        }
+    }
+    const int target = (epoch + 1) * a.ng;
+    const int nw = blockDim.x >> 5;
+    bool ok = true;
+    for (int wi = blockIdx.x * nw + (threadIdx.x >> 5); wi < a.e.T * a.e.nc; wi += G * nw)
+        dec_expand_item(a.e, wi % a.e.T, wi / a.e.T, [&](int q) {
+            if (ok)
+                ok = wait_count(m.zcnt + q, target, status);
+        });
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(m.hdr + HDR_DEXIT, 1) == G - 1) {  // the last CTA of this launch
+            m.hdr[HDR_DEXIT] = 0;
+            __threadfence();
+            atomicAdd(m.hdr + HDR_EPOCH, 1);
+        }
+    }
+}
+
 }  // namespace
 
 // The x row is staged in shared memory: d_in * 2 bytes of at most 200 KB.
-bool decode_supported(int d_in, int d_out) { return d_in % 8 == 0 && d_out % 8 == 0 && d_in <= 100 * 1024; }
+constexpr int DS_SMEM_MAX = 200 * 1024;
+bool decode_supported(int d_in, int d_out) { return d_in % 8 == 0 && d_out % 8 == 0 && d_in * 2 <= DS_SMEM_MAX; }
 
 cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
                           const MapDev &m, int T, int P, cudaStream_t st)
@@ -269,7 +365,7 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_dec_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        cudaError_t e = cudaFuncSetAttribute(k_dec_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, DS_SMEM_MAX);
         if (e != cudaSuccess)
             return e;
         attr_dev = dev;
@@ -304,6 +400,45 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_dec_expand, ea);
+}
+
+cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
+                                const MapDev &m, int T, int P, cudaStream_t st)
+{
+    if (!decode_supported(pool.d_in, pool.d_out))
+        return cudaErrorNotSupported;
+    static int attr_dev = -1, resident = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const size_t smem = (size_t)pool.d_in * 2;
+    if (attr_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(k_dec_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, DS_SMEM_MAX);
+        if (e != cudaSuccess)
+            return e;
+        // co-residency of every CTA: one per SM (the launch bound and the
+        // largest staging buffer allow one at the least)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, k_dec_fused, 256, DS_SMEM_MAX);
+        if (e != cudaSuccess)
+            return e;
+        attr_dev = dev;
+    }
+    if (resident < 1)
+        return cudaErrorNotSupported;
+    const int ng = (pool.r_max + 7) / 8;
+    const int nc = (pool.d_out + 255) / 256;
+    DecFusedArgs a{{x, pool, ranks, m, z_stride(pool.r_max)}, {y, pool, ranks, m, T, z_stride(pool.r_max), nc}, ng};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(sm_count(), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    (void)P;
+    return cudaLaunchKernelEx(&cfg, k_dec_fused, a);
 }
 
 }  // namespace tcl

@@ -43,8 +43,10 @@ constexpr int RANK_TAB_MAX = 2048;
 // Header words of the mapping (device int32).
 // HDR_BAR, HDR_BAR_BASE, HDR_EXIT: grid-barrier counters of the fused kernel.
 // HDR_NMTILES: tensor-core shrink tiles (MMA_TM pairs of one segment).
+// HDR_EPOCH, HDR_DEXIT: launches of the fused decode kernel since the mapping
+// was built, and its CTAs that have exited in the current launch.
 enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_BAR = 5, HDR_BAR_BASE = 6,
-       HDR_EXIT = 7, HDR_NMTILES = 8, HDR_WORDS = 9 };
+       HDR_EXIT = 7, HDR_NMTILES = 8, HDR_EPOCH = 9, HDR_DEXIT = 10, HDR_WORDS = 11 };
 
 // Tensor-core (tcgen05) prefill path: tiles of MMA_TM rows (pairs of one
 // segment for the shrink, consecutive tokens for the expand).
@@ -75,6 +77,7 @@ struct MapDev {
     int4 *mtile;                         // [mma_tile_bound] tensor-core shrink tiles {adapter, q0, n, segment}
     int32_t *toff;                       // [max_tokens+1] copy of the batch's CSR offsets
     int2 *pq;                            // [max_pairs] per CSR pair: {sorted position, adapter}, -1s if left out
+    int32_t *zcnt;                       // [max_pairs] per sorted pair: z row groups written (fused decode)
     float *z;                            // [max_pairs][LORA_MAX_RANK] shrink output
     float *partial;                      // [partial_ctas][EXP_TILE_ELEMS] fused-kernel tiles
     int partial_ctas;
@@ -114,6 +117,10 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
                           const MapDev &m, int T, int P, cudaStream_t st);
 // Dispatch: batches of at most this many tokens take the decode path.
 constexpr int DECODE_MAX_TOKENS = 256;
+// The same decode work as one cooperative launch (a CTA per SM): shrink
+// items first, then expand warps that wait on per-pair counters.
+cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
+                                const MapDev &m, int T, int P, cudaStream_t st);
 cudaError_t launch_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
                          const MapDev &m, int T, int P, const ExpandPlan &plan, int grid, cudaStream_t st);
 

@@ -135,10 +135,14 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
     pdl_wait();  // the previous kernel (which may still read this mapping) is done
     if (tid == 0) {
         m.hdr[HDR_STATUS] = 0;
-        m.hdr[HDR_BAR] = 0;  // fused-kernel barrier counters start over with every mapping
+        m.hdr[HDR_BAR] = 0;  // fused-kernel counters start over with every mapping
         m.hdr[HDR_BAR_BASE] = 0;
         m.hdr[HDR_EXIT] = 0;
+        m.hdr[HDR_EPOCH] = 0;
+        m.hdr[HDR_DEXIT] = 0;
     }
+    for (int q = tid; q < P; q += nthr)
+        m.zcnt[q] = 0;
     __syncthreads();
 
     // 1. CSR check
