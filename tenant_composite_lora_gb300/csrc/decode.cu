@@ -273,6 +273,107 @@ __global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
     });
 }
 
+// Few tokens at large ranks: a CTA of 8 warps per (token, 256 columns), warp
+// w taking rank rows w, w + 8, ... of every pair (all of a warp's rows of the
+// first pairs fetched before the dependency wait), partial sums reduced
+// through shared memory.
+constexpr int DW_WARPS = 8;
+constexpr int DW_PP = 2;                         // pairs whose rows are fetched before the wait
+constexpr int DW_PR = LORA_MAX_RANK / DW_WARPS;  // rows per warp and pair
+
+__global__ void __launch_bounds__(32 * DW_WARPS, 1) k_dec_expand_wide(const DecExpandArgs a)
+{
+    __shared__ float red[DW_WARPS - 1][256];
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x % a.T, c = blockIdx.x / a.T;
+    const int d_out = a.pool.d_out, r_max = a.pool.r_max;
+    const int col = c * 256 + lane * 8;
+    const bool on = col < d_out;
+    __nv_bfloat16 *yp = a.y + (size_t)t * d_out + (on ? col : 0);
+    const uint4 yv = on && warp == 0 ? *reinterpret_cast<const uint4 *>(yp) : make_uint4(0u, 0u, 0u, 0u);
+    const int pvalid = a.m.hdr[HDR_PVALID];
+    const int p0 = a.m.toff[t], p1 = a.m.toff[t + 1];
+    if (pvalid == 0)
+        return;  // uniform over the CTA
+    int2 pq[DW_PP];
+#pragma unroll
+    for (int i = 0; i < DW_PP; ++i)
+        pq[i] = p0 + i < p1 ? a.m.pq[p0 + i] : make_int2(-1, -1);
+    uint4 bpre[DW_PP][DW_PR];
+    int kk[DW_PP];
+#pragma unroll
+    for (int i = 0; i < DW_PP; ++i) {
+        const int ad = pq[i].y;
+        const __nv_bfloat16 *br = a.pool.B + (size_t)(ad < 0 ? 0 : ad) * r_max * d_out + col;
+#pragma unroll
+        for (int u = 0; u < DW_PR; ++u) {
+            const int j = warp + DW_WARPS * u;
+            bpre[i][u] = ad >= 0 && on && j < r_max ? __ldg(reinterpret_cast<const uint4 *>(br + (size_t)j * d_out))
+                                                    : make_uint4(0u, 0u, 0u, 0u);
+        }
+        kk[i] = ad >= 0 ? dec_rank(a.pool, a.ranks, ad) : 0;
+    }
+    pdl_wait();  // z of the shrink
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < DW_PP; ++i) {
+        const int k = kk[i];
+        if (k > 0) {
+            const float *zr = a.m.z + (size_t)pq[i].x * a.zs;
+            float zz[DW_PR];
+#pragma unroll
+            for (int u = 0; u < DW_PR; ++u) {
+                const int j = warp + DW_WARPS * u;
+                zz[u] = j < k ? __ldcg(zr + j) : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < DW_PR; ++u)
+                fma8(acc, zz[u], bpre[i][u]);
+        }
+    }
+    for (int p = p0 + DW_PP; p < p1; ++p) {
+        const int2 v = a.m.pq[p];
+        if (v.y < 0)
+            continue;
+        const int k = dec_rank(a.pool, a.ranks, v.y);
+        if (k <= 0)
+            continue;
+        const __nv_bfloat16 *br = a.pool.B + (size_t)v.y * r_max * d_out + col;
+        const float *zr = a.m.z + (size_t)v.x * a.zs;
+        uint4 bb[DW_PR];
+        float zz[DW_PR];
+#pragma unroll
+        for (int u = 0; u < DW_PR; ++u) {
+            const int j = warp + DW_WARPS * u;
+            const bool use = j < k;
+            bb[u] = use && on ? __ldg(reinterpret_cast<const uint4 *>(br + (size_t)j * d_out)) : make_uint4(0u, 0u, 0u, 0u);
+            zz[u] = use ? __ldcg(zr + j) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < DW_PR; ++u)
+            fma8(acc, zz[u], bb[u]);
+    }
+    if (warp > 0)
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            red[warp - 1][lane * 8 + e] = acc[e];
+    __syncthreads();
+    if (warp == 0) {
+        for (int w = 0; w < DW_WARPS - 1; ++w)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                acc[e] += red[w][lane * 8 + e];
+        uint4 o;
+        o.x = pack2(bf16lo(yv.x) + acc[0], bf16hi(yv.x) + acc[1]);
+        o.y = pack2(bf16lo(yv.y) + acc[2], bf16hi(yv.y) + acc[3]);
+        o.z = pack2(bf16lo(yv.z) + acc[4], bf16hi(yv.z) + acc[5]);
+        o.w = pack2(bf16lo(yv.w) + acc[6], bf16hi(yv.w) + acc[7]);
+        if (on)
+            *reinterpret_cast<uint4 *>(yp) = o;
+    }
+}
+
 // ------------------------------------------------------------ fused (one launch)
 
 struct DecFusedArgs {
@@ -389,10 +490,20 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
         return e;
     const int nc = (pool.d_out + 255) / 256;
     const long long warps = (long long)T * nc;
+    DecExpandArgs ea{y, pool, ranks, m, T, z_stride(pool.r_max), nc};
+    if (pool.r_max > 16 && warps <= 2LL * sm_count()) {
+        // few (token, chunk) items at large ranks: 8 warps share each item's rows
+        cudaLaunchConfig_t wcfg = {};
+        wcfg.gridDim = dim3((unsigned)warps, 1, 1);
+        wcfg.blockDim = dim3(32 * DW_WARPS, 1, 1);
+        wcfg.stream = st;
+        wcfg.attrs = attr;
+        wcfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&wcfg, k_dec_expand_wide, ea);
+    }
     int wpc = 8;  // warps per CTA: the most that still gives a CTA per SM
     while (wpc > 1 && (warps + wpc - 1) / wpc < sm_count())
         wpc >>= 1;
-    DecExpandArgs ea{y, pool, ranks, m, T, z_stride(pool.r_max), nc};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((warps + wpc - 1) / wpc), 1, 1);
     cfg.blockDim = dim3(32 * wpc, 1, 1);
