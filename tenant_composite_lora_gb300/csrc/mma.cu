@@ -773,18 +773,22 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                     for (int uu = u; uu < ut_end; ++uu)
                         epilogue(uu);
                 } else {
-                    for (int uu = u; uu < ut_end; ++uu) {
+                    // several passes: two units at a time (one per accumulator) share each pass
+                    for (int uu = u; uu < ut_end; uu += 2) {
+                        const int u2 = min(uu + 2, ut_end);
                         for (int p = 0; p < npass; ++p) {
                             const int s0 = p * ME_SMAX, s1 = min(ns, s0 + ME_SMAX);
                             wait_free();
                             build_zsel(0, nu, s0, s1);
-                            publish(uu, uu + 1, s0, s1, nu, p == 0, p == npass - 1, 0);
+                            publish(uu, u2, s0, s1, nu, p == 0, p == npass - 1, 0);
                         }
-                        epilogue(uu);
+                        for (int v = uu; v < u2; ++v)
+                            epilogue(v);
                     }
                 }
             } else {
-                for (int uu = u; uu < ut_end; ++uu) {
+                for (int uu = u; uu < ut_end; uu += 2) {
+                    const int u2 = min(uu + 2, ut_end);
                     for (int w = 0; w < nwin; ++w) {
                         const int w0 = w * ME_NU_MAX;
                         wait_free();
@@ -795,10 +799,11 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                             const int s0 = p * ME_SMAX, s1 = min(ns, s0 + ME_SMAX);
                             wait_free();
                             build_zsel(w0, nu, s0, s1);
-                            publish(uu, uu + 1, s0, s1, nu, w == 0 && p == 0, w == nwin - 1 && p == npass - 1, 0);
+                            publish(uu, u2, s0, s1, nu, w == 0 && p == 0, w == nwin - 1 && p == npass - 1, 0);
                         }
                     }
-                    epilogue(uu);
+                    for (int v = uu; v < u2; ++v)
+                        epilogue(v);
                 }
             }
         }
