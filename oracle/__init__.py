@@ -135,7 +135,7 @@ def apply_workload(wl, ranks=None, threads: int = 1, want_acc: bool = True, y_in
                        r_max=wl.r_max, capacity=wl.capacity, threads=threads, want_acc=want_acc)
 
 
-def apply_tokens(wl, tokens, ranks=None):
+def apply_tokens(wl, tokens, ranks=None, threads: int = 1):
     """The oracle on a subset of tokens (their own pair lists); returns
     (y_out [len(tokens), d_out], acc, status).  Used for sampled parity at
     full size."""
@@ -151,4 +151,4 @@ def apply_tokens(wl, tokens, ranks=None):
     al = np.concatenate(lists_alpha) if lists_alpha else np.zeros(0, np.float32)
     r = wl.ranks if ranks is None else ranks
     return delta_apply(offs, ids, al, wl.x[tokens], wl.A, wl.B, r, wl.y[tokens],
-                       d_in=wl.d_in, d_out=wl.d_out, r_max=wl.r_max, capacity=wl.capacity)
+                       d_in=wl.d_in, d_out=wl.d_out, r_max=wl.r_max, capacity=wl.capacity, threads=threads)

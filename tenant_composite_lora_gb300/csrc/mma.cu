@@ -275,7 +275,7 @@ struct MeLayout {
 
 // One A-operand build, handed from the workers to the MMA warp.
 struct MeBuild {
-    int u0, u1;       // units [u0, u1) take their slots [s0, s1) from this build
+    int u0, u1;       // units [u0, u1) take their slots [s0, s1) from this operand
     int s0, s1;       // window slots held (operand column block jj = s - s0)
     int nu;           // adapters in the window lists
     int first, last;  // the build starts / ends each unit's sum
