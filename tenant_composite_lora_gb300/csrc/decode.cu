@@ -68,7 +68,16 @@ __device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *x
     const int r_max = a.pool.r_max;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = j0 + warp;
-    const bool row = j < r_max;  // rows are fetched before the rank is known
+    // the first row group fetches its rows before the rank is known (they are
+    // almost always below it); later groups read the rank first, so rows at or
+    // beyond it are never fetched
+    int k_early = r_max;
+    if (j0 > 0) {
+        k_early = effective_rank(a.pool, a.ranks, ad);
+        if (k_early <= j0)
+            return;  // no row of this group is used (status reported by group 0)
+    }
+    const bool row = j < k_early;
     const int d_in = a.pool.d_in, nv = d_in / 8;  // 16-byte vectors per row
     // second round trip: x row (to shared memory), the A row, the rank
     const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)tk * d_in);
