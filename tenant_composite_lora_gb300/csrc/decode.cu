@@ -195,7 +195,7 @@ __device__ __forceinline__ void dec_rows(float (&acc)[8], const __nv_bfloat16 *b
 
 // One expand item: token t, 256-column chunk c, on one warp.  wait_pair(q)
 // is called before the first read of pair q's z (the shrink's output).
-template <class WaitPair>
+template <int PP, class WaitPair>
 __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, int c, WaitPair wait_pair)
 {
     const int lane = threadIdx.x & 31;
@@ -210,15 +210,15 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
     if (pvalid == 0)
         return;  // nothing valid (also: offsets malformed, the pair range is not defined)
     // round trip 2: {sorted position, adapter} of the first pairs
-    int2 pq[DE_PP];
+    int2 pq[PP];
 #pragma unroll
-    for (int i = 0; i < DE_PP; ++i)
+    for (int i = 0; i < PP; ++i)
         pq[i] = p0 + i < p1 ? a.m.pq[p0 + i] : make_int2(-1, -1);
     // round trip 3: their first B rows (whatever the rank turns out to be) and ranks
-    uint4 bpre[DE_PP][DE_PR];
-    int kk[DE_PP];
+    uint4 bpre[PP][DE_PR];
+    int kk[PP];
 #pragma unroll
-    for (int i = 0; i < DE_PP; ++i) {
+    for (int i = 0; i < PP; ++i) {
         const int ad = pq[i].y;
         const __nv_bfloat16 *br = a.pool.B + (size_t)(ad < 0 ? 0 : ad) * r_max * d_out + col;
 #pragma unroll
@@ -229,7 +229,7 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
     }
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < DE_PP; ++i) {
+    for (int i = 0; i < PP; ++i) {
         const int k = kk[i];
         if (k > 0) {
             wait_pair(pq[i].x);
@@ -245,7 +245,7 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
                 dec_rows(acc, a.pool.B + (size_t)pq[i].y * r_max * d_out + col, zr, DE_PR, k, d_out, on);
         }
     }
-    for (int p = p0 + DE_PP; p < p1; ++p) {
+    for (int p = p0 + PP; p < p1; ++p) {
         const int2 v = a.m.pq[p];
         if (v.y < 0)
             continue;
@@ -265,7 +265,11 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
         *reinterpret_cast<uint4 *>(yp) = o;
 }
 
-__global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
+// PP pairs' rows are fetched before the dependency wait; MINB CTAs per SM
+// (two when the batch needs more than one wave of warps, at the price of one
+// fewer prefetched pair).
+template <int PP, int MINB>
+__global__ void __launch_bounds__(256, MINB) k_dec_expand(const DecExpandArgs a)
 {
     pdl_launch_dependents();  // the next kernel in the stream may start its prologue
     const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(256, 1) k_dec_expand(const DecExpandArgs a)
     // consecutive warps: consecutive tokens on one column chunk, so the B rows
     // of an adapter several of them use come from L1 after the first
     bool waited = false;
-    dec_expand_item(a, g % a.T, g / a.T, [&](int) {
+    dec_expand_item<PP>(a, g % a.T, g / a.T, [&](int) {
         if (!waited) {
             pdl_wait();  // z of the shrink
             waited = true;
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(256, 1) k_dec_fused(const DecFusedArgs a)
     const int nw = blockDim.x >> 5;
     bool ok = true;
     for (int wi = blockIdx.x * nw + (threadIdx.x >> 5); wi < a.e.T * a.e.nc; wi += G * nw)
-        dec_expand_item(a.e, wi % a.e.T, wi / a.e.T, [&](int q) {
+        dec_expand_item<DE_PP>(a.e, wi % a.e.T, wi / a.e.T, [&](int q) {
             if (ok)
                 ok = wait_count(m.zcnt + q, target, status);
         });
@@ -519,7 +523,9 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_dec_expand, ea);
+    if (warps > 8LL * sm_count())  // more than one wave at one 8-warp CTA per SM
+        return cudaLaunchKernelEx(&cfg, k_dec_expand<2, 2>, ea);
+    return cudaLaunchKernelEx(&cfg, k_dec_expand<DE_PP, 1>, ea);
 }
 
 cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
