@@ -147,6 +147,17 @@ def dist_setup(n):
     return dist.get_rank(), dist.get_world_size(), dist
 
 
+def max_over_ranks(x, dist, device=None):
+    """The maximum of a float over all ranks (the float itself on one rank)."""
+    if dist is None:
+        return x
+    import torch
+    dev = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def bench_ours(args, rank, world, dist):
     import torch
     import tenant_composite_lora_gb300 as tcl
@@ -230,12 +241,7 @@ def bench_ours(args, rank, world, dist):
             e1.record(stream)
             e1.synchronize()
             torch.cuda.synchronize(dev)
-            ms = e0.elapsed_time(e1)
-            if dist is not None:
-                t = torch.tensor([ms], dtype=torch.float64, device=dev)
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                ms = float(t.item())
-            return ms
+            return max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
         passes = max(1, int(np.ceil(args.steps / R)))
         clk = ClockSampler(local)
@@ -256,6 +262,9 @@ def bench_ours(args, rank, world, dist):
             native.lora_delta_apply_host(x_h, y_h, off_h, ids_h, al_h, wl.T, wl.P, rep["pool"].handle, None,
                                          rep["mapping"].handle, stream)
         stream.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
         e2e_steps = max(args.steps, 10)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -265,7 +274,7 @@ def bench_ours(args, rank, world, dist):
                                          rep["mapping"].handle, stream)
         e1.record(stream)
         e1.synchronize()
-        ms_e2e = e0.elapsed_time(e1) / e2e_steps
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist, dev) / e2e_steps
         h2d = wl.x.nbytes + wl.y.nbytes + wl.offsets.nbytes + wl.ids.nbytes + wl.alpha.nbytes
         d2h = wl.y.nbytes
 
@@ -336,12 +345,12 @@ def oracle_baseline(wl, budget_s: float):
 def bench_reference(args):
     """The reference arm: the fp64 oracle on the host cores, W untimed and K
     timed steps, each step a bounded sample of the workload's tokens (the
-    whole batch when it fits) sized so that the run takes about 90 s."""
+    whole batch when it fits) sized so that the run takes about --ref-seconds (90 s by default)."""
     import oracle
     import workloads as W
     wl = W.make(args.config)
     th = oracle.max_threads()
-    budget = max(0.002, 90.0 / (args.steps + args.warmup))  # seconds per step
+    budget = max(0.002, args.ref_seconds / (args.steps + args.warmup))  # seconds per step
     n0 = min(wl.T, 16)
     t0 = time.perf_counter()
     oracle.apply_tokens(wl, np.arange(n0), threads=th)
@@ -380,6 +389,8 @@ def main():
     ap.add_argument("--config", default="distinct", choices=sorted(CONFIG_NAMES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="wall time the reference arm aims for over its warm-up and timed steps")
     ap.add_argument("--max-replicas", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", default="auto", choices=["auto", "split", "fused", "mma", "decode"],
@@ -387,12 +398,14 @@ def main():
     args = ap.parse_args()
     args.path_id = {"auto": 0, "split": 1, "fused": 2, "mma": 3, "decode": 4}[args.path]
     args.warmup = max(3, args.warmup)
-    rank, world, dist = dist_setup(args.gpus)
 
     if args.impl == "reference":
-        if rank == 0:
+        # the CPU oracle needs no process group: rank 0 alone runs and prints
+        if int(os.environ.get("RANK", "0")) == 0:
             print(json.dumps(bench_reference(args)))
         return
+
+    rank, world, dist = dist_setup(args.gpus)
 
     line, wl = bench_ours(args, rank, world, dist)
     if rank == 0:
