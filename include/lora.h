@@ -194,6 +194,12 @@ int lora_dispatch_choose(int T, int P, int r_max, int d_in, int d_out);
  * allocated inside the mapping on the first call for a given (d_in, d_out)
  * and reused after.  Stream-ordered: y_host is valid after the stream
  * synchronises.  Same element layouts as the device calls.
+ * A call that repeats the previous call's arguments exactly (pointers, T, P,
+ * pool, ranks, stream) is captured into a CUDA graph of the whole step, and
+ * later calls with those arguments replay it (one launch instead of nine
+ * API calls); the buffers' contents may change between calls.  Calls on a
+ * default stream, or on a stream that is being captured, always run eagerly,
+ * as does a step whose capture fails (e.g. copies from pageable memory).
  */
 lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_t *offsets_host,
                                   const int32_t *ids_host, const float *alpha_host, int T, int P,

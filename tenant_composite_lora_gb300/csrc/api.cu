@@ -13,6 +13,23 @@ struct lora_pool {
     tcl::MmaMaps maps;  // TMA descriptors of At and B (tensor-core path)
 };
 
+// The arguments of a lora_delta_apply_host call: a repeat of the same ones
+// replays a captured graph of the whole step.
+struct HostStepKey {
+    const void *x, *y;
+    const int32_t *off, *ids;
+    const float *alpha;
+    int T, P;
+    const lora_pool *pool;
+    const int32_t *ranks;
+    void *stream;
+    bool operator==(const HostStepKey &o) const
+    {
+        return x == o.x && y == o.y && off == o.off && ids == o.ids && alpha == o.alpha && T == o.T && P == o.P &&
+               pool == o.pool && ranks == o.ranks && stream == o.stream;
+    }
+};
+
 struct lora_mapping {
     int max_tokens, max_pairs, capacity, device;
     int T, P;
@@ -23,6 +40,11 @@ struct lora_mapping {
     int32_t *soff, *sids;
     float *salpha;
     int s_d_in, s_d_out;
+    // its step graph: `seen` is the last eager call's arguments, `exec` the
+    // graph captured for `graph_key`; nocap_key's capture failed (it stays eager)
+    HostStepKey seen, graph_key, nocap_key;
+    bool have_seen, have_nocap;
+    cudaGraphExec_t exec;
 };
 
 namespace tcl {
@@ -50,6 +72,33 @@ __global__ void k_transpose_bf16(const __nv_bfloat16 *__restrict__ src, __nv_bfl
 
 __global__ void k_set_int(int32_t *p, int v) { *p = v; }
 
+// Up to five copies in one launch, 16 bytes per thread-step where both ends
+// allow it: the host entry point's transfers between pinned host memory
+// (addressed directly by the GPU) and device staging.
+struct CopySet {
+    const unsigned char *src[5];
+    unsigned char *dst[5];
+    unsigned long long bytes[5];
+    int n;
+};
+
+__global__ void k_copy_set(const CopySet c)
+{
+    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+    const unsigned long long tid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+    for (int i = 0; i < c.n; ++i) {
+        const unsigned char *s = c.src[i];
+        unsigned char *d = c.dst[i];
+        const unsigned long long n = c.bytes[i];
+        const bool vec = ((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d)) & 15u) == 0;
+        const unsigned long long nv = vec ? n / 16 : 0;
+        for (unsigned long long j = tid; j < nv; j += stride)
+            reinterpret_cast<uint4 *>(d)[j] = reinterpret_cast<const uint4 *>(s)[j];
+        for (unsigned long long j = nv * 16 + tid; j < n; j += stride)
+            d[j] = s[j];
+    }
+}
+
 int g_sm_count = 0;
 int g_sm_dev = -1;
 
@@ -66,6 +115,21 @@ cudaError_t launch_transpose_bf16(const __nv_bfloat16 *src, __nv_bfloat16 *dst, 
 cudaError_t launch_set_int(int32_t *p, int v, cudaStream_t st)
 {
     k_set_int<<<1, 1, 0, st>>>(p, v);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_set(const CopySet &c, cudaStream_t st)
+{
+    unsigned long long total = 0;
+    for (int i = 0; i < c.n; ++i)
+        total += c.bytes[i];
+    if (total == 0)
+        return cudaSuccess;
+    unsigned long long blocks = (total / 16 + 255) / 256;
+    const unsigned long long cap = 2ull * sm_count();
+    if (blocks > cap)
+        blocks = cap;
+    k_copy_set<<<(unsigned)(blocks ? blocks : 1), 256, 0, st>>>(c);
     return cudaGetLastError();
 }
 
@@ -118,6 +182,8 @@ cudaError_t dalloc(T **p, size_t count)
 
 void free_mapping(lora_mapping *m)
 {
+    if (m->exec)
+        cudaGraphExecDestroy(m->exec);
     MapDev &d = m->dev;
     void *ptrs[] = {d.tok,  d.adapter, d.src, d.pos,     d.alpha, d.seg_adapter, d.seg_start,
                     d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.pq, d.zcnt, d.z,
@@ -451,6 +517,88 @@ lora_status lora_delta_apply(const void *x_dev, void *y_dev, const lora_pool *po
     return lora_delta_apply_path(x_dev, y_dev, pool, ranks_dev, m, LORA_PATH_AUTO, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// The device address of a host buffer when the GPU can address it directly
+// (pinned memory), else nullptr.
+const void *device_alias(const void *host)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+// One step of lora_delta_apply_host, enqueued on the stream: the inputs in,
+// the mapping, the apply, y back.  With pinned buffers the transfers are two
+// copy kernels reading and writing host memory directly (one launch in, one
+// out); otherwise one cudaMemcpyAsync per buffer.
+lora_status host_step(const void *x_host, void *y_host, const int32_t *offsets_host, const int32_t *ids_host,
+                      const float *alpha_host, int T, int P, const lora_pool *pool, const int32_t *ranks_dev,
+                      lora_mapping *m, lora_stream_t stream)
+{
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t xb = (size_t)T * pool->d_in * sizeof(__nv_bfloat16);
+    const size_t yb = (size_t)T * pool->d_out * sizeof(__nv_bfloat16);
+    const size_t ob = (size_t)(T + 1) * sizeof(int32_t), pb = (size_t)P * sizeof(int32_t);
+    const void *ax = device_alias(x_host), *ay = device_alias(y_host), *ao = device_alias(offsets_host);
+    const void *ai = P > 0 ? device_alias(ids_host) : ao, *aa = P > 0 ? device_alias(alpha_host) : ao;
+    cudaError_t e = cudaSuccess;
+    const bool direct = ax && ay && ao && ai && aa;
+    if (direct) {
+        CopySet in{};
+        const void *srcs[5] = {ao, ai, aa, ax, ay};
+        void *dsts[5] = {m->soff, m->sids, m->salpha, m->sx, m->sy};
+        const size_t sizes[5] = {ob, P > 0 ? pb : 0, P > 0 ? pb : 0, xb, yb};
+        for (int i = 0; i < 5; ++i) {
+            in.src[in.n] = static_cast<const unsigned char *>(srcs[i]);
+            in.dst[in.n] = static_cast<unsigned char *>(dsts[i]);
+            in.bytes[in.n] = sizes[i];
+            ++in.n;
+        }
+        e = launch_copy_set(in, st);
+    } else {
+        e = cudaMemcpyAsync(m->soff, offsets_host, ob, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess && P > 0)
+            e = cudaMemcpyAsync(m->sids, ids_host, pb, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess && P > 0)
+            e = cudaMemcpyAsync(m->salpha, alpha_host, pb, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess && xb)
+            e = cudaMemcpyAsync(m->sx, x_host, xb, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess && yb)
+            e = cudaMemcpyAsync(m->sy, y_host, yb, cudaMemcpyHostToDevice, st);
+    }
+    if (e != cudaSuccess)
+        return from_cuda(e);
+    lora_status s = lora_build_mapping(m, m->soff, m->sids, m->salpha, T, P, stream);
+    if (s != LORA_OK)
+        return s;
+    s = lora_delta_apply(m->sx, m->sy, pool, ranks_dev, m, stream);
+    if (s != LORA_OK)
+        return s;
+    if (yb) {
+        if (direct) {
+            CopySet out{};
+            out.src[0] = static_cast<const unsigned char *>(m->sy);
+            out.dst[0] = static_cast<unsigned char *>(const_cast<void *>(ay));
+            out.bytes[0] = yb;
+            out.n = 1;
+            e = launch_copy_set(out, st);
+        } else {
+            e = cudaMemcpyAsync(y_host, m->sy, yb, cudaMemcpyDeviceToHost, st);
+        }
+    }
+    return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
 lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_t *offsets_host,
                                   const int32_t *ids_host, const float *alpha_host, int T, int P,
                                   const lora_pool *pool, const int32_t *ranks_dev, lora_mapping *m,
@@ -482,30 +630,53 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
             return from_cuda(e);
         m->s_d_in = pool->d_in;
         m->s_d_out = pool->d_out;
+        if (m->exec) {  // it copies into the old staging
+            cudaGraphExecDestroy(m->exec);
+            m->exec = nullptr;
+        }
+        m->have_seen = false;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t xb = (size_t)T * pool->d_in * sizeof(__nv_bfloat16);
-    const size_t yb = (size_t)T * pool->d_out * sizeof(__nv_bfloat16);
-    e = cudaMemcpyAsync(m->soff, offsets_host, (size_t)(T + 1) * sizeof(int32_t), cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && P > 0)
-        e = cudaMemcpyAsync(m->sids, ids_host, (size_t)P * sizeof(int32_t), cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && P > 0)
-        e = cudaMemcpyAsync(m->salpha, alpha_host, (size_t)P * sizeof(float), cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && xb)
-        e = cudaMemcpyAsync(m->sx, x_host, xb, cudaMemcpyHostToDevice, st);
-    if (e == cudaSuccess && yb)
-        e = cudaMemcpyAsync(m->sy, y_host, yb, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess)
-        return from_cuda(e);
-    lora_status s = lora_build_mapping(m, m->soff, m->sids, m->salpha, T, P, stream);
-    if (s != LORA_OK)
-        return s;
-    s = lora_delta_apply(m->sx, m->sy, pool, ranks_dev, m, stream);
-    if (s != LORA_OK)
-        return s;
-    if (yb)
-        e = cudaMemcpyAsync(y_host, m->sy, yb, cudaMemcpyDeviceToHost, st);
-    return from_cuda(e);
+    const HostStepKey key{x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, stream};
+    if (m->exec && m->graph_key == key) {
+        m->T = T;  // the host-side state lora_build_mapping would leave
+        m->P = P;
+        m->built = true;
+        return from_cuda(cudaGraphLaunch(m->exec, st));
+    }
+    // A repeat of the previous eager call (whose run did every lazy set-up) is
+    // captured; graphs need a stream of the caller's own that is not capturing.
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const bool capturable = st != nullptr && st != cudaStreamPerThread &&
+                            cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone;
+    if (capturable && m->have_seen && m->seen == key && !(m->have_nocap && m->nocap_key == key)) {
+        cudaGraph_t graph = nullptr;
+        cudaGraphExec_t exec = nullptr;
+        lora_status s = from_cuda(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
+        if (s == LORA_OK) {
+            s = host_step(x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, m, stream);
+            const cudaError_t e2 = cudaStreamEndCapture(st, &graph);
+            if (s == LORA_OK && e2 == cudaSuccess && graph)
+                s = from_cuda(cudaGraphInstantiate(&exec, graph, 0));
+            else if (s == LORA_OK)
+                s = from_cuda(e2 != cudaSuccess ? e2 : cudaErrorStreamCaptureInvalidated);
+            if (graph)
+                cudaGraphDestroy(graph);
+        }
+        if (s == LORA_OK && exec) {
+            if (m->exec)
+                cudaGraphExecDestroy(m->exec);
+            m->exec = exec;
+            m->graph_key = key;
+            return from_cuda(cudaGraphLaunch(exec, st));
+        }
+        cudaGetLastError();  // capture failed: this key runs eagerly from now on
+        m->nocap_key = key;
+        m->have_nocap = true;
+    }
+    m->seen = key;
+    m->have_seen = true;
+    return host_step(x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, m, stream);
 }
 
 lora_status lora_mapping_status(const lora_mapping *m, lora_stream_t stream, int *device_error)

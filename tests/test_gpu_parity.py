@@ -6,6 +6,8 @@ on runs with y_in = 0 the delta-only bound |y - ref| <= 2^-7 |ref| +
 1e-3 rms(ref), which one bf16 rounding plus fp32 summation noise satisfy and a
 wrong or missing term does not (|delta| is far below the bf16 spacing of y_in).
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -291,6 +293,39 @@ def test_host_entry_point_matches_device_path():
     finally:
         dw.close()
     np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_entry_point_graph_replay(pinned):
+    """Repeated identical host calls: eager, then captured, then replayed;
+    new input values between calls must be picked up by the replay.  Pinned
+    buffers take the copy kernels, pageable ones the copy calls (whose
+    capture may be refused, leaving every call eager)."""
+    import tenant_composite_lora_gb300 as tcl
+    wl = W.distinct_decode()
+    dw = DeviceWorkload(wl)
+    s = torch.cuda.Stream()
+    host = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    try:
+        x_host = host(torch.from_numpy(wl.x.view(np.int16).copy()))
+        y_host = host(torch.empty(wl.y.shape, dtype=torch.int16))
+        off = host(torch.from_numpy(wl.offsets))
+        ids = host(torch.from_numpy(wl.ids))
+        al = host(torch.from_numpy(wl.alpha))
+        rng = np.random.default_rng(4)
+        for it in range(5):
+            y_in = W.f32_to_bf16_bits(rng.standard_normal(wl.y.shape).astype(np.float32))
+            al.copy_(torch.from_numpy((wl.alpha * (1 + it)).astype(np.float32)))
+            y_host.copy_(torch.from_numpy(y_in.view(np.int16)))
+            tcl.lora_delta_apply_host(x_host, y_host, off, ids, al, wl.T, wl.P, dw.pool.handle, None,
+                                      dw.mapping.handle, s)
+            s.synchronize()
+            got = y_host.numpy().view(np.uint16).copy()
+            wl_it = dataclasses.replace(wl, alpha=(wl.alpha * (1 + it)).astype(np.float32), y=y_in)
+            yref, _, _ = oracle.apply_workload(wl_it, threads=0)
+            stated_gate(got, yref)
+    finally:
+        dw.close()
 
 
 # ---------------------------------------------------------------- edge shapes
