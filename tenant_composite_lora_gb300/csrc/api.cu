@@ -82,19 +82,40 @@ struct CopySet {
     int n;
 };
 
-__global__ void k_copy_set(const CopySet c)
+constexpr int CP_UNROLL = 4;  // 16-byte loads each thread keeps in flight
+
+__global__ void __launch_bounds__(256) k_copy_set(const CopySet c)
 {
-    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+    const unsigned long long nthr = (unsigned long long)gridDim.x * blockDim.x;
     const unsigned long long tid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
-    for (int i = 0; i < c.n; ++i) {
+    const unsigned long long span = nthr * CP_UNROLL;  // vectors one round of the grid moves
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {  // unrolled: the parameter arrays stay unindexed at run time
+        if (i >= c.n)
+            break;
         const unsigned char *s = c.src[i];
         unsigned char *d = c.dst[i];
         const unsigned long long n = c.bytes[i];
         const bool vec = ((reinterpret_cast<uintptr_t>(s) | reinterpret_cast<uintptr_t>(d)) & 15u) == 0;
         const unsigned long long nv = vec ? n / 16 : 0;
-        for (unsigned long long j = tid; j < nv; j += stride)
-            reinterpret_cast<uint4 *>(d)[j] = reinterpret_cast<const uint4 *>(s)[j];
-        for (unsigned long long j = nv * 16 + tid; j < n; j += stride)
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(s);
+        uint4 *d4 = reinterpret_cast<uint4 *>(d);
+        // whole rounds: block b's threads own [b * 256 * CP_UNROLL, +256 * CP_UNROLL) of each
+        // round, the CP_UNROLL loads of a thread blockDim apart (coalesced per warp)
+        const unsigned long long full = nv / span * span;
+        for (unsigned long long base = (unsigned long long)blockIdx.x * blockDim.x * CP_UNROLL + threadIdx.x;
+             base < full; base += span) {
+            uint4 v[CP_UNROLL];
+#pragma unroll
+            for (int u = 0; u < CP_UNROLL; ++u)
+                v[u] = s4[base + (unsigned long long)u * blockDim.x];
+#pragma unroll
+            for (int u = 0; u < CP_UNROLL; ++u)
+                d4[base + (unsigned long long)u * blockDim.x] = v[u];
+        }
+        for (unsigned long long j = full + tid; j < nv; j += nthr)
+            d4[j] = s4[j];
+        for (unsigned long long j = nv * 16 + tid; j < n; j += nthr)
             d[j] = s[j];
     }
 }
@@ -125,8 +146,8 @@ cudaError_t launch_copy_set(const CopySet &c, cudaStream_t st)
         total += c.bytes[i];
     if (total == 0)
         return cudaSuccess;
-    unsigned long long blocks = (total / 16 + 255) / 256;
-    const unsigned long long cap = 2ull * sm_count();
+    unsigned long long blocks = (total / 16 + 256ull * CP_UNROLL - 1) / (256ull * CP_UNROLL);
+    const unsigned long long cap = 4ull * sm_count();
     if (blocks > cap)
         blocks = cap;
     k_copy_set<<<(unsigned)(blocks ? blocks : 1), 256, 0, st>>>(c);
