@@ -61,13 +61,23 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def sources_digest() -> str:
-    """Digest of every kernel source and the ABI header: a traffic figure taken
-    with other sources no longer describes the kernels."""
+# kernel sources of each path's apply kernels (besides the shared headers)
+PATH_SOURCES = {
+    "decode": ["decode.cu"],
+    "mma": ["mma.cu", "tcgen05.cuh"],
+    "split": ["shrink.cu", "shrink_core.cuh", "expand.cu", "expand_core.cuh"],
+    "fused": ["fused.cu", "shrink_core.cuh", "expand_core.cuh"],
+}
+SHARED_SOURCES = ["internal.h", "ptx.cuh"]
+
+
+def sources_digest(path: str) -> str:
+    """Digest of the sources a path's apply kernels are built from and of the
+    ABI header: a traffic figure taken with other sources no longer describes
+    the kernels."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tenant_composite_lora_gb300", "csrc")
-    files = sorted(f for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h")))
-    for f in files:
+    for f in sorted(set(PATH_SOURCES[path] + SHARED_SOURCES)):
         h.update(f.encode())
         h.update(open(os.path.join(csrc, f), "rb").read())
     h.update(open(os.path.join(ROOT, "include", "lora.h"), "rb").read())
@@ -76,8 +86,8 @@ def sources_digest() -> str:
 
 def ncu_traffic(config: str, path: str):
     """dram bytes (read + write) per lora_delta_apply, summed over the apply's
-    kernels, from a committed ncu summary; valid only while the kernel sources
-    are unchanged."""
+    kernels, from a committed ncu summary; valid only while the path's kernel
+    sources are unchanged."""
     fp = os.path.join(ROOT, "profiles", f"traffic_{config}_{path}.txt")
     if not os.path.exists(fp):
         return None
@@ -86,7 +96,7 @@ def ncu_traffic(config: str, path: str):
         if ":" in line:
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    if kv.get("sources_sha256_16") != sources_digest():
+    if kv.get("sources_sha256_16") != sources_digest(path):
         return None
     try:
         return int(kv["dram_bytes_per_apply"])

@@ -47,13 +47,21 @@ namespace {
 
 constexpr int MS_THREADS = 192;  // warps 0-3: x gather + epilogue; warp 4: MMA; warp 5: A by TMA
 constexpr int MS_STAGES = 4;
-constexpr int MS_LAG = 2;                                // cp.async groups kept in flight per gather thread
-constexpr int MS_X_BYTES = MMA_TM * 128;                 // 128 rows x 64 bf16
-constexpr int MS_A_BYTES = LORA_MAX_RANK * 128;          // up to 64 rows x 64 bf16
-constexpr int MS_STAGE_BYTES = MS_X_BYTES + MS_A_BYTES;  // 24 KB
-constexpr int MS_SMEM = 1024 + MS_STAGES * MS_STAGE_BYTES;
-constexpr int MS_PART_STRIDE = LORA_MAX_RANK + 4;        // fp32 partial row stride (floats)
-static_assert(MMA_TM * MS_PART_STRIDE * 4 <= MS_STAGES * MS_STAGE_BYTES, "partial fits the stages");
+constexpr int MS_LAG = 3;                        // cp.async groups kept in flight per gather thread, < MS_STAGES
+constexpr int MS_X_BYTES = MMA_TM * 128;         // 128 rows x 64 bf16
+constexpr int MS_A_BYTES = LORA_MAX_RANK * 128;  // up to 64 rows x 64 bf16
+constexpr int MS_SMEM_MAX = 1024 + MS_STAGES * (MS_X_BYTES + MS_A_BYTES);
+constexpr int MS_PART_STRIDE = LORA_MAX_RANK + 4;  // fp32 partial row stride (floats)
+static_assert(MS_LAG < MS_STAGES, "the gather runs at most MS_STAGES stages ahead of the MMAs");
+static_assert(MMA_TM * MS_PART_STRIDE * 4 <= MS_STAGES * (MS_X_BYTES + 16 * 128), "partial fits the stages");
+
+// A stage holds the x rows and A's rows up to the pool's rank rounded to 16
+// (a multiple of 2 KB, so every stage starts 1024-aligned); small ranks leave
+// room for three CTAs per SM.
+inline int ms_stage_bytes(int r_max)
+{
+    return MS_X_BYTES + ((r_max + 15) & ~15) * 128;
+}
 
 struct MmaShrinkArgs {
     const __nv_bfloat16 *x;
@@ -62,6 +70,7 @@ struct MmaShrinkArgs {
     MapDev m;
     int zs;  // z row stride (floats)
     int ck;  // CTAs per cluster (K split)
+    int sb;  // bytes per pipeline stage (ms_stage_bytes)
 };
 
 __device__ __forceinline__ uint32_t xrow_offset(int row, int ch)
@@ -116,21 +125,31 @@ __global__ void __launch_bounds__(MS_THREADS, 1)
     const uint32_t taddr = s_taddr;
 
     if (warp < 4) {
-        // ---- x rows of the tile's pairs, gathered into the swizzled K-major layout
-        const int row = tid;
-        const bool valid = row < n;
-        const __nv_bfloat16 *xr = a.x + (valid ? (size_t)a.m.tok[q0 + row] * d_in : 0);
+        // ---- x rows of the tile's pairs, gathered into the swizzled K-major layout.
+        // Eight lanes share a row (16 bytes each), so one warp instruction moves
+        // four whole 128-byte lines; warp w owns rows 32w .. 32w + 31.
+        const int sub = lane >> 3, ch = lane & 7;
+        const __nv_bfloat16 *xr[8];
+        uint32_t dst[8];
+        unsigned live = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int row = warp * 32 + i * 4 + sub;
+            const bool valid = row < n;
+            xr[i] = a.x + (valid ? (size_t)a.m.tok[q0 + row] * d_in : 0) + ch * 8;
+            dst[i] = xrow_offset(row, ch);
+            live |= valid ? 1u << i : 0u;
+        }
         for (int it = 0; it < nk; ++it) {
             const int s = it % MS_STAGES;
             if (it >= MS_STAGES && !mbar_wait_bounded(&empty[s], ((it / MS_STAGES) - 1) & 1, status))
                 break;
-            unsigned char *sx = smem + s * MS_STAGE_BYTES;
-            if (valid) {
-                const __nv_bfloat16 *src = xr + (size_t)(kb0 + it) * 64;
+            unsigned char *sx = smem + s * a.sb;
+            const size_t col = (size_t)(kb0 + it) * 64;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                    cp_async16(sx + xrow_offset(row, ch), src + ch * 8);
-            }
+            for (int i = 0; i < 8; ++i)
+                if (live & (1u << i))
+                    cp_async16(sx + dst[i], xr[i] + col);
             cp_async_commit();
             if (it >= MS_LAG) {
                 cp_async_wait_group<MS_LAG>();
@@ -150,7 +169,7 @@ __global__ void __launch_bounds__(MS_THREADS, 1)
                 const int s = it % MS_STAGES;
                 if (it >= MS_STAGES && !mbar_wait_bounded(&empty[s], ((it / MS_STAGES) - 1) & 1, status))
                     break;
-                unsigned char *sa = smem + s * MS_STAGE_BYTES + MS_X_BYTES;
+                unsigned char *sa = smem + s * a.sb + MS_X_BYTES;
                 mbar_arrive_expect_tx(&full_a[s], (uint32_t)N * 128);
                 for (int c = 0; c < N / 16; ++c)
                     tma_load_2d(sa + c * 2048, &map_at, (kb0 + it) * 64, row0 + 16 * c, &full_a[s]);
@@ -171,7 +190,7 @@ __global__ void __launch_bounds__(MS_THREADS, 1)
                 if (!ok)
                     break;
                 tc_fence_after();
-                const uint32_t xs = smem_u32(smem + s * MS_STAGE_BYTES);
+                const uint32_t xs = smem_u32(smem + s * a.sb);
                 const uint32_t as = xs + MS_X_BYTES;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
@@ -963,7 +982,8 @@ cudaError_t launch_mma(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &
         int dev = 0;
         cudaGetDevice(&dev);
         if (attr_dev != dev) {
-            cudaError_t e = cudaFuncSetAttribute(k_mma_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, MS_SMEM);
+            cudaError_t e = cudaFuncSetAttribute(k_mma_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   MS_SMEM_MAX);
             if (e == cudaSuccess)
                 e = cudaFuncSetAttribute(k_mma_shrink, cudaFuncAttributePreferredSharedMemoryCarveout,
                                          cudaSharedmemCarveoutMaxShared);
@@ -971,11 +991,12 @@ cudaError_t launch_mma(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &
                 return e;
             attr_dev = dev;
         }
-        MmaShrinkArgs sa{x, pool, ranks, m, z_stride(pool.r_max), ck};
+        const int sb = ms_stage_bytes(pool.r_max);
+        MmaShrinkArgs sa{x, pool, ranks, m, z_stride(pool.r_max), ck, sb};
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(tiles * ck, 1, 1);
         cfg.blockDim = dim3(MS_THREADS, 1, 1);
-        cfg.dynamicSmemBytes = MS_SMEM;
+        cfg.dynamicSmemBytes = 1024 + MS_STAGES * sb;
         cfg.stream = st;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
