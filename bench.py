@@ -104,11 +104,84 @@ def ncu_traffic(config: str, path: str):
         return None
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons read through NVML (the driver's
+    libnvidia-ml), polled from a thread: fine-grained enough for timed
+    regions of a few milliseconds.  Reading only; no setting is changed."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        found = False
+        try:  # the CUDA device by UUID (NVML indexes ignore CUDA_VISIBLE_DEVICES)
+            import torch
+            uuid = str(torch.cuda.get_device_properties(cuda_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            found = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) == 0
+        except Exception:
+            found = False
+        if not found:
+            n = ctypes.c_uint()
+            self.lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+            idx = 0 if n.value == 1 else cuda_index
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx), ctypes.byref(self.dev)) != 0:
+                raise RuntimeError("no NVML handle")
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))  # 1 = SM clock
+        self.max_mhz = float(mx.value)
+        self.reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.sm, self.bits = [], 0
+        self.stop_flag = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def sample(self):
+        c = self.ct.c_uint()
+        r = self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, self.ct.byref(c)) == 0:
+            self.sm.append(float(c.value))
+        if self.reason_fn(self.dev, self.ct.byref(r)) == 0:
+            self.bits |= int(r.value)
+
+    def _run(self):
+        while not self.stop_flag.is_set():
+            self.sample()
+            time.sleep(0.0005)
+
+    def start(self):
+        self.sample()
+        self.thread.start()
+
+    def stop(self) -> dict:
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        self.sample()
+        reasons = sorted(v for k, v in self.REASONS.items() if self.bits & k)
+        return {"sm_mhz": statistics.median(self.sm) if self.sm else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.sm), "source": "nvml"}
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """Clock / throttle samples during the timed region: NVML when the driver
+    library loads, else nvidia-smi."""
 
     def __init__(self, index: int):
         self.proc = None
+        self.nvml = None
+        try:
+            self.nvml = NvmlClocks(index)
+            self.nvml.start()
+            return
+        except Exception:
+            self.nvml = None
         self.path = os.path.join(tempfile.gettempdir(), f"tclora_clocks_{os.getpid()}.csv")
         q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -123,6 +196,8 @@ class ClockSampler:
             self.proc = None
 
     def stop(self) -> dict:
+        if self.nvml is not None:
+            return self.nvml.stop()
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -146,7 +221,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvidia-smi"}
 
 
 def dist_setup(n):

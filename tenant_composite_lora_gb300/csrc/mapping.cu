@@ -83,6 +83,8 @@ __device__ Scan4 block_exclusive_scan4(Scan4 v, Scan4 &total, int *sh /* [4 * 32
     return {r[0], r[1], r[2], r[3]};
 }
 
+constexpr int MAP_STAGE_U = 8;  // staged words per thread per round (loads in flight)
+
 struct MapArgs {
     MapDev m;
     const int32_t *off, *ids;
@@ -111,12 +113,29 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         int32_t *s_off = sh, *s_ids = sh + (T + 1), *s_al = s_ids + P;
         tok = s_al + P;
         hist = tok + P;
-        for (int i = tid; i <= T; i += nthr)
-            s_off[i] = a.off[i];
+        // offsets, ids and alpha bits are consecutive in shared memory: one
+        // index space, MAP_STAGE_U loads in flight per thread before any store
         const int32_t *alg = reinterpret_cast<const int32_t *>(a.alpha);
-        for (int p = tid; p < P; p += nthr) {
-            s_ids[p] = a.ids[p];
-            s_al[p] = alg[p];
+        const int n_off = T + 1, n_all = T + 1 + 2 * P;
+        for (int base = 0; base < n_all; base += MAP_STAGE_U * nthr) {
+            int32_t v[MAP_STAGE_U];
+#pragma unroll
+            for (int u = 0; u < MAP_STAGE_U; ++u) {
+                const int i = base + u * nthr + tid;
+                v[u] = 0;
+                if (i < n_off)
+                    v[u] = __ldg(a.off + i);
+                else if (i < n_off + P)
+                    v[u] = __ldg(a.ids + (i - n_off));
+                else if (i < n_all)
+                    v[u] = __ldg(alg + (i - n_off - P));
+            }
+#pragma unroll
+            for (int u = 0; u < MAP_STAGE_U; ++u) {
+                const int i = base + u * nthr + tid;
+                if (i < n_all)
+                    sh[i] = v[u];
+            }
         }
         off = s_off;
         ids = s_ids;
