@@ -13,15 +13,18 @@
 //      (one coalesced read; every later step works on shared memory);
 //   1. check the CSR offsets;
 //   2. expand the offsets into the token of each pair, and build per-warp
-//      histograms of the ids over contiguous chunks of the pairs (warp-level
-//      match + popcount, no atomics; layout [warp][bin], conflict-free);
+//      histograms of the ids over contiguous chunks of the pairs (shared
+//      memory atomics into the warp's own row; layout [warp][bin]);
 //   3. block scans over the bins give every warp's first output slot per
 //      bin, the segments, the shrink tiles (<= SHRINK_TT pairs of one
 //      segment) and the tensor-core shrink tiles (<= MMA_TM pairs of one
 //      segment); slots up to the host-known bounds get empty sentinels;
 //   4. each warp rescans its chunk and scatters: rank among equal keys =
 //      earlier lanes with the same key + the warp's running cursor; the
-//      token also goes to its shrink tile's token list.
+//      token also goes to its shrink tile's token list;
+//   5. when the sorted token and source of every position fit in shared
+//      memory, step 4 scatters only there and the sorted arrays are written
+//      afterwards position by position, so that every store is coalesced.
 // Stability: chunks are in CSR order, warps are ranked by chunk, lanes by
 // pair index, so ties keep CSR order -- the tuples come out ordered by
 // (adapter, p).  The result does not depend on timing.
@@ -90,6 +93,7 @@ struct MapArgs {
     const int32_t *off, *ids;
     const float *alpha;
     int T, P, cap, nw, staged, tile_bound, mtile_bound;
+    int sorted_smem;  // the scatter lands in shared memory, the sorted arrays are written coalesced after
 };
 
 
@@ -149,6 +153,8 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
     }
     // per bin: first sorted position and first shrink tile of its segment
     int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
+    // sorted token and source pair per position (with sorted_smem)
+    int32_t *s_stok = bin_tile + cap, *s_ssrc = s_stok + P;
     for (int i = tid; i < nw * cap; i += nthr)
         hist[i] = 0;
     pdl_wait();  // the previous kernel (which may still read this mapping) is done
@@ -207,9 +213,8 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
             const int id = valid ? ids[p] : 0;
             const bool ok = valid && id >= 0 && id < cap;
             bad_id |= valid && !ok;
-            const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
-            if (ok && lane == __ffs(peers) - 1)
-                h[id] += __popc(peers);
+            if (ok)
+                atomicAdd(&h[id], 1);  // the warp's own histogram: counts only, order is irrelevant here
         }
     }
     if (bad_id)
@@ -278,12 +283,17 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
             if (ok) {
                 const int dst = cur + __popc(peers & lt);
                 const int t = tok[p];
-                m.tok[dst] = t;
-                const int r = dst - bin_first[id];
-                m.tile_tok[(bin_tile[id] + r / SHRINK_TT) * SHRINK_TT + r % SHRINK_TT] = t;
-                m.adapter[dst] = id;
-                reinterpret_cast<int32_t *>(m.alpha)[dst] = alb[p];
-                m.src[dst] = p;
+                if (a.sorted_smem) {
+                    s_stok[dst] = t;
+                    s_ssrc[dst] = p;
+                } else {
+                    m.tok[dst] = t;
+                    const int r = dst - bin_first[id];
+                    m.tile_tok[(bin_tile[id] + r / SHRINK_TT) * SHRINK_TT + r % SHRINK_TT] = t;
+                    m.adapter[dst] = id;
+                    reinterpret_cast<int32_t *>(m.alpha)[dst] = alb[p];
+                    m.src[dst] = p;
+                }
                 m.pos[p] = dst;
                 m.pq[p] = make_int2(dst, id);
             } else if (valid) {
@@ -294,6 +304,20 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
             if (ok && lane == __ffs(peers) - 1)
                 h[id] = cur + __popc(peers);
             __syncwarp();
+        }
+    }
+    if (a.sorted_smem) {
+        // 5. the sorted arrays, position by position (coalesced stores)
+        __syncthreads();
+        const int pvalid = carry.a;
+        for (int d = tid; d < pvalid; d += nthr) {
+            const int p = s_ssrc[d], t = s_stok[d], id = ids[p];
+            m.tok[d] = t;
+            m.src[d] = p;
+            m.adapter[d] = id;
+            reinterpret_cast<int32_t *>(m.alpha)[d] = alb[p];
+            const int r = d - bin_first[id];
+            m.tile_tok[(bin_tile[id] + r / SHRINK_TT) * SHRINK_TT + r % SHRINK_TT] = t;
         }
     }
 }
@@ -342,7 +366,12 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
     }
     if (nw < 1)
         return cudaErrorInvalidValue;
-    const size_t smem = 4 * ((staged ? (size_t)staged_words : 0) + (size_t)(nw + 2) * capacity);
+    // long batches: the sorted positions' token and source pair also in shared
+    // memory when they fit (short ones gain less than the extra phase costs)
+    const int sorted_smem =
+        staged && P >= 2048 && staged_words + (long long)(nw + 2) * capacity + 2LL * P <= budget;
+    const size_t smem = 4 * ((staged ? (size_t)staged_words : 0) + (size_t)(nw + 2) * capacity +
+                             (sorted_smem ? 2 * (size_t)P : 0));
     static int attr_done = -1;
     int dev = 0;
     cudaGetDevice(&dev);
@@ -357,7 +386,7 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
         attr_done = dev;
     }
     MapArgs a{m, offsets, ids, alpha, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity),
-              mma_tile_bound(P, capacity)};
+              mma_tile_bound(P, capacity), sorted_smem};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);

@@ -97,11 +97,14 @@ def _map_raw(offsets, ids, alpha, cap):
         m.close()
 
 
-def test_mapping_invalid_ids_and_empty_tokens():
+@pytest.mark.parametrize("n_tok", [300, 2000])
+def test_mapping_invalid_ids_and_empty_tokens(n_tok):
+    """Out-of-range ids among valid ones; 2000 tokens (about 4000 pairs) takes
+    the long-batch variant that stages the sorted arrays in shared memory."""
     rng = np.random.default_rng(11)
     cap = 37
-    counts = rng.integers(0, 5, size=300)
-    offsets = np.zeros(301, np.int32)
+    counts = rng.integers(0, 5, size=n_tok)
+    offsets = np.zeros(n_tok + 1, np.int32)
     offsets[1:] = np.cumsum(counts)
     ids = rng.integers(-3, cap + 3, size=int(counts.sum())).astype(np.int32)
     alpha = rng.standard_normal(ids.size).astype(np.float32)
