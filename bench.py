@@ -22,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -71,16 +72,33 @@ PATH_SOURCES = {
 SHARED_SOURCES = ["internal.h", "ptx.cuh"]
 
 
-def sources_digest(path: str) -> str:
-    """Digest of the sources a path's apply kernels are built from and of the
-    ABI header: a traffic figure taken with other sources no longer describes
-    the kernels."""
+_C_TOKENS = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'', re.S)
+
+
+def code_only(text: str) -> str:
+    """C/C++/CUDA source with comments removed and whitespace collapsed (string
+    and character literals kept): what the compiler sees, so that an edit of
+    the documentation does not count as a change of the kernels."""
+    text = _C_TOKENS.sub(lambda mt: " " if mt.group(0).startswith("/") else mt.group(0), text)
+    return " ".join(text.split())
+
+
+def path_source_files(path: str) -> list:
+    """Repository-relative files a path's apply kernels are built from."""
+    files = sorted(set(PATH_SOURCES[path] + SHARED_SOURCES))
+    return [f"tenant_composite_lora_gb300/csrc/{f}" for f in files] + ["include/lora.h"]
+
+
+def sources_digest(path: str, read=None) -> str:
+    """Digest of the code (comments aside) a path's apply kernels are built
+    from, the ABI header included: a traffic figure taken with other code no
+    longer describes the kernels.  `read(relpath) -> str` defaults to this
+    checkout."""
+    read = read or (lambda rel: open(os.path.join(ROOT, rel), encoding="utf-8").read())
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "tenant_composite_lora_gb300", "csrc")
-    for f in sorted(set(PATH_SOURCES[path] + SHARED_SOURCES)):
-        h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "lora.h"), "rb").read())
+    for rel in path_source_files(path):
+        h.update(rel.encode())
+        h.update(code_only(read(rel)).encode())
     return h.hexdigest()[:16]
 
 

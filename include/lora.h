@@ -194,12 +194,19 @@ int lora_dispatch_choose(int T, int P, int r_max, int d_in, int d_out);
  * allocated inside the mapping on the first call for a given (d_in, d_out)
  * and reused after.  Stream-ordered: y_host is valid after the stream
  * synchronises.  Same element layouts as the device calls.
+ * When all five host buffers are page-locked (device-addressable), the
+ * transfers are two launches of a copy kernel that reads and writes host
+ * memory directly; otherwise one cudaMemcpyAsync per buffer.
  * A call that repeats the previous call's arguments exactly (pointers, T, P,
  * pool, ranks, stream) is captured into a CUDA graph of the whole step, and
  * later calls with those arguments replay it (one launch instead of nine
- * API calls); the buffers' contents may change between calls.  Calls on a
- * default stream, or on a stream that is being captured, always run eagerly,
- * as does a step whose capture fails (e.g. copies from pageable memory).
+ * API calls); the buffers' contents may change between calls.  Every call
+ * looks up again whether each buffer is page-locked and at which device
+ * address; a replay happens only when that is unchanged since the capture.
+ * Calls on a default stream, or on a stream that is being captured, always
+ * run eagerly, as does a step whose capture fails (e.g. copies from
+ * pageable memory).  The mapping holds the staging and the graph: calls
+ * with one mapping must not run concurrently from several host threads.
  */
 lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_t *offsets_host,
                                   const int32_t *ids_host, const float *alpha_host, int T, int P,

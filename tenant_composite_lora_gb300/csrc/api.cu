@@ -30,6 +30,18 @@ struct HostStepKey {
     }
 };
 
+// Device addresses of a call's host buffers (null where the GPU cannot
+// address one directly); direct = all five exist, so the copy kernels run.
+struct HostAliases {
+    const void *x, *y, *off, *ids, *alpha;
+    bool direct;
+    bool operator==(const HostAliases &o) const
+    {
+        return x == o.x && y == o.y && off == o.off && ids == o.ids && alpha == o.alpha && direct == o.direct;
+    }
+    bool operator!=(const HostAliases &o) const { return !(*this == o); }
+};
+
 struct lora_mapping {
     int max_tokens, max_pairs, capacity, device;
     int T, P;
@@ -41,8 +53,10 @@ struct lora_mapping {
     float *salpha;
     int s_d_in, s_d_out;
     // its step graph: `seen` is the last eager call's arguments, `exec` the
-    // graph captured for `graph_key`; nocap_key's capture failed (it stays eager)
+    // graph captured for `graph_key` with the buffers' addresses `graph_alias`;
+    // nocap_key's capture failed (it stays eager)
     HostStepKey seen, graph_key, nocap_key;
+    HostAliases graph_alias;
     bool have_seen, have_nocap;
     cudaGraphExec_t exec;
 };
@@ -554,22 +568,34 @@ const void *device_alias(const void *host)
     return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
+HostAliases host_aliases(const void *x_host, const void *y_host, const int32_t *offsets_host, const int32_t *ids_host,
+                         const float *alpha_host, int P)
+{
+    HostAliases a{};
+    a.x = device_alias(x_host);
+    a.y = device_alias(y_host);
+    a.off = device_alias(offsets_host);
+    a.ids = P > 0 ? device_alias(ids_host) : a.off;
+    a.alpha = P > 0 ? device_alias(alpha_host) : a.off;
+    a.direct = a.x && a.y && a.off && a.ids && a.alpha;
+    return a;
+}
+
 // One step of lora_delta_apply_host, enqueued on the stream: the inputs in,
 // the mapping, the apply, y back.  With pinned buffers the transfers are two
 // copy kernels reading and writing host memory directly (one launch in, one
 // out); otherwise one cudaMemcpyAsync per buffer.
 lora_status host_step(const void *x_host, void *y_host, const int32_t *offsets_host, const int32_t *ids_host,
                       const float *alpha_host, int T, int P, const lora_pool *pool, const int32_t *ranks_dev,
-                      lora_mapping *m, lora_stream_t stream)
+                      lora_mapping *m, lora_stream_t stream, const HostAliases &al)
 {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t xb = (size_t)T * pool->d_in * sizeof(__nv_bfloat16);
     const size_t yb = (size_t)T * pool->d_out * sizeof(__nv_bfloat16);
     const size_t ob = (size_t)(T + 1) * sizeof(int32_t), pb = (size_t)P * sizeof(int32_t);
-    const void *ax = device_alias(x_host), *ay = device_alias(y_host), *ao = device_alias(offsets_host);
-    const void *ai = P > 0 ? device_alias(ids_host) : ao, *aa = P > 0 ? device_alias(alpha_host) : ao;
+    const void *ax = al.x, *ay = al.y, *ao = al.off, *ai = al.ids, *aa = al.alpha;
     cudaError_t e = cudaSuccess;
-    const bool direct = ax && ay && ao && ai && aa;
+    const bool direct = al.direct;
     if (direct) {
         CopySet in{};
         const void *srcs[5] = {ao, ai, aa, ax, ay};
@@ -659,11 +685,21 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const HostStepKey key{x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, stream};
+    // where the GPU can address each buffer, looked up on every call: the
+    // graph replays only while that is what it was captured with (a buffer
+    // freed and another one allocated at its address, pinned or not, is
+    // caught here)
+    const HostAliases al = host_aliases(x_host, y_host, offsets_host, ids_host, alpha_host, P);
     if (m->exec && m->graph_key == key) {
-        m->T = T;  // the host-side state lora_build_mapping would leave
-        m->P = P;
-        m->built = true;
-        return from_cuda(cudaGraphLaunch(m->exec, st));
+        if (m->graph_alias == al) {
+            m->T = T;  // the host-side state lora_build_mapping would leave
+            m->P = P;
+            m->built = true;
+            return from_cuda(cudaGraphLaunch(m->exec, st));
+        }
+        cudaGraphExecDestroy(m->exec);
+        m->exec = nullptr;
+        m->have_seen = false;  // run eagerly now, capture again on the next repeat
     }
     // A repeat of the previous eager call (whose run did every lazy set-up) is
     // captured; graphs need a stream of the caller's own that is not capturing.
@@ -675,7 +711,7 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
         cudaGraphExec_t exec = nullptr;
         lora_status s = from_cuda(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
         if (s == LORA_OK) {
-            s = host_step(x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, m, stream);
+            s = host_step(x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, m, stream, al);
             const cudaError_t e2 = cudaStreamEndCapture(st, &graph);
             if (s == LORA_OK && e2 == cudaSuccess && graph)
                 s = from_cuda(cudaGraphInstantiate(&exec, graph, 0));
@@ -689,6 +725,7 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
                 cudaGraphExecDestroy(m->exec);
             m->exec = exec;
             m->graph_key = key;
+            m->graph_alias = al;
             return from_cuda(cudaGraphLaunch(exec, st));
         }
         cudaGetLastError();  // capture failed: this key runs eagerly from now on
@@ -697,7 +734,7 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
     }
     m->seen = key;
     m->have_seen = true;
-    return host_step(x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, m, stream);
+    return host_step(x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, m, stream, al);
 }
 
 lora_status lora_mapping_status(const lora_mapping *m, lora_stream_t stream, int *device_error)

@@ -1,0 +1,53 @@
+"""Host-side pieces of the benchmark that need no GPU: the code digest that
+keeps a committed DRAM-traffic figure tied to the kernels it was measured on,
+and the reading of those figures."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_code_only_drops_comments_keeps_literals():
+    src = 'int a = 1; // note\n/* block\n comment */ const char *s = "//kept /*too*/"; char c = \'/\';\n'
+    assert bench.code_only(src) == 'int a = 1; const char *s = "//kept /*too*/"; char c = \'/\';'
+
+
+def _reader(overrides):
+    def read(rel):
+        if rel in overrides:
+            return overrides[rel]
+        return open(os.path.join(ROOT, rel), encoding="utf-8").read()
+    return read
+
+
+def test_digest_ignores_documentation_but_not_code():
+    rel = "tenant_composite_lora_gb300/csrc/decode.cu"
+    text = open(os.path.join(ROOT, rel), encoding="utf-8").read()
+    base = bench.sources_digest("decode")
+    assert bench.sources_digest("decode", _reader({rel: "// a new comment line\n" + text})) == base
+    assert bench.sources_digest("decode", _reader({rel: text.replace("{", "{ ", 1)})) == base
+    assert bench.sources_digest("decode", _reader({rel: text + "\nint extra_symbol;\n"})) != base
+    # a header shared by every path changes every path's digest; a path's own file only its own
+    hdr = "tenant_composite_lora_gb300/csrc/internal.h"
+    htext = open(os.path.join(ROOT, hdr), encoding="utf-8").read() + "\nint extra_symbol;\n"
+    for path in bench.PATH_SOURCES:
+        assert bench.sources_digest(path, _reader({hdr: htext})) != bench.sources_digest(path)
+    assert bench.sources_digest("mma", _reader({rel: text + "\nint extra_symbol;\n"})) == \
+        bench.sources_digest("mma")
+
+
+def test_traffic_files_parse(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "traffic_demo_decode.txt").write_text(
+        "# header\ndram_bytes_per_apply: 1234\nsources_sha256_16: %s\n" % bench.sources_digest("decode"))
+    (prof / "traffic_stale_decode.txt").write_text("dram_bytes_per_apply: 99\nsources_sha256_16: 0000\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "sources_digest", lambda path, read=None: bench_digest[path])
+    bench_digest = {"decode": open(prof / "traffic_demo_decode.txt").read().split()[-1]}
+    assert bench.ncu_traffic("demo", "decode") == 1234
+    assert bench.ncu_traffic("stale", "decode") is None  # taken with other kernel code
+    assert bench.ncu_traffic("absent", "decode") is None

@@ -298,36 +298,68 @@ def test_host_entry_point_matches_device_path():
     np.testing.assert_array_equal(got, ref)
 
 
+def _host_calls(wl, dw, x_host, y_host, off, ids, al, n_calls, before_call=None):
+    """n_calls host-entry steps on one stream with new alpha and y values each
+    time, every result checked against the oracle."""
+    import tenant_composite_lora_gb300 as tcl
+    s = torch.cuda.Stream()
+    rng = np.random.default_rng(4)
+    for it in range(n_calls):
+        if before_call is not None:
+            before_call(it)
+        y_in = W.f32_to_bf16_bits(rng.standard_normal(wl.y.shape).astype(np.float32))
+        al.copy_(torch.from_numpy((wl.alpha * (1 + it)).astype(np.float32)))
+        y_host.copy_(torch.from_numpy(y_in.view(np.int16)))
+        tcl.lora_delta_apply_host(x_host, y_host, off, ids, al, wl.T, wl.P, dw.pool.handle, None,
+                                  dw.mapping.handle, s)
+        s.synchronize()
+        got = y_host.numpy().view(np.uint16).copy()
+        wl_it = dataclasses.replace(wl, alpha=(wl.alpha * (1 + it)).astype(np.float32), y=y_in)
+        yref, _, _ = oracle.apply_workload(wl_it, threads=0)
+        stated_gate(got, yref)
+
+
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 def test_host_entry_point_graph_replay(pinned):
     """Repeated identical host calls: eager, then captured, then replayed;
     new input values between calls must be picked up by the replay.  Pinned
     buffers take the copy kernels, pageable ones the copy calls (whose
     capture may be refused, leaving every call eager)."""
-    import tenant_composite_lora_gb300 as tcl
     wl = W.distinct_decode()
     dw = DeviceWorkload(wl)
-    s = torch.cuda.Stream()
     host = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
     try:
-        x_host = host(torch.from_numpy(wl.x.view(np.int16).copy()))
-        y_host = host(torch.empty(wl.y.shape, dtype=torch.int16))
-        off = host(torch.from_numpy(wl.offsets))
-        ids = host(torch.from_numpy(wl.ids))
-        al = host(torch.from_numpy(wl.alpha))
-        rng = np.random.default_rng(4)
-        for it in range(5):
-            y_in = W.f32_to_bf16_bits(rng.standard_normal(wl.y.shape).astype(np.float32))
-            al.copy_(torch.from_numpy((wl.alpha * (1 + it)).astype(np.float32)))
-            y_host.copy_(torch.from_numpy(y_in.view(np.int16)))
-            tcl.lora_delta_apply_host(x_host, y_host, off, ids, al, wl.T, wl.P, dw.pool.handle, None,
-                                      dw.mapping.handle, s)
-            s.synchronize()
-            got = y_host.numpy().view(np.uint16).copy()
-            wl_it = dataclasses.replace(wl, alpha=(wl.alpha * (1 + it)).astype(np.float32), y=y_in)
-            yref, _, _ = oracle.apply_workload(wl_it, threads=0)
-            stated_gate(got, yref)
+        _host_calls(wl, dw, host(torch.from_numpy(wl.x.view(np.int16).copy())),
+                    host(torch.empty(wl.y.shape, dtype=torch.int16)), host(torch.from_numpy(wl.offsets)),
+                    host(torch.from_numpy(wl.ids)), host(torch.from_numpy(wl.alpha)), 5)
     finally:
+        dw.close()
+
+
+def test_host_entry_point_buffer_unpinned_between_calls():
+    """x is page-locked in place for the first calls (eager, captured with the
+    copy kernels, replayed), then unlocked at the same address: the next call
+    must see that the GPU no longer addresses it and run with copy calls."""
+    cudart = torch.cuda.cudart()
+    wl = W.distinct_decode()
+    dw = DeviceWorkload(wl)
+    x_host = torch.from_numpy(wl.x.view(np.int16).copy())
+    nbytes = x_host.numel() * x_host.element_size()
+    assert int(cudart.cudaHostRegister(x_host.data_ptr(), nbytes, 0)) == 0
+    state = {"registered": True}
+
+    def unpin_at_fourth(it):
+        if it == 3:
+            assert int(cudart.cudaHostUnregister(x_host.data_ptr())) == 0
+            state["registered"] = False
+
+    try:
+        _host_calls(wl, dw, x_host, torch.empty(wl.y.shape, dtype=torch.int16).pin_memory(),
+                    torch.from_numpy(wl.offsets).pin_memory(), torch.from_numpy(wl.ids).pin_memory(),
+                    torch.from_numpy(wl.alpha).pin_memory(), 6, before_call=unpin_at_fourth)
+    finally:
+        if state["registered"]:
+            cudart.cudaHostUnregister(x_host.data_ptr())
         dw.close()
 
 
