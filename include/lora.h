@@ -199,8 +199,8 @@ int lora_dispatch_choose(int T, int P, int r_max, int d_in, int d_out);
  * memory directly; otherwise one cudaMemcpyAsync per buffer.
  * A call that repeats the previous call's arguments exactly (pointers, T, P,
  * pool, ranks, stream) is captured into a CUDA graph of the whole step, and
- * later calls with those arguments replay it (one launch instead of nine
- * API calls); the buffers' contents may change between calls.  Every call
+ * later calls with those arguments replay it (one graph launch instead of
+ * five to nine API calls); the buffers' contents may change between calls.  Every call
  * looks up again whether each buffer is page-locked and at which device
  * address; a replay happens only when that is unchanged since the capture.
  * Calls on a default stream, or on a stream that is being captured, always
