@@ -23,7 +23,9 @@
 // round trips to memory as possible: a decode batch moves little data, and
 // its time is the chain of latencies.  The shrink is itself a programmatic
 // dependent of the mapping kernel (its CTAs are resident when the mapping
-// ends), and the expand lets the next kernel in the stream start early.
+// ends) and releases the expand only once its own wait has returned, since
+// the expand's prologue reads the mapping and y; the expand lets the next
+// kernel in the stream start early (that kernel waits before it writes).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -132,8 +134,14 @@ __device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *x
 __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a)
 {
     extern __shared__ __align__(16) uint4 xs[];  // the pair's x row
+    pdl_wait();  // launched as a programmatic dependent of the mapping (or of a previous apply)
+    // Only now may the expand launch: it reads the mapping (pair lists, the
+    // header) and y before its own wait on this kernel, so everything that
+    // precedes this kernel in the stream -- the mapping, and through the
+    // mapping's own wait every earlier kernel, a previous expand that wrote y
+    // included -- must have completed.  Its prologue still overlaps the work
+    // below.
     pdl_launch_dependents();
-    pdl_wait();  // launched as a programmatic dependent of the mapping
     dec_shrink_item(a, xs, blockIdx.x, blockIdx.y * (blockDim.x >> 5), blockIdx.y == 0);
 }
 

@@ -192,6 +192,68 @@ def test_prefill_full_size_sampled(path):
     assert np.isfinite(bf16_bits_to_f32(y)).all()
 
 
+# ---------------------------------------------------------------- stream ordering
+def _other_batch(wl, seed):
+    """The same pool and tokens with new pair lists: per token the same number
+    of pairs, distinct ids drawn afresh, new alpha."""
+    rng = np.random.default_rng(seed)
+    counts = np.diff(wl.offsets)
+    ids = np.concatenate([rng.choice(wl.capacity, size=int(c), replace=False) for c in counts]).astype(np.int32)
+    alpha = rng.random(ids.size).astype(np.float32)
+    return dataclasses.replace(wl, ids=ids, alpha=alpha)
+
+
+@pytest.mark.parametrize("name", ["zipf", "sweep8", "distinct"])
+def test_new_mapping_then_apply_without_a_break(name):
+    """Batch after batch on one stream, each apply straight after its mapping
+    (no other kernel, no synchronisation in between), as a decode loop runs:
+    every apply must see its own batch's mapping, not the previous one."""
+    import tenant_composite_lora_gb300 as tcl
+    wl = W.make(name, y_zero=True)
+    batches = [wl] + [_other_batch(wl, 100 + i) for i in range(3)]
+    dw = DeviceWorkload(wl, build=False)
+    s = torch.cuda.Stream()
+    try:
+        dev = [(torch.from_numpy(b.offsets).cuda(), torch.from_numpy(b.ids).cuda(),
+                torch.from_numpy(b.alpha).cuda()) for b in batches]
+        ys = [dw.y0.clone() for _ in batches]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for (off, ids, al), y in zip(dev, ys):
+                dw.mapping.build(off, ids, al, s)
+                tcl.delta_apply(dw.x, y, dw.pool, dw.mapping, path=PATH_DECODE, stream=s)
+        s.synchronize()
+        got = [bf16_to_numpy_bits(y) for y in ys]
+    finally:
+        dw.close()
+    for b, y in zip(batches, got):
+        _, acc, _ = oracle.apply_workload(b, threads=0)
+        delta_gate(y, acc)
+
+
+@pytest.mark.parametrize("name", ["zipf", "sweep8"])
+def test_two_applies_into_one_y_without_a_break(name):
+    """Two applies of one mapping into the same y back to back (y starts at
+    zero): the second must read the first one's result, so y ends at twice
+    the delta."""
+    import tenant_composite_lora_gb300 as tcl
+    wl = W.make(name, y_zero=True)
+    dw = DeviceWorkload(wl)
+    s = torch.cuda.Stream()
+    try:
+        y = dw.y0.clone()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                tcl.delta_apply(dw.x, y, dw.pool, dw.mapping, path=PATH_DECODE, stream=s)
+        s.synchronize()
+        got = bf16_to_numpy_bits(y)
+    finally:
+        dw.close()
+    _, acc, _ = oracle.apply_workload(wl, threads=0)
+    delta_gate(got, 2.0 * acc)
+
+
 # ---------------------------------------------------------------- contracts
 @pytest.mark.parametrize("path", ALL_PATHS)
 def test_garbage_padding_is_inert(path):
