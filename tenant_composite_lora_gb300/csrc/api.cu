@@ -215,6 +215,26 @@ cudaError_t dalloc(T **p, size_t count)
     return cudaMalloc(reinterpret_cast<void **>(p), (count > 0 ? count : 1) * sizeof(T));
 }
 
+// Frees the host entry point's device staging; the step graph (which copies
+// into it) goes first, and the recorded shape is cleared until a new staging
+// is complete.
+void free_staging(lora_mapping *m)
+{
+    if (m->exec) {
+        cudaGraphExecDestroy(m->exec);
+        m->exec = nullptr;
+    }
+    m->have_seen = false;
+    void *ptrs[] = {m->sx, m->sy, m->soff, m->sids, m->salpha};
+    for (void *p : ptrs)
+        if (p)
+            cudaFree(p);
+    m->sx = m->sy = nullptr;
+    m->soff = m->sids = nullptr;
+    m->salpha = nullptr;
+    m->s_d_in = m->s_d_out = 0;
+}
+
 void free_mapping(lora_mapping *m)
 {
     if (m->exec)
@@ -658,30 +678,20 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
         return LORA_ERR_INVALID_ARG;
     cudaError_t e = cudaSuccess;
     if (!m->sx || m->s_d_in != pool->d_in || m->s_d_out != pool->d_out) {
-        e = cudaDeviceSynchronize();
-        if (m->sx) cudaFree(m->sx);
-        if (m->sy) cudaFree(m->sy);
-        if (m->soff) cudaFree(m->soff);
-        if (m->sids) cudaFree(m->sids);
-        if (m->salpha) cudaFree(m->salpha);
-        m->sx = m->sy = nullptr;
-        m->soff = m->sids = nullptr;
-        m->salpha = nullptr;
+        e = cudaDeviceSynchronize();  // earlier steps may still use the old staging
+        free_staging(m);
         const size_t mt = (size_t)(m->max_tokens > 0 ? m->max_tokens : 1);
         if (e == cudaSuccess) e = cudaMalloc(&m->sx, mt * pool->d_in * sizeof(__nv_bfloat16));
         if (e == cudaSuccess) e = cudaMalloc(&m->sy, mt * pool->d_out * sizeof(__nv_bfloat16));
         if (e == cudaSuccess) e = dalloc(&m->soff, mt + 1);
         if (e == cudaSuccess) e = dalloc(&m->sids, (size_t)m->max_pairs);
         if (e == cudaSuccess) e = dalloc(&m->salpha, (size_t)m->max_pairs);
-        if (e != cudaSuccess)
+        if (e != cudaSuccess) {
+            free_staging(m);  // nothing half-built is kept
             return from_cuda(e);
+        }
         m->s_d_in = pool->d_in;
         m->s_d_out = pool->d_out;
-        if (m->exec) {  // it copies into the old staging
-            cudaGraphExecDestroy(m->exec);
-            m->exec = nullptr;
-        }
-        m->have_seen = false;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const HostStepKey key{x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, stream};
