@@ -108,13 +108,53 @@ def _check(fn: str, s: int):
         raise LoraError(fn, s)
 
 
-def _ptr(t) -> int | None:
-    if t is None:
-        return None
-    if isinstance(t, int):
+_BF16_LIKE = 2  # bytes per element of x, y, A, B (bf16, or its bits as int16)
+
+
+def _dtype_ok(t, kind: str) -> bool:
+    if kind == "bf16":
+        return t.itemsize == _BF16_LIKE if isinstance(t, np.ndarray) else t.element_size() == _BF16_LIKE
+    if isinstance(t, np.ndarray):
+        return t.dtype == np.dtype(kind)
+    import torch
+    return t.dtype == {"int32": torch.int32, "float32": torch.float32}[kind]
+
+
+def _dptr(t, name: str, kind: str) -> int | None:
+    """Address of a device array: a contiguous CUDA tensor of the expected
+    element type, or a raw integer address (the caller's responsibility).
+    Host memory is refused here: a kernel must never be handed a host
+    address."""
+    if t is None or isinstance(t, int):
         return t
     if isinstance(t, np.ndarray):
+        raise ValueError(f"{name}: a device array is expected, not a numpy (host) array")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: a CUDA tensor is expected, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: the tensor must be contiguous")
+    if not _dtype_ok(t, kind):
+        raise ValueError(f"{name}: {kind} elements expected, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _hptr(t, name: str, kind: str) -> int | None:
+    """Address of a host array: a contiguous CPU tensor or C-ordered numpy
+    array of the expected element type, or a raw integer address."""
+    if t is None or isinstance(t, int):
+        return t
+    if isinstance(t, np.ndarray):
+        if not t.flags.c_contiguous:
+            raise ValueError(f"{name}: the array must be C-contiguous")
+        if not _dtype_ok(t, kind):
+            raise ValueError(f"{name}: {kind} elements expected, got {t.dtype}")
         return t.ctypes.data
+    if t.is_cuda:
+        raise ValueError(f"{name}: a host tensor is expected, got a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: the tensor must be contiguous")
+    if not _dtype_ok(t, kind):
+        raise ValueError(f"{name}: {kind} elements expected, got {t.dtype}")
     return t.data_ptr()
 
 
@@ -135,7 +175,8 @@ def lora_pool_create(d_in: int, d_out: int, r_max: int, capacity: int) -> int:
 
 
 def lora_pool_register(pool: int, slot: int, A, B, k: int, stream=None):
-    _check("lora_pool_register", load().lora_pool_register(pool, slot, _ptr(A), _ptr(B), k, _stream(stream)))
+    _check("lora_pool_register", load().lora_pool_register(pool, slot, _dptr(A, "A", "bf16"), _dptr(B, "B", "bf16"), k,
+                                                     _stream(stream)))
 
 
 def lora_pool_unregister(pool: int, slot: int, stream=None):
@@ -156,17 +197,20 @@ def lora_mapping_create(max_tokens: int, max_pairs: int, capacity: int) -> int:
 
 def lora_build_mapping(m: int, offsets, ids, alpha, T: int, P: int, stream=None):
     _check("lora_build_mapping",
-           load().lora_build_mapping(m, _ptr(offsets), _ptr(ids), _ptr(alpha), T, P, _stream(stream)))
+           load().lora_build_mapping(m, _dptr(offsets, "offsets", "int32"), _dptr(ids, "ids", "int32"),
+                                     _dptr(alpha, "alpha", "float32"), T, P, _stream(stream)))
 
 
 def lora_delta_apply(x, y, pool: int, ranks, m: int, stream=None):
     _check("lora_delta_apply",
-           load().lora_delta_apply(_ptr(x), _ptr(y), pool, _ptr(ranks), m, _stream(stream)))
+           load().lora_delta_apply(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool,
+                                   _dptr(ranks, "ranks", "int32"), m, _stream(stream)))
 
 
 def lora_delta_apply_path(x, y, pool: int, ranks, m: int, path: int, stream=None):
     _check("lora_delta_apply_path",
-           load().lora_delta_apply_path(_ptr(x), _ptr(y), pool, _ptr(ranks), m, path, _stream(stream)))
+           load().lora_delta_apply_path(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool,
+                                        _dptr(ranks, "ranks", "int32"), m, path, _stream(stream)))
 
 
 def lora_dispatch_choose(T: int, P: int, r_max: int, d_in: int, d_out: int) -> int:
@@ -176,15 +220,20 @@ def lora_dispatch_choose(T: int, P: int, r_max: int, d_in: int, d_out: int) -> i
 def lora_delta_apply_host(x_host, y_host, offsets_host, ids_host, alpha_host, T: int, P: int,
                           pool: int, ranks, m: int, stream=None):
     _check("lora_delta_apply_host",
-           load().lora_delta_apply_host(_ptr(x_host), _ptr(y_host), _ptr(offsets_host), _ptr(ids_host),
-                                        _ptr(alpha_host), T, P, pool, _ptr(ranks), m, _stream(stream)))
+           load().lora_delta_apply_host(_hptr(x_host, "x_host", "bf16"), _hptr(y_host, "y_host", "bf16"),
+                                        _hptr(offsets_host, "offsets_host", "int32"),
+                                        _hptr(ids_host, "ids_host", "int32"),
+                                        _hptr(alpha_host, "alpha_host", "float32"), T, P, pool,
+                                        _dptr(ranks, "ranks", "int32"), m, _stream(stream)))
 
 
 def lora_delta_apply_noalloc(x, y, pool: int, ranks, offsets, ids, alpha, T: int, P: int,
                              status=None, stream=None):
     _check("lora_delta_apply_noalloc",
-           load().lora_delta_apply_noalloc(_ptr(x), _ptr(y), pool, _ptr(ranks), _ptr(offsets), _ptr(ids),
-                                           _ptr(alpha), T, P, _ptr(status), _stream(stream)))
+           load().lora_delta_apply_noalloc(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool,
+                                           _dptr(ranks, "ranks", "int32"), _dptr(offsets, "offsets", "int32"),
+                                           _dptr(ids, "ids", "int32"), _dptr(alpha, "alpha", "float32"), T, P,
+                                           _dptr(status, "status", "int32"), _stream(stream)))
 
 
 def lora_mapping_status(m: int, stream=None) -> int:

@@ -91,3 +91,78 @@ def test_product_never_touches_the_oracle():
         if f.endswith((".py", ".c")):
             src = open(os.path.join(ROOT, "oracle", f)).read()
             assert "tenant_composite_lora_gb300" not in src
+
+
+def test_binding_refuses_wrong_memory_and_layouts():
+    """The binding hands kernels only what they can read: host memory, a
+    non-contiguous view or a wrong element type is refused before the
+    library is called (no GPU involved: the checks come first)."""
+    import numpy as np
+    import torch
+    from tenant_composite_lora_gb300 import native
+
+    fake = 1  # never dereferenced: every call below raises before the library
+    off = torch.zeros(5, dtype=torch.int32)
+    ids = torch.zeros(4, dtype=torch.int32)
+    alpha = torch.zeros(4, dtype=torch.float32)
+    x = torch.zeros(4, 64, dtype=torch.bfloat16)
+    # device entry points: host tensors and numpy arrays are refused
+    with pytest.raises(ValueError, match="offsets: a CUDA tensor is expected"):
+        native.lora_build_mapping(fake, off, ids, alpha, 4, 4, 0)
+    with pytest.raises(ValueError, match="x: a device array is expected"):
+        native.lora_delta_apply(np.zeros((4, 64), np.int16), 0, fake, None, fake, 0)
+    with pytest.raises(ValueError, match="A: a CUDA tensor is expected"):
+        native.lora_pool_register(fake, 0, x, x, 1, 0)
+    with pytest.raises(ValueError, match="x: a CUDA tensor is expected"):
+        native.lora_delta_apply_noalloc(x, 0, fake, None, 0, 0, 0, 4, 4, stream=0)
+    # host entry point: layouts and element types
+    y = torch.zeros(4, 64, dtype=torch.int16)
+    with pytest.raises(ValueError, match="x_host: the tensor must be contiguous"):
+        native.lora_delta_apply_host(torch.zeros(64, 4, dtype=torch.int16).t(), y, off, ids, alpha, 4, 4,
+                                     fake, None, fake, 0)
+    with pytest.raises(ValueError, match="ids_host: int32 elements expected"):
+        native.lora_delta_apply_host(x, y, off, ids.long(), alpha, 4, 4, fake, None, fake, 0)
+    with pytest.raises(ValueError, match="alpha_host: float32 elements expected"):
+        native.lora_delta_apply_host(x, y, off, ids, alpha.double(), 4, 4, fake, None, fake, 0)
+    with pytest.raises(ValueError, match="y_host: bf16 elements expected"):
+        native.lora_delta_apply_host(x, y.float(), off, ids, alpha, 4, 4, fake, None, fake, 0)
+    with pytest.raises(ValueError, match="offsets_host: the array must be C-contiguous"):
+        native.lora_delta_apply_host(x, y, np.zeros((5, 2), np.int32)[:, 0], ids, alpha, 4, 4, fake, None,
+                                     fake, 0)
+
+
+def test_binding_accepts_what_the_library_takes():
+    """The argument kinds the tests, the benchmark and the smoke run pass
+    (bf16 or int16 x / y, int32 offsets / ids / ranks / status, float32
+    alpha, contiguous) go through as their data pointers."""
+    import numpy as np
+    import torch
+    from tenant_composite_lora_gb300 import native
+
+    class OnDevice:  # a contiguous tensor as a CUDA tensor would present itself
+        def __init__(self, t):
+            self.t = t
+            self.is_cuda = True
+            self.dtype = t.dtype
+            self.device = "cuda:0"
+
+        def is_contiguous(self):
+            return self.t.is_contiguous()
+
+        def element_size(self):
+            return self.t.element_size()
+
+        def data_ptr(self):
+            return self.t.data_ptr()
+
+    for t, kind in ((torch.zeros(4, 64, dtype=torch.bfloat16), "bf16"),
+                    (torch.zeros(4, 64, dtype=torch.int16), "bf16"),
+                    (torch.zeros(5, dtype=torch.int32), "int32"),
+                    (torch.zeros(5, dtype=torch.float32), "float32")):
+        assert native._dptr(OnDevice(t), "arg", kind) == t.data_ptr()
+        assert native._hptr(t, "arg", kind) == t.data_ptr()
+    a = np.zeros(5, np.int32)
+    assert native._hptr(a, "arg", "int32") == a.ctypes.data
+    assert native._dptr(None, "arg", "int32") is None and native._dptr(1234, "arg", "int32") == 1234
+    with pytest.raises(ValueError, match="int32 elements expected"):
+        native._dptr(OnDevice(torch.zeros(5, dtype=torch.int64)), "arg", "int32")
