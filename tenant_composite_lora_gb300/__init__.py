@@ -64,7 +64,11 @@ class LoraMapping:
 
     def build(self, offsets, ids, alpha, stream=None):
         """offsets int32 [T+1], ids int32 [P], alpha float32 [P]: CUDA tensors."""
+        if offsets.dim() != 1 or ids.dim() != 1 or alpha.dim() != 1 or offsets.shape[0] < 1:
+            raise ValueError("build: offsets, ids and alpha are 1-D, offsets of length T + 1 >= 1")
         T, P = offsets.shape[0] - 1, ids.shape[0]
+        if alpha.shape[0] != P:
+            raise ValueError(f"build: alpha has {alpha.shape[0]} entries for {P} ids")
         lora_build_mapping(self.handle, offsets, ids, alpha, T, P, stream)
         self.T, self.P = T, P
 
@@ -87,6 +91,14 @@ class LoraMapping:
 
 
 def delta_apply(x, y, pool: LoraPool, mapping: LoraMapping, ranks=None, path: int = 0, stream=None):
-    """In place: y += composite delta (bf16 CUDA tensors [T, d_in], [T, d_out])."""
+    """In place: y += composite delta (bf16 CUDA tensors [T, d_in], [T, d_out],
+    T of the mapping's last build; ranks: None or int32 [capacity])."""
+    T = mapping.T
+    if x.dim() != 2 or x.shape[0] < T or x.shape[1] != pool.d_in:
+        raise ValueError(f"delta_apply: x must be [>= {T}, {pool.d_in}], got {tuple(x.shape)}")
+    if y.dim() != 2 or y.shape[0] < T or y.shape[1] != pool.d_out:
+        raise ValueError(f"delta_apply: y must be [>= {T}, {pool.d_out}], got {tuple(y.shape)}")
+    if ranks is not None and ranks.numel() < pool.capacity:
+        raise ValueError(f"delta_apply: ranks must hold {pool.capacity} entries, got {ranks.numel()}")
     lora_delta_apply_path(x, y, pool.handle, ranks, mapping.handle, path, stream)
     return y

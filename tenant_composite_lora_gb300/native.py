@@ -1,8 +1,11 @@
 """ctypes binding of libtclora.so: the C-ABI entry points under the same names.
 
-Argument marshalling only.  Device arrays are passed as torch CUDA tensors
-(their data_ptr) or raw integer addresses; streams as torch.cuda.Stream, a raw
-cudaStream_t integer, or None for the current torch stream.  Every step of the
+Argument marshalling only.  Device arrays are passed as contiguous torch CUDA
+tensors (their data_ptr) or raw integer addresses, host arrays as contiguous
+CPU tensors or numpy arrays; a tensor in the wrong memory, not contiguous or
+of the wrong element type is refused before the library is called.  Streams
+are torch.cuda.Stream, a raw cudaStream_t integer, or None for the current
+torch stream.  Every step of the
 delta runs inside the library's CUDA kernels; nothing here computes.
 """
 from __future__ import annotations

@@ -166,3 +166,37 @@ def test_binding_accepts_what_the_library_takes():
     assert native._dptr(None, "arg", "int32") is None and native._dptr(1234, "arg", "int32") == 1234
     with pytest.raises(ValueError, match="int32 elements expected"):
         native._dptr(OnDevice(torch.zeros(5, dtype=torch.int64)), "arg", "int32")
+
+
+def test_wrappers_check_shapes_before_the_library():
+    """delta_apply and LoraMapping.build refuse shapes the kernels would read
+    past (x / y rows and widths, alpha's length), before any library call."""
+    import torch
+    import tenant_composite_lora_gb300 as tcl
+
+    class Pool:
+        d_in, d_out, capacity, handle = 64, 128, 8, 1
+
+    class Mapping(tcl.LoraMapping):
+        def __init__(self, T):  # no library object: the checks come first
+            self.T, self.P, self.handle = T, 0, 1
+
+        def close(self):  # nothing to destroy
+            self.handle = None
+
+    m = Mapping(4)
+    bf = torch.bfloat16
+    with pytest.raises(ValueError, match="x must be"):
+        tcl.delta_apply(torch.zeros(3, 64, dtype=bf), torch.zeros(4, 128, dtype=bf), Pool, m)
+    with pytest.raises(ValueError, match="x must be"):
+        tcl.delta_apply(torch.zeros(4, 32, dtype=bf), torch.zeros(4, 128, dtype=bf), Pool, m)
+    with pytest.raises(ValueError, match="y must be"):
+        tcl.delta_apply(torch.zeros(4, 64, dtype=bf), torch.zeros(4, 64, dtype=bf), Pool, m)
+    with pytest.raises(ValueError, match="ranks must hold 8"):
+        tcl.delta_apply(torch.zeros(4, 64, dtype=bf), torch.zeros(4, 128, dtype=bf), Pool, m,
+                        ranks=torch.zeros(7, dtype=torch.int32))
+    off = torch.zeros(5, dtype=torch.int32)
+    with pytest.raises(ValueError, match="alpha has 3 entries for 4 ids"):
+        m.build(off, torch.zeros(4, dtype=torch.int32), torch.zeros(3))
+    with pytest.raises(ValueError, match="1-D"):
+        m.build(off.view(5, 1), torch.zeros(4, dtype=torch.int32), torch.zeros(4))
