@@ -51,3 +51,12 @@ def test_traffic_files_parse(tmp_path, monkeypatch):
     assert bench.ncu_traffic("demo", "decode") == 1234
     assert bench.ncu_traffic("stale", "decode") is None  # taken with other kernel code
     assert bench.ncu_traffic("absent", "decode") is None
+
+
+def test_cpu_baseline_reports_threads_model_and_single_thread():
+    import workloads as W
+    cb = bench.oracle_baseline(W.make("tiny"), 0.5)
+    assert cb["kind"] == "oracle" and cb["unit"] == "tokens/s" and cb["value"] > 0
+    assert cb["cores"] >= 1 and cb["nproc"] >= 1 and isinstance(cb["cpu_model"], str) and cb["cpu_model"]
+    st = cb["single_thread"]
+    assert st["unit"] == "tokens/s" and st["value"] > 0 and "one thread" in st["sample"]
