@@ -261,6 +261,25 @@ def max_over_ranks(x, dist, device=None):
     return float(t.item())
 
 
+def pass_times_ms(replay, passes: int, stream, event_cls) -> list:
+    """Device time of each of `passes` consecutive replays, from events
+    recorded on the stream between them (one event per boundary)."""
+    evs = [event_cls(enable_timing=True) for _ in range(passes + 1)]
+    evs[0].record(stream)
+    for i in range(passes):
+        replay()
+        evs[i + 1].record(stream)
+    evs[-1].synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(passes)]
+
+
+def spread(values_us: list) -> dict:
+    """Median, p10 and p90 of per-step times (microseconds)."""
+    v = np.asarray(values_us, np.float64)
+    return {"p10": round(float(np.percentile(v, 10)), 3), "median": round(float(np.median(v)), 3),
+            "p90": round(float(np.percentile(v, 90)), 3), "samples": int(v.size)}
+
+
 def bench_ours(args, rank, world, dist):
     import torch
     import tenant_composite_lora_gb300 as tcl
@@ -354,6 +373,16 @@ def bench_ours(args, rank, world, dist):
         ms_per_step = ms_step_total / steps_done
         ms_apply = timed(g_apply, passes) / steps_done
 
+        # spread of the step time: each pass (R steps, one per replica) timed on
+        # its own, after the contract's timed region; reported per step
+        try:
+            n_pass = min(max(passes, 20), 200)
+            spread_step = spread([ms * 1e3 / R for ms in pass_times_ms(g_step.replay, n_pass, stream,
+                                                                        torch.cuda.Event)])
+            spread_step["steps_per_sample"] = R
+        except Exception as exc:  # an auxiliary figure never costs the line itself
+            spread_step = {"error": f"{type(exc).__name__}: {exc}"}
+
         # end to end through the host entry point (pinned buffers, copies timed)
         x_h = torch.from_numpy(wl.x.view(np.int16).copy()).pin_memory()
         y_h = torch.from_numpy(wl.y.view(np.int16).copy()).pin_memory()
@@ -422,6 +451,7 @@ def bench_ours(args, rank, world, dist):
                 "api": "lora_delta_apply_host"},
         "gpu_launches": (1 + n_apply_kernels) * steps_done,
         "clocks": clocks,
+        "step_us_spread": spread_step,
     }
     return line, wl
 

@@ -60,3 +60,34 @@ def test_cpu_baseline_reports_threads_model_and_single_thread():
     assert cb["cores"] >= 1 and cb["nproc"] >= 1 and isinstance(cb["cpu_model"], str) and cb["cpu_model"]
     st = cb["single_thread"]
     assert st["unit"] == "tokens/s" and st["value"] > 0 and "one thread" in st["sample"]
+
+
+def test_pass_times_and_spread():
+    """Per-pass event timing and its percentiles, with events that tick a
+    fake device clock on every replay."""
+    clock = {"t": 0.0}
+    durations = iter([2.0, 4.0, 3.0, 1.0, 5.0])
+
+    class Event:
+        def __init__(self, enable_timing=False):
+            assert enable_timing
+            self.t = None
+
+        def record(self, stream):
+            assert stream == "s"
+            self.t = clock["t"]
+
+        def synchronize(self):
+            assert self.t is not None
+
+        def elapsed_time(self, other):
+            return other.t - self.t
+
+    def replay():
+        clock["t"] += next(durations)
+
+    ms = bench.pass_times_ms(replay, 5, "s", Event)
+    assert ms == [2.0, 4.0, 3.0, 1.0, 5.0]
+    sp = bench.spread([m * 1e3 / 4 for m in ms])  # 4 steps per pass, microseconds
+    assert sp["median"] == 750.0 and sp["samples"] == 5
+    assert sp["p10"] == 350.0 and sp["p90"] == 1150.0
