@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(EXP_THREADS, 2) k_expand(ExpandArgs a)
 template <int CPT>
 cudaError_t launch_cpt(const ExpandArgs &a, dim3 grid, size_t smem, bool pdl, cudaStream_t st)
 {
-    static int attr_done = -1;
+    static thread_local int attr_done = -1;  // per host thread
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {

@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(EXP_THREADS, 1) k_fused(FusedArgs a)
 template <int CPT>
 int fused_dynamic_limit()
 {
-    static int cached = -1, cached_dev = -1;
+    static thread_local int cached = -1, cached_dev = -1;  // per host thread
     int dev = 0;
     cudaGetDevice(&dev);
     if (cached_dev != dev) {
@@ -216,7 +216,7 @@ cudaError_t launch_fused_cpt(FusedArgs a, int grid, size_t exp_bytes, cudaStream
         return cudaErrorNotSupported;
     a.s.ring_bytes = ring;
     a.s.entry_bytes = ring / 2;
-    static int attr_done = -1;
+    static thread_local int attr_done = -1;  // per host thread
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {

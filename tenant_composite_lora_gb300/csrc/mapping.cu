@@ -372,7 +372,7 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
         staged && P >= 2048 && staged_words + (long long)(nw + 2) * capacity + 2LL * P <= budget;
     const size_t smem = 4 * ((staged ? (size_t)staged_words : 0) + (size_t)(nw + 2) * capacity +
                              (sorted_smem ? 2 * (size_t)P : 0));
-    static int attr_done = -1;
+    static thread_local int attr_done = -1;  // per host thread
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {

@@ -849,17 +849,17 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 EncodeTiledFn encode_fn()
 {
-    static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    // looked up once per process (a function-local static is initialised
+    // exactly once, whatever the number of threads calling)
+    static const EncodeTiledFn fn = [] {
         void *p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 
@@ -917,7 +917,7 @@ cudaError_t launch_expand_bn(__nv_bfloat16 *y, const PoolDev &pool, const CUtens
                              const MapDev &m, int T, cudaStream_t st)
 {
     const MeLayout L(pool.capacity);
-    static int attr_dev = -1;
+    static thread_local int attr_dev = -1;  // per host thread
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_dev != dev) {
@@ -978,7 +978,7 @@ cudaError_t launch_mma(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &
     const int ck = shrink_cluster(pool.d_in);
     const int tiles = mma_tile_bound(P, pool.capacity);
     if (tiles > 0) {
-        static int attr_dev = -1;
+        static thread_local int attr_dev = -1;  // per host thread
         int dev = 0;
         cudaGetDevice(&dev);
         if (attr_dev != dev) {

@@ -32,7 +32,7 @@ cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int
 {
     const int use_tab = pool.capacity <= RANK_TAB_MAX ? 1 : 0;
     const size_t smem = (size_t)SHRINK_RING_BYTES + (use_tab ? (size_t)((pool.capacity + 3) & ~3) * sizeof(int) : 0);
-    static int attr_done = -1;
+    static thread_local int attr_done = -1;  // per host thread
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_done != dev) {
