@@ -279,6 +279,25 @@ lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, const lora_
                                      const int32_t *ids_dev, const float *alpha_dev, int T, int P,
                                      int32_t *status_dev, lora_stream_t stream);
 
+/*
+ * lora_diag_wait_expiry: diagnostic.  Every on-chip wait of the library is
+ * bounded; this launches one kernel whose single wait can never be
+ * satisfied, so that the expiry path can be observed: the wait gives up
+ * after limit_ns, sets LORA_DEV_TIMEOUT and the kernel returns normally,
+ * leaving the context usable.  (The pages have no counterpart: bounded
+ * waits are this library's rule for any wait between CTAs.)
+ *   kind      : 0 = an mbarrier phase with no arrival (the wait of the TMA
+ *               pipelines), 1 = a counter in global memory that nothing
+ *               increments (the wait of the cooperative kernels)
+ *   limit_ns  : 1e3 .. 1e8 (1 us .. 100 ms)
+ *   words_dev : device int32 [4]; words[1] must hold 0 for kind 1.  On
+ *               return (stream-ordered): words[0] |= LORA_DEV_TIMEOUT,
+ *               words[2] = 1 if the wait was satisfied else 0, words[3] =
+ *               microseconds waited.
+ * Returns LORA_ERR_INVALID_ARG for other kinds or limits.
+ */
+lora_status lora_diag_wait_expiry(int kind, long long limit_ns, int32_t *words_dev, lora_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,12 +1,17 @@
 // The C ABI declared in include/lora.h: objects, argument checks, dispatch.
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 
 struct lora_pool {
     int d_in, d_out, r_max, capacity, device;
+    // unique over the process lifetime: a pool created where a destroyed one
+    // lived (same host address) is still a different pool
+    unsigned long long serial;
     __nv_bfloat16 *At;  // [capacity][r_max][d_in]
     __nv_bfloat16 *B;   // [capacity][r_max][d_out]
     int32_t *reg_rank;  // [capacity]
@@ -14,19 +19,22 @@ struct lora_pool {
 };
 
 // The arguments of a lora_delta_apply_host call: a repeat of the same ones
-// replays a captured graph of the whole step.
+// replays a captured graph of the whole step.  The pool enters by its serial
+// number, not its address: a graph captured against a destroyed pool holds
+// that pool's device pointers and must never replay for a new pool that
+// happens to occupy the same host memory.
 struct HostStepKey {
     const void *x, *y;
     const int32_t *off, *ids;
     const float *alpha;
     int T, P;
-    const lora_pool *pool;
+    unsigned long long pool_serial;
     const int32_t *ranks;
     void *stream;
     bool operator==(const HostStepKey &o) const
     {
         return x == o.x && y == o.y && off == o.off && ids == o.ids && alpha == o.alpha && T == o.T && P == o.P &&
-               pool == o.pool && ranks == o.ranks && stream == o.stream;
+               pool_serial == o.pool_serial && ranks == o.ranks && stream == o.stream;
     }
 };
 
@@ -134,8 +142,14 @@ __global__ void __launch_bounds__(256) k_copy_set(const CopySet c)
     }
 }
 
-int g_sm_count = 0;
-int g_sm_dev = -1;
+// SM count of the current device, cached per host thread (device and count
+// together, so a thread never pairs one device with another's count).
+struct SmCache {
+    int dev = -1, count = 0;
+};
+thread_local SmCache t_sm;
+
+std::atomic<unsigned long long> g_pool_serial{0};
 
 }  // namespace
 
@@ -172,11 +186,14 @@ int sm_count()
 {
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev != g_sm_dev) {
-        cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev);
-        g_sm_dev = dev;
+    if (dev != t_sm.dev) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return 1;  // not cached: asked again on the next call
+        t_sm.count = n;
+        t_sm.dev = dev;
     }
-    return g_sm_count > 0 ? g_sm_count : 1;
+    return t_sm.count;
 }
 
 }  // namespace tcl
@@ -242,7 +259,7 @@ void free_mapping(lora_mapping *m)
     MapDev &d = m->dev;
     void *ptrs[] = {d.tok,  d.adapter, d.src, d.pos,     d.alpha, d.seg_adapter, d.seg_start,
                     d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.pq, d.zcnt, d.z,
-                    d.partial, m->sx, m->sy, m->soff, m->sids, m->salpha};
+                    d.partial, d.ghist, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -405,6 +422,7 @@ lora_status lora_pool_create(int d_in, int d_out, int r_max, int capacity, lora_
     p->d_out = d_out;
     p->r_max = r_max;
     p->capacity = capacity;
+    p->serial = ++g_pool_serial;
     cudaGetDevice(&p->device);
     const size_t na = (size_t)capacity * r_max * d_in, nb = (size_t)capacity * r_max * d_out;
     cudaError_t e = dalloc(&p->At, na);
@@ -510,6 +528,8 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.z, P * LORA_MAX_RANK);
     d.partial_ctas = sm_count();
     if (e == cudaSuccess) e = dalloc(&d.partial, (size_t)d.partial_ctas * EXP_TILE_ELEMS);
+    if (e == cudaSuccess && map_global_hist_words(capacity) > 0)
+        e = dalloc(&d.ghist, (size_t)map_global_hist_words(capacity));
     if (e == cudaSuccess) e = cudaMemset(d.hdr, 0, HDR_WORDS * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(d.seg_start, 0, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -694,7 +714,7 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
         m->s_d_out = pool->d_out;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const HostStepKey key{x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, stream};
+    const HostStepKey key{x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool->serial, ranks_dev, stream};
     // where the GPU can address each buffer, looked up on every call: the
     // graph replays only while that is what it was captured with (a buffer
     // freed and another one allocated at its address, pinned or not, is
@@ -811,11 +831,11 @@ lora_status lora_mapping_destroy(lora_mapping *m)
 namespace {
 
 // The fixed scratch of lora_delta_apply_noalloc (one per device).
-__device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
+static __device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
 
 struct NoallocLayout {
     size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, pq, zcnt,
-        z;
+        z, ghist;
     size_t total;
 };
 
@@ -847,18 +867,23 @@ NoallocLayout noalloc_layout(int T, int P, int capacity, int r_max)
     L.pq = take(8 * p);
     L.zcnt = take(4 * p);
     L.z = take(4 * p * (size_t)z_stride(r_max));
+    L.ghist = take(4 * (size_t)map_global_hist_words(capacity));
     L.total = off;
     return L;
 }
 
-// Device address of the scratch on the current device (looked up once per device).
+// Device address of the scratch on the current device, looked up once per
+// device (under a lock: concurrent first calls from several host threads
+// see either no entry or the finished one).
 unsigned char *noalloc_base()
 {
     constexpr int MAX_DEVICES = 64;
     static unsigned char *base[MAX_DEVICES] = {};
+    static std::mutex lock;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES)
         return nullptr;
+    std::lock_guard<std::mutex> g(lock);
     if (!base[dev]) {
         unsigned char *ptr = nullptr;
         if (cudaGetSymbolAddress((void **)&ptr, g_noalloc_scratch) != cudaSuccess)
@@ -906,6 +931,7 @@ extern "C" lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, 
     d.pq = reinterpret_cast<int2 *>(base + L.pq);
     d.zcnt = reinterpret_cast<int32_t *>(base + L.zcnt);
     d.z = reinterpret_cast<float *>(base + L.z);
+    d.ghist = map_global_hist_words(pool->capacity) > 0 ? reinterpret_cast<int32_t *>(base + L.ghist) : nullptr;
     d.partial = nullptr;  // used by the fused kernel only
     d.partial_ctas = 0;
 

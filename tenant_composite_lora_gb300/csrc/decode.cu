@@ -403,30 +403,10 @@ struct DecFusedArgs {
     int ng;  // shrink items per pair: rank rows in groups of 8
 };
 
-__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p)
-{
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // Waits until *cnt >= target, for at most WAIT_LIMIT_NS (then LORA_DEV_TIMEOUT).
 __device__ __forceinline__ bool wait_count(const int32_t *cnt, int target, int32_t *status)
 {
-    if (ld_acquire_gpu(cnt) >= target)
-        return true;
-    const uint64_t t0 = global_timer_ns();
-    for (;;) {
-        for (int i = 0; i < 16; ++i) {
-            if (ld_acquire_gpu(cnt) >= target)
-                return true;
-            __nanosleep(32);
-        }
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
-            atomicOr(status, LORA_DEV_TIMEOUT);
-            return false;
-        }
-    }
+    return wait_count_bounded(cnt, (unsigned)target, status);
 }
 
 // A cooperative launch, every CTA resident: each CTA first runs shrink items

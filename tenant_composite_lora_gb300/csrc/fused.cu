@@ -36,13 +36,6 @@ struct FusedArgs {
     float *partial;  // [n_exp][tb][w] fp32 tiles when ng > 1
 };
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
 // All CTAs of the (cooperative, fully resident) grid arrive; returns when the
 // counter reaches `target` or after WAIT_LIMIT_NS (then sets LORA_DEV_TIMEOUT
 // and returns false).  Uniform across the CTA.
@@ -53,15 +46,7 @@ __device__ bool grid_barrier(unsigned *count, unsigned target, int32_t *status)
     if (threadIdx.x == 0) {
         __threadfence();
         atomicAdd(count, 1u);
-        const uint64_t t0 = global_timer_ns();
-        while ((int)(ld_acquire_u32(count) - target) < 0) {
-            if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
-                atomicOr(status, LORA_DEV_TIMEOUT);
-                ok = 0;
-                break;
-            }
-            __nanosleep(32);
-        }
+        ok = wait_count_bounded(count, target, status);
         __threadfence();
     }
     return __syncthreads_and(ok) != 0;

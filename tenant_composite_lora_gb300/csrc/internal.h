@@ -35,6 +35,12 @@ struct ExpandPlan {
 
 constexpr int MAP_THREADS = 1024;
 constexpr int MAP_SMEM_BYTES = 200 * 1024;
+// Pools whose per-warp histograms do not fit in shared memory (one warp's
+// row plus two per-bin arrays above MAP_SMEM_BYTES) keep them in global
+// memory, MAP_GHIST_WARPS rows of `capacity` words plus the two per-bin arrays.
+constexpr int MAP_GHIST_WARPS = 8;
+// Words of global histogram scratch a mapping over `capacity` ids needs (0: none).
+int map_global_hist_words(int capacity);
 
 // Ranks of pools up to this capacity are staged in shared memory by the
 // apply kernels (one coalesced read instead of a dependent lookup).
@@ -81,6 +87,8 @@ struct MapDev {
     float *z;                            // [max_pairs][LORA_MAX_RANK] shrink output
     float *partial;                      // [partial_ctas][EXP_TILE_ELEMS] fused-kernel tiles
     int partial_ctas;
+    int32_t *ghist;                      // [map_global_hist_words(capacity)] or null: mapping
+                                         // histograms of pools too large for shared memory
 };
 
 // Launchers (each returns cudaGetLastError()).

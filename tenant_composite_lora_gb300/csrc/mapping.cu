@@ -92,6 +92,7 @@ struct MapArgs {
     MapDev m;
     const int32_t *off, *ids;
     const float *alpha;
+    int32_t *hist_g;  // histograms and per-bin arrays in global memory (null: shared memory)
     int T, P, cap, nw, staged, tile_bound, mtile_bound;
     int sorted_smem;  // the scatter lands in shared memory, the sorted arrays are written coalesced after
 };
@@ -149,15 +150,19 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         ids = a.ids;
         alb = reinterpret_cast<const int32_t *>(a.alpha);
         tok = m.tmp_tok;
-        hist = sh;
+        hist = a.hist_g ? a.hist_g : sh;
     }
     // per bin: first sorted position and first shrink tile of its segment
     int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
     // sorted token and source pair per position (with sorted_smem)
     int32_t *s_stok = bin_tile + cap, *s_ssrc = s_stok + P;
-    for (int i = tid; i < nw * cap; i += nthr)
-        hist[i] = 0;
+    if (!a.hist_g)
+        for (int i = tid; i < nw * cap; i += nthr)
+            hist[i] = 0;
     pdl_wait();  // the previous kernel (which may still read this mapping) is done
+    if (a.hist_g)  // global scratch of this mapping: written only after the wait
+        for (int i = tid; i < nw * cap; i += nthr)
+            hist[i] = 0;
     if (tid == 0) {
         m.hdr[HDR_STATUS] = 0;
         m.hdr[HDR_BAR] = 0;  // fused-kernel counters start over with every mapping
@@ -340,6 +345,15 @@ int mma_tile_bound(int P, int capacity)
     return (int)(b < P ? b : P);
 }
 
+int map_global_hist_words(int capacity)
+{
+    // shared memory holds one warp's histogram and the two per-bin arrays
+    // (unstaged inputs) up to this capacity
+    if (3LL * capacity <= MAP_SMEM_BYTES / 4)
+        return 0;
+    return (MAP_GHIST_WARPS + 2) * capacity;
+}
+
 cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const int32_t *ids,
                                  const float *alpha, int T, int P, int capacity, int max_pairs,
                                  cudaStream_t st)
@@ -353,8 +367,16 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
     int nw = (P + 63) / 64;
     nw = nw < 1 ? 1 : (nw > threads / 32 ? threads / 32 : nw);
     int staged = 0;
+    int32_t *hist_g = nullptr;
     // words: [staged arrays] + nw histograms + two per-bin arrays
-    if (staged_words + 3LL * capacity <= budget) {
+    if (map_global_hist_words(capacity) > 0) {
+        // a pool too large for shared memory: histograms in global memory
+        if (!m.ghist)
+            return cudaErrorInvalidValue;
+        hist_g = m.ghist;
+        if (nw > MAP_GHIST_WARPS)
+            nw = MAP_GHIST_WARPS;
+    } else if (staged_words + 3LL * capacity <= budget) {
         staged = 1;
         const long long fit = (budget - staged_words) / capacity - 2;
         if (nw > fit)
@@ -370,8 +392,9 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
     // memory when they fit (short ones gain less than the extra phase costs)
     const int sorted_smem =
         staged && P >= 2048 && staged_words + (long long)(nw + 2) * capacity + 2LL * P <= budget;
-    const size_t smem = 4 * ((staged ? (size_t)staged_words : 0) + (size_t)(nw + 2) * capacity +
-                             (sorted_smem ? 2 * (size_t)P : 0));
+    const size_t smem =
+        4 * ((staged ? (size_t)staged_words : 0) + (hist_g ? 0 : (size_t)(nw + 2) * capacity) +
+             (sorted_smem ? 2 * (size_t)P : 0));
     static thread_local int attr_done = -1;  // per host thread
     int dev = 0;
     cudaGetDevice(&dev);
@@ -385,7 +408,7 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
             return e;
         attr_done = dev;
     }
-    MapArgs a{m, offsets, ids, alpha, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity),
+    MapArgs a{m, offsets, ids, alpha, hist_g, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity),
               mma_tile_bound(P, capacity), sorted_smem};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1, 1, 1);

@@ -71,9 +71,11 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
-// Waits for the barrier phase with the given parity, for at most
-// WAIT_LIMIT_NS; on expiry sets LORA_DEV_TIMEOUT in *status and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *status)
+// Waits for the barrier phase with the given parity, for at most limit_ns
+// (WAIT_LIMIT_NS unless a caller passes less); on expiry sets
+// LORA_DEV_TIMEOUT in *status and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *status,
+                                                  uint64_t limit_ns = WAIT_LIMIT_NS)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -82,7 +84,37 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         for (int i = 0; i < 8; ++i)
             if (mbar_try_wait_sleep(bar, parity, 2000))
                 return true;
-        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+        if (global_timer_ns() - t0 > limit_ns) {
+            atomicOr(status, LORA_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu_u32(const void *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until the counter *cnt (written by other CTAs) has reached `target`
+// -- (int)(*cnt - target) >= 0, so a counter may wrap around --, for at most
+// limit_ns; on expiry sets LORA_DEV_TIMEOUT in *status and returns false.
+// The read that ends the wait has acquire semantics at GPU scope.
+__device__ __forceinline__ bool wait_count_bounded(const void *cnt, unsigned target, int32_t *status,
+                                                   uint64_t limit_ns = WAIT_LIMIT_NS)
+{
+    if ((int)(ld_acquire_gpu_u32(cnt) - target) >= 0)
+        return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        for (int i = 0; i < 16; ++i) {
+            if ((int)(ld_acquire_gpu_u32(cnt) - target) >= 0)
+                return true;
+            __nanosleep(32);
+        }
+        if (global_timer_ns() - t0 > limit_ns) {
             atomicOr(status, LORA_DEV_TIMEOUT);
             return false;
         }

@@ -46,6 +46,7 @@ EXPORTS = [
     "lora_mapping_create", "lora_build_mapping", "lora_delta_apply", "lora_delta_apply_path",
     "lora_dispatch_choose", "lora_delta_apply_host", "lora_mapping_status", "lora_mapping_export",
     "lora_mapping_destroy", "lora_status_string", "lora_version", "lora_delta_apply_noalloc",
+    "lora_diag_wait_expiry",
 ]
 
 LORA_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -90,6 +91,7 @@ def load(path: str | None = None):
         "lora_mapping_destroy": ([V], I),
         "lora_status_string": ([I], ctypes.c_char_p),
         "lora_version": ([], ctypes.c_char_p),
+        "lora_diag_wait_expiry": ([I, ctypes.c_longlong, V, V], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -230,10 +232,55 @@ def lora_delta_apply_host(x_host, y_host, offsets_host, ids_host, alpha_host, T:
                                         _dptr(ranks, "ranks", "int32"), m, _stream(stream)))
 
 
-def lora_delta_apply_noalloc(x, y, pool: int, ranks, offsets, ids, alpha, T: int, P: int,
+def _numel(t) -> int | None:
+    """Element count of a tensor or array (None for a raw address or None)."""
+    if t is None or isinstance(t, int):
+        return None
+    return int(t.size) if isinstance(t, np.ndarray) else int(t.numel())
+
+
+def _rows_cols(t):
+    """(rows, columns) of a 2-D tensor or array, else None."""
+    if t is None or isinstance(t, int) or len(t.shape) != 2:
+        return None
+    return int(t.shape[0]), int(t.shape[1])
+
+
+def _noalloc_checks(x, y, pool, ranks, offsets, ids, alpha, T: int, P: int):
+    """Sizes the kernels would otherwise read past: the pair arrays against
+    T and P, x and y against T rows (and the pool's widths when a LoraPool is
+    given), ranks against the pool's capacity."""
+    if T < 0 or P < 0:
+        raise ValueError(f"lora_delta_apply_noalloc: T = {T} and P = {P} must be >= 0")
+    for name, t, want in (("offsets", offsets, T + 1), ("ids", ids, P), ("alpha", alpha, P)):
+        n = _numel(t)
+        if n is not None and n != want:
+            raise ValueError(f"lora_delta_apply_noalloc: {name} holds {n} entries, {want} expected "
+                             f"(T = {T}, P = {P})")
+    d_in, d_out, cap = (getattr(pool, "d_in", None), getattr(pool, "d_out", None),
+                        getattr(pool, "capacity", None))
+    for name, t, width in (("x", x, d_in), ("y", y, d_out)):
+        rc = _rows_cols(t)
+        if rc is None:
+            continue
+        if rc[0] < T:
+            raise ValueError(f"lora_delta_apply_noalloc: {name} has {rc[0]} rows, at least T = {T} needed")
+        if width is not None and rc[1] != width:
+            raise ValueError(f"lora_delta_apply_noalloc: {name} has {rc[1]} columns, the pool's width is {width}")
+    n = _numel(ranks)
+    if n is not None and cap is not None and n < cap:
+        raise ValueError(f"lora_delta_apply_noalloc: ranks holds {n} entries, the pool has {cap} slots")
+
+
+def lora_delta_apply_noalloc(x, y, pool, ranks, offsets, ids, alpha, T: int, P: int,
                              status=None, stream=None):
+    """pool: a pool handle, or an object with ``handle`` (and ``d_in``,
+    ``d_out``, ``capacity``, which enable the width and rank-table checks),
+    such as ``LoraPool``."""
+    _noalloc_checks(x, y, pool, ranks, offsets, ids, alpha, T, P)
+    handle = pool if pool is None or isinstance(pool, int) else pool.handle
     _check("lora_delta_apply_noalloc",
-           load().lora_delta_apply_noalloc(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool,
+           load().lora_delta_apply_noalloc(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), handle,
                                            _dptr(ranks, "ranks", "int32"), _dptr(offsets, "offsets", "int32"),
                                            _dptr(ids, "ids", "int32"), _dptr(alpha, "alpha", "float32"), T, P,
                                            _dptr(status, "status", "int32"), _stream(stream)))
@@ -269,6 +316,12 @@ def lora_mapping_export(m: int, P: int, capacity: int, stream=None) -> dict:
 
 def lora_mapping_destroy(m: int):
     _check("lora_mapping_destroy", load().lora_mapping_destroy(m))
+
+
+def lora_diag_wait_expiry(kind: int, limit_ns: int, words, stream=None):
+    """words: device int32 [4] (words[1] = 0 for kind 1)."""
+    _check("lora_diag_wait_expiry",
+           load().lora_diag_wait_expiry(kind, limit_ns, _dptr(words, "words", "int32"), _stream(stream)))
 
 
 def lora_version() -> str:

@@ -200,3 +200,50 @@ def test_wrappers_check_shapes_before_the_library():
         m.build(off, torch.zeros(4, dtype=torch.int32), torch.zeros(3))
     with pytest.raises(ValueError, match="1-D"):
         m.build(off.view(5, 1), torch.zeros(4, dtype=torch.int32), torch.zeros(4))
+
+
+def test_noalloc_binding_checks_sizes_before_the_library():
+    """lora_delta_apply_noalloc refuses pair arrays whose lengths disagree
+    with T and P, x / y with fewer than T rows or the wrong width, and a rank
+    table shorter than the pool, before any library call (CPU tensors: the
+    size checks come before the memory checks)."""
+    import torch
+    from tenant_composite_lora_gb300 import native
+
+    class Pool:
+        d_in, d_out, capacity, handle = 64, 128, 8, 1
+
+    T, P = 4, 6
+    bf = torch.bfloat16
+    x, y = torch.zeros(T, 64, dtype=bf), torch.zeros(T, 128, dtype=bf)
+    off, ids, al = torch.zeros(T + 1, dtype=torch.int32), torch.zeros(P, dtype=torch.int32), torch.zeros(P)
+
+    def call(**kw):
+        a = dict(x=x, y=y, pool=Pool, ranks=None, offsets=off, ids=ids, alpha=al, T=T, P=P)
+        a.update(kw)
+        native.lora_delta_apply_noalloc(a["x"], a["y"], a["pool"], a["ranks"], a["offsets"], a["ids"],
+                                        a["alpha"], a["T"], a["P"], stream=0)
+
+    with pytest.raises(ValueError, match="ids holds 5 entries, 6 expected"):
+        call(ids=torch.zeros(5, dtype=torch.int32))
+    with pytest.raises(ValueError, match="ids holds 6 entries, 7 expected"):
+        call(P=7, alpha=torch.zeros(7))
+    with pytest.raises(ValueError, match="alpha holds 5 entries, 6 expected"):
+        call(alpha=torch.zeros(5))
+    with pytest.raises(ValueError, match="offsets holds 5 entries, 6 expected"):
+        call(T=5)
+    with pytest.raises(ValueError, match="x has 3 rows"):
+        call(x=torch.zeros(3, 64, dtype=bf))
+    with pytest.raises(ValueError, match="y has 3 rows"):
+        call(y=torch.zeros(3, 128, dtype=bf))
+    with pytest.raises(ValueError, match="x has 32 columns"):
+        call(x=torch.zeros(T, 32, dtype=bf))
+    with pytest.raises(ValueError, match="y has 64 columns"):
+        call(y=torch.zeros(T, 64, dtype=bf))
+    with pytest.raises(ValueError, match="ranks holds 7 entries"):
+        call(ranks=torch.zeros(7, dtype=torch.int32))
+    with pytest.raises(ValueError, match="must be >= 0"):
+        call(T=-1)
+    # everything consistent: the size checks pass and the memory check refuses the host tensors
+    with pytest.raises(ValueError, match="x: a CUDA tensor is expected"):
+        call(ranks=torch.zeros(8, dtype=torch.int32))
