@@ -44,11 +44,9 @@
  *    created; call with that device current.
  *  - Host threads: distinct pools and mappings may be created and used from
  *    several threads at once (one-time set-up, such as the tensor-map encoder
- *    lookup and the kernels' launch attributes, is safe to race).  One object
- *    is used by one thread at a time.  The forced fused path
- *    (LORA_PATH_FUSED) caches its co-residency figure per process: its first
- *    call on a device must not race another first call of that path on a
- *    different device.
+ *    lookup, the kernels' launch attributes and the cached SM count, is kept
+ *    per host thread or done once under a lock, so it is safe to race).  One
+ *    object is used by one thread at a time.
  */
 #ifndef TCLORA_LORA_H
 #define TCLORA_LORA_H

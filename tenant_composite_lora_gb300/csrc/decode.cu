@@ -463,7 +463,7 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
 {
     if (!decode_supported(pool.d_in, pool.d_out))
         return cudaErrorNotSupported;
-    static int attr_dev = -1;
+    static thread_local int attr_dev = -1;  // per host thread: concurrent first calls each set the attribute
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_dev != dev) {
@@ -521,7 +521,8 @@ cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const 
 {
     if (!decode_supported(pool.d_in, pool.d_out))
         return cudaErrorNotSupported;
-    static int attr_dev = -1, resident = 0;
+    // per host thread: the device and its co-residency figure are set together
+    static thread_local int attr_dev = -1, resident = 0;
     int dev = 0;
     cudaGetDevice(&dev);
     const size_t smem = (size_t)pool.d_in * 2;

@@ -258,8 +258,9 @@ def _other_batch(wl, seed):
     return dataclasses.replace(wl, ids=ids, alpha=alpha)
 
 
+@pytest.mark.parametrize("path", [PATH_DECODE, PATH_FUSED])
 @pytest.mark.parametrize("name", ["zipf", "sweep8", "distinct"])
-def test_new_mapping_then_apply_without_a_break(name):
+def test_new_mapping_then_apply_without_a_break(name, path):
     """Batch after batch on one stream, each apply straight after its mapping
     (no other kernel, no synchronisation in between), as a decode loop runs:
     every apply must see its own batch's mapping, not the previous one."""
@@ -276,7 +277,7 @@ def test_new_mapping_then_apply_without_a_break(name):
         with torch.cuda.stream(s):
             for (off, ids, al), y in zip(dev, ys):
                 dw.mapping.build(off, ids, al, s)
-                tcl.delta_apply(dw.x, y, dw.pool, dw.mapping, path=PATH_DECODE, stream=s)
+                tcl.delta_apply(dw.x, y, dw.pool, dw.mapping, path=path, stream=s)
         s.synchronize()
         got = [bf16_to_numpy_bits(y) for y in ys]
     finally:
@@ -286,8 +287,9 @@ def test_new_mapping_then_apply_without_a_break(name):
         delta_gate(y, acc)
 
 
+@pytest.mark.parametrize("path", [PATH_DECODE, PATH_FUSED])
 @pytest.mark.parametrize("name", ["zipf", "sweep8"])
-def test_two_applies_into_one_y_without_a_break(name):
+def test_two_applies_into_one_y_without_a_break(name, path):
     """Two applies of one mapping into the same y back to back (y starts at
     zero): the second must read the first one's result, so y ends at twice
     the delta."""
@@ -300,7 +302,7 @@ def test_two_applies_into_one_y_without_a_break(name):
         torch.cuda.synchronize()
         with torch.cuda.stream(s):
             for _ in range(2):
-                tcl.delta_apply(dw.x, y, dw.pool, dw.mapping, path=PATH_DECODE, stream=s)
+                tcl.delta_apply(dw.x, y, dw.pool, dw.mapping, path=path, stream=s)
         s.synchronize()
         got = bf16_to_numpy_bits(y)
     finally:
@@ -558,6 +560,21 @@ def test_shapes(d_in, d_out, r, k, path):
     wl = _custom(rng, d_in, d_out, r, cap, lists, ranks)
     y, st = run_gpu(wl, path=path)
     _, acc, _ = oracle.apply_workload(wl)
+    delta_gate(y, acc)
+
+
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_DECODE, PATH_FUSED])
+def test_decode_many_tokens_rank64_wide(path):
+    """256 tokens x 3 adapters of 1000 at rank 64 and a wide output (the
+    largest decode batch: more (token, column) items than a wave of warps,
+    the wide-rank expand, every row of every adapter)."""
+    rng = np.random.default_rng(44)
+    lists = [list(rng.choice(1000, size=3, replace=False)) for _ in range(256)]
+    wl = W.make_custom(rng, d_in=256, d_out=4096, r_max=64, capacity=1000, id_lists=lists,
+                       alpha_lists=[list(rng.random(3).astype(np.float32)) for _ in lists], y_sigma=0.0)
+    y, st = run_gpu(wl, path=path)
+    _, acc, _ = oracle.apply_workload(wl, threads=0)
+    assert st == 0
     delta_gate(y, acc)
 
 
