@@ -333,22 +333,30 @@ def bench_ours(args, rank, world, dist):
         if st != 0:
             raise RuntimeError(f"device status {st}")
 
-        # graphs: one pass over all replicas
-        def capture(fn):
+        # graphs: one pass over all replicas, and the first K mod R replicas
+        # for the remainder, so that exactly K steps are timed
+        def capture(fn, n=None):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                for rep in reps:
+                for rep in reps[: (R if n is None else n)]:
                     fn(rep)
             return g
 
         for rep in reps:  # build every mapping once before the apply-only graph
             native.lora_build_mapping(rep["mapping"].handle, rep["off"], rep["ids"], rep["alpha"],
                                       wl.T, wl.P, stream)
+        K = max(1, args.steps)
+        full, rem = divmod(K, R)
         g_step = capture(step)
         g_apply = capture(apply_only)
+        g_step_rem = capture(step, rem) if rem else None
+        g_apply_rem = capture(apply_only, rem) if rem else None
         stream.synchronize()
 
-        def timed(graph, passes):
+        def timed(graph, graph_rem):
+            """Device time of exactly K steps: `full` replays of the pass and
+            one of the remainder, after W warm-up passes, with a barrier and a
+            synchronisation on both sides; the maximum over ranks."""
             for _ in range(max(1, args.warmup)):
                 graph.replay()
             stream.synchronize()
@@ -358,20 +366,22 @@ def bench_ours(args, rank, world, dist):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for _ in range(passes):
+            for _ in range(full):
                 graph.replay()
+            if graph_rem is not None:
+                graph_rem.replay()
             e1.record(stream)
             e1.synchronize()
             torch.cuda.synchronize(dev)
             return max_over_ranks(e0.elapsed_time(e1), dist, dev)
 
-        passes = max(1, int(np.ceil(args.steps / R)))
         clk = ClockSampler(local)
-        ms_step_total = timed(g_step, passes)
+        ms_step_total = timed(g_step, g_step_rem)
         clocks = clk.stop()
-        steps_done = passes * R
+        steps_done = K
         ms_per_step = ms_step_total / steps_done
-        ms_apply = timed(g_apply, passes) / steps_done
+        ms_apply = timed(g_apply, g_apply_rem) / steps_done
+        passes = max(1, full)
 
         # spread of the step time: each pass (R steps, one per replica) timed on
         # its own, after the contract's timed region; reported per step
@@ -454,6 +464,192 @@ def bench_ours(args, rank, world, dist):
         "step_us_spread": spread_step,
     }
     return line, wl
+
+
+class ColdTimer:
+    """Device time of a captured piece of work with a cold L2: every timed
+    replay runs a graph [read of FLUSH_BYTES, work]; a graph of the read
+    alone is timed the same way and subtracted, so the figure is the work's
+    own time starting from an L2 that holds none of its data."""
+
+    FLUSH_BYTES = 256 << 20  # twice the L2
+
+    def __init__(self, torch, stream, device):
+        self.torch, self.stream, self.dev = torch, stream, device
+        self.src = torch.empty(self.FLUSH_BYTES // 4, dtype=torch.float32, device=device).fill_(1.0)
+        self.out = torch.empty((), dtype=torch.float32, device=device)
+        self.g_flush = self.capture(lambda: None)
+        self.flush_ms = None
+
+    def capture(self, fn):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            torch.sum(self.src, dim=0, out=self.out)
+            fn()
+        return g
+
+    def _mean_ms(self, g, n):
+        torch = self.torch
+        for _ in range(3):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.stream)
+        for _ in range(n):
+            g.replay()
+        e1.record(self.stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def time_us(self, fn, n=100):
+        g = self.capture(fn)
+        with self.torch.cuda.stream(self.stream):
+            a = self._mean_ms(g, n)
+            b = self._mean_ms(self.g_flush, n)
+            a2 = self._mean_ms(g, n)
+            b2 = self._mean_ms(self.g_flush, n)
+        return max(0.0, ((a + a2) - (b + b2)) / 2 * 1e3)
+
+
+def per_config_lines(args, peak, torch, stream, dev):
+    """Every workload of the metric: the apply and the step (mapping +
+    apply) from a cold L2, tokens/s, achieved HBM bandwidth against the
+    measured peak, and the ncu traffic of the path when it is on file."""
+    from tenant_composite_lora_gb300 import native
+    import workloads as W
+    from workloads.device import DeviceWorkload
+    timer = ColdTimer(torch, stream, dev)
+    out = {}
+    for name in ["distinct", "zipf", "prefill", "sweep1", "sweep8", "sweep64", "sweep256"]:
+        t0 = time.perf_counter()
+        wl = W.make(name)
+        ab = W.algorithmic_bytes(wl)
+        with torch.cuda.stream(stream):
+            dw = DeviceWorkload(wl, stream=stream)
+            try:
+                y = dw.y0.clone()
+                m, pool = dw.mapping.handle, dw.pool.handle
+
+                def apply_():
+                    native.lora_delta_apply(dw.x, y, pool, None, m, stream)
+
+                def step_():
+                    native.lora_build_mapping(m, dw.offsets, dw.ids, dw.alpha, wl.T, wl.P, stream)
+                    native.lora_delta_apply(dw.x, y, pool, None, m, stream)
+
+                apply_us = timer.time_us(apply_)
+                step_us = timer.time_us(step_)
+            finally:
+                dw.close()
+        path = PATH_NAMES[native.lora_dispatch_choose(wl.T, wl.P, wl.r_max, wl.d_in, wl.d_out)]
+        achieved = ab["total"] / (apply_us * 1e-6) / 1e9 if apply_us > 0 else None
+        out[name] = {
+            "T": wl.T, "P": wl.P, "path": path, "apply_us": round(apply_us, 3), "step_us": round(step_us, 3),
+            "tokens_per_s": round(wl.T / (step_us * 1e-6), 1) if step_us > 0 else None,
+            "algorithmic_bytes": ab["total"], "achieved_gbs": round(achieved, 1) if achieved else None,
+            "frac": round(achieved / peak, 4) if achieved else None, "traffic": ncu_traffic(name, path),
+            "setup_s": round(time.perf_counter() - t0, 2),
+        }
+    return {"protocol": "cold L2: a 256 MB read before every timed replay, its own time subtracted; "
+                        "mean over 200 replays; path = the dispatch table's", "configs": out}
+
+
+def ablation_lines(torch, stream, dev):
+    """The pages' kernel ablation on this GPU: the fused path against the
+    naive per-adapter loop, Copy + SGMV and the explicit pre-merge, each
+    timed eagerly from a cold L2 (events around the call; the naive loop and
+    Copy + SGMV read the batch's segments back to the host inside the call)."""
+    import tenant_composite_lora_gb300 as tcl
+    from tenant_composite_lora_gb300 import native
+    import workloads as W
+    from workloads.device import DeviceWorkload
+    flush = torch.empty(ColdTimer.FLUSH_BYTES // 4, dtype=torch.float32, device=dev).fill_(1.0)
+    out = {}
+    for name in ["distinct", "zipf"]:
+        wl = W.make(name)
+        res = {}
+        with torch.cuda.stream(stream):
+            dw = DeviceWorkload(wl, stream=stream)
+            try:
+                y = dw.y0.clone()
+                nb = max(native.lora_ablation_workspace_bytes(v, wl.T, wl.P, wl.d_in, wl.d_out, wl.r_max)
+                         for v in (1, 2, 3))
+                ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+                calls = {
+                    "fused_path": lambda: native.lora_delta_apply(dw.x, y, dw.pool.handle, None, dw.mapping.handle,
+                                                                  stream),
+                    "naive_loop": lambda: native.lora_delta_apply_ablation(dw.x, y, dw.pool.handle, None,
+                                                                           dw.mapping.handle, 1, ws, nb, stream),
+                    "copy_sgmv": lambda: native.lora_delta_apply_ablation(dw.x, y, dw.pool.handle, None,
+                                                                          dw.mapping.handle, 2, ws, nb, stream),
+                    "premerge": lambda: native.lora_delta_apply_ablation(dw.x, y, dw.pool.handle, None,
+                                                                         dw.mapping.handle, 3, ws, nb, stream),
+                }
+                for key, fn in calls.items():
+                    times = []
+                    for it in range(8):
+                        torch.sum(flush)
+                        stream.synchronize()
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        fn()
+                        e1.record(stream)
+                        e1.synchronize()
+                        if it >= 2:
+                            times.append(e0.elapsed_time(e1) * 1e3)
+                    res[key] = round(statistics.median(times), 2)
+                del ws
+            finally:
+                dw.close()
+        base = res["fused_path"]
+        res["ratio_to_fused"] = {k: round(v / base, 2) for k, v in res.items() if k != "fused_path"}
+        out[name] = res
+    return {"unit": "us per apply (eager, cold L2, median of 6)", "workloads": out,
+            "pages_claim": "fused ~1/2 of Copy+SGMV and ~1/5 of the naive loop (DyMerge-LoRA, L40, Fig 16)"}
+
+
+def multi_projection_lines(torch, stream, dev):
+    """One layer's q, k, v, o projections (Llama-3-8B shapes, r = 8) over the
+    distinct decode batch: lora_delta_apply_multi against four separate
+    lora_delta_apply calls, cold L2."""
+    import tenant_composite_lora_gb300 as tcl
+    from tenant_composite_lora_gb300 import native
+    import workloads as W
+    from workloads.device import bf16_tensor
+    base = W.make("distinct")
+    timer = ColdTimer(torch, stream, dev)
+    shapes = {"q": (4096, 4096), "k": (4096, 1024), "v": (4096, 1024), "o": (4096, 4096)}
+    rng = np.random.default_rng(5)
+    pools, xs, ys = [], [], []
+    m = tcl.LoraMapping(base.T, base.P, base.capacity)
+    try:
+        with torch.cuda.stream(stream):
+            for _, (d_in, d_out) in shapes.items():
+                p = tcl.LoraPool(d_in, d_out, 8, base.capacity)
+                for a in range(base.capacity):
+                    A = torch.randn(d_in, 8, device=dev).mul_(0.02).to(torch.bfloat16)
+                    B = torch.randn(8, d_out, device=dev).mul_(0.02).to(torch.bfloat16)
+                    p.register(a, A, B, 8, stream)
+                pools.append(p)
+                xs.append(bf16_tensor(W.f32_to_bf16_bits(rng.standard_normal((base.T, d_in)).astype(np.float32) * 0.02),
+                                      dev))
+                ys.append(torch.zeros(base.T, d_out, dtype=torch.bfloat16, device=dev))
+            m.build(torch.from_numpy(base.offsets).to(dev), torch.from_numpy(base.ids).to(dev),
+                    torch.from_numpy(base.alpha).to(dev), stream)
+            stream.synchronize()
+            projs = [(x, y, p.handle, None) for x, y, p in zip(xs, ys, pools)]
+            multi = timer.time_us(lambda: native.lora_delta_apply_multi(projs, m.handle, stream))
+            separate = timer.time_us(lambda: [native.lora_delta_apply(x, y, p, None, m.handle, stream)
+                                              for x, y, p, _ in projs])
+    finally:
+        for p in pools:
+            p.close()
+        m.close()
+    return {"projections": {k: f"{v[0]}->{v[1]}, r=8" for k, v in shapes.items()}, "batch": "distinct decode",
+            "multi_us": round(multi, 3), "separate_us": round(separate, 3),
+            "per_projection_us": {"multi": round(multi / 4, 3), "separate": round(separate / 4, 3)}}
 
 
 def cpu_model() -> str:
@@ -560,6 +756,8 @@ def main():
                     help="wall time the reference arm aims for over its warm-up and timed steps")
     ap.add_argument("--max-replicas", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the per-config, ablation and multi-projection figures")
     ap.add_argument("--path", default="auto", choices=["auto", "split", "fused", "mma", "decode"],
                     help="force an execution path (default: the library's dispatch table)")
     args = ap.parse_args()
@@ -576,6 +774,19 @@ def main():
 
     line, wl = bench_ours(args, rank, world, dist)
     if rank == 0:
+        if not args.no_extras and world == 1:
+            import torch
+            dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+            stream = torch.cuda.Stream(device=dev)
+            peak, _ = peaks()
+            for key, fn in (("per_config", lambda: per_config_lines(args, peak, torch, stream, dev)),
+                            ("ablation", lambda: ablation_lines(torch, stream, dev)),
+                            ("multi_projection", lambda: multi_projection_lines(torch, stream, dev))):
+                try:
+                    line[key] = fn()
+                except Exception as exc:  # an auxiliary figure never costs the line itself
+                    line[key] = {"error": f"{type(exc).__name__}: {exc}"}
+                torch.cuda.empty_cache()
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = oracle_baseline(wl, args.cpu_seconds)
         print(json.dumps(line))

@@ -51,6 +51,7 @@
 #ifndef TCLORA_LORA_H
 #define TCLORA_LORA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -177,6 +178,70 @@ lora_status lora_build_mapping(lora_mapping *m, const int32_t *offsets_dev, cons
  */
 lora_status lora_delta_apply(const void *x_dev, void *y_dev, const lora_pool *pool,
                              const int32_t *ranks_dev, const lora_mapping *m, lora_stream_t stream);
+
+/*
+ * lora_delta_apply_multi: lora_delta_apply for several projections of one
+ * batch at once -- e.g. the q, k, v and o projections of a layer, each with
+ * its own pool (any d_in, d_out, r_max) -- sharing one mapping.  The pages
+ * apply LoRA to every dense projection of the model (DyMerge-LoRA page,
+ * "What they did", paper Sec. 5.1) and build the token-LoRA mapping once per
+ * batch (same page, "Core idea", Sec. 4.3); this entry point runs all the
+ * projections' shrinks in one launch and all their expands in a second one.
+ *   projs  : host array of n_proj descriptors; each x_dev / y_dev / pool /
+ *            ranks_dev has the meaning and layout of lora_delta_apply's, and
+ *            every pool's capacity must equal the mapping's
+ *   n_proj : 1 .. LORA_MAX_PROJECTIONS
+ * The projections' y buffers must not overlap one another or any x.
+ * Result per projection: what lora_delta_apply on that projection gives on
+ * the decode path -- the same shrink and the same (token, 256 columns)
+ * expand, so the same bits, except where a single call takes the wide-rank
+ * expand (r_max > 16 with few (token, column) items), whose summation order
+ * differs (last-bit differences, within the stated tolerance).  Decode
+ * batches (T <= 256) whose sum of round4(r_max) over the projections is at
+ * most 256 take the two shared launches; other batches run one
+ * lora_delta_apply per projection, in order.  Stream-ordered; no allocation.
+ * Returns LORA_ERR_INVALID_ARG for NULL or mismatched arguments or aliased
+ * outputs, LORA_ERR_NOT_SUPPORTED above LORA_MAX_PROJECTIONS.
+ */
+#define LORA_MAX_PROJECTIONS 8
+typedef struct {
+    const void *x_dev;
+    void *y_dev;
+    const lora_pool *pool;
+    const int32_t *ranks_dev;
+} lora_projection;
+lora_status lora_delta_apply_multi(const lora_projection *projs, int n_proj, const lora_mapping *m,
+                                   lora_stream_t stream);
+
+/*
+ * The pages' kernel ablation (DyMerge-LoRA page, "How far to trust it":
+ * the fused kernel against Copy+SGMV and a naive for-loop, paper Sec. 5.4 -
+ * 5.5, Figs. 14 and 16; pre-merging the composite weight, Figs. 3 - 4),
+ * reproduced as baselines for timing.  Each computes the same result as
+ * lora_delta_apply (fp32 accumulation, y rounded once) by the method named:
+ *   LORA_ABLATION_NAIVE     : per adapter of the batch, a shrink launch over
+ *                             its pairs and an expand launch adding into an
+ *                             fp32 copy of y (the host reads the segments
+ *                             back first: the call synchronises the stream);
+ *   LORA_ABLATION_COPY_SGMV : gather x into adapter order (a row per pair),
+ *                             segment shrink and expand into per-pair rows,
+ *                             then add each token's rows back into y (the
+ *                             host reads the valid pair count: synchronises);
+ *   LORA_ABLATION_PREMERGE  : per token dW_t = sum alpha A[:, :k] B[:k, :]
+ *                             (fp32, d_in x d_out), then y_t += x_t dW_t.
+ * workspace_dev: device scratch of at least lora_ablation_workspace_bytes()
+ * bytes for this batch (16-byte aligned, caller-owned).  Unusable adapters
+ * contribute nothing but set no status bit.  Returns LORA_ERR_INVALID_ARG
+ * for bad arguments or a short workspace, LORA_ERR_NOT_SUPPORTED for an
+ * unknown variant.
+ */
+#define LORA_ABLATION_NAIVE 1
+#define LORA_ABLATION_COPY_SGMV 2
+#define LORA_ABLATION_PREMERGE 3
+size_t lora_ablation_workspace_bytes(int variant, int T, int P, int d_in, int d_out, int r_max);
+lora_status lora_delta_apply_ablation(const void *x_dev, void *y_dev, const lora_pool *pool,
+                                      const int32_t *ranks_dev, const lora_mapping *m, int variant,
+                                      void *workspace_dev, size_t workspace_bytes, lora_stream_t stream);
 
 /* lora_delta_apply_path: lora_delta_apply with the execution path forced
  * (LORA_PATH_AUTO = the dispatch table).  Returns LORA_ERR_NOT_SUPPORTED if the

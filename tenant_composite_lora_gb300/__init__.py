@@ -15,7 +15,8 @@ from .native import (LoraError, lora_build_mapping, lora_delta_apply, lora_delta
                      lora_delta_apply_noalloc, lora_delta_apply_path, lora_dispatch_choose, lora_mapping_create,
                      lora_mapping_destroy, lora_mapping_export, lora_mapping_status,
                      lora_pool_create, lora_pool_destroy, lora_pool_register,
-                     lora_pool_unregister, lora_version, lora_diag_wait_expiry)
+                     lora_pool_unregister, lora_version, lora_diag_wait_expiry, lora_delta_apply_multi,
+                     lora_ablation_workspace_bytes, lora_delta_apply_ablation)
 
 __all__ = [
     "native", "LoraError", "LoraPool", "LoraMapping", "delta_apply",
@@ -23,6 +24,7 @@ __all__ = [
     "lora_mapping_create", "lora_build_mapping", "lora_delta_apply", "lora_delta_apply_path",
     "lora_dispatch_choose", "lora_delta_apply_host", "lora_mapping_status", "lora_mapping_export",
     "lora_mapping_destroy", "lora_version", "lora_delta_apply_noalloc", "lora_diag_wait_expiry",
+    "lora_delta_apply_multi", "lora_ablation_workspace_bytes", "lora_delta_apply_ablation",
 ]
 
 

@@ -525,7 +525,7 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.toff, (size_t)max_tokens + 1);
     if (e == cudaSuccess) e = dalloc(&d.pq, P);
     if (e == cudaSuccess) e = dalloc(&d.zcnt, P);
-    if (e == cudaSuccess) e = dalloc(&d.z, P * LORA_MAX_RANK);
+    if (e == cudaSuccess) e = dalloc(&d.z, P * Z_ROW_FLOATS);
     d.partial_ctas = sm_count();
     if (e == cudaSuccess) e = dalloc(&d.partial, (size_t)d.partial_ctas * EXP_TILE_ELEMS);
     if (e == cudaSuccess && map_global_hist_words(capacity) > 0)
@@ -590,6 +590,83 @@ lora_status lora_delta_apply(const void *x_dev, void *y_dev, const lora_pool *po
                              const lora_mapping *m, lora_stream_t stream)
 {
     return lora_delta_apply_path(x_dev, y_dev, pool, ranks_dev, m, LORA_PATH_AUTO, stream);
+}
+
+size_t lora_ablation_workspace_bytes(int variant, int T, int P, int d_in, int d_out, int r_max)
+{
+    if (T < 0 || P < 0 || d_in <= 0 || d_out <= 0 || r_max <= 0)
+        return 0;
+    return ablation_workspace_bytes(variant, T, P, d_in, d_out, r_max);
+}
+
+lora_status lora_delta_apply_ablation(const void *x_dev, void *y_dev, const lora_pool *pool,
+                                      const int32_t *ranks_dev, const lora_mapping *m, int variant,
+                                      void *workspace_dev, size_t workspace_bytes, lora_stream_t stream)
+{
+    if (!x_dev || !y_dev || !pool || !m || !m->built || x_dev == y_dev || m->capacity != pool->capacity)
+        return LORA_ERR_INVALID_ARG;
+    if (!aligned16(x_dev) || !aligned16(y_dev))
+        return LORA_ERR_INVALID_ARG;
+    if (variant != LORA_ABLATION_NAIVE && variant != LORA_ABLATION_COPY_SGMV && variant != LORA_ABLATION_PREMERGE)
+        return LORA_ERR_NOT_SUPPORTED;
+    const size_t need = ablation_workspace_bytes(variant, m->T, m->P, pool->d_in, pool->d_out, pool->r_max);
+    if (need > 0 && (!workspace_dev || workspace_bytes < need || !aligned16(workspace_dev)))
+        return LORA_ERR_INVALID_ARG;
+    if (m->T == 0 || m->P == 0)
+        return LORA_OK;
+    return from_cuda(run_ablation(variant, static_cast<const __nv_bfloat16 *>(x_dev), static_cast<__nv_bfloat16 *>(y_dev),
+                                  pool_dev(pool), ranks_dev, m->dev, m->T, m->P, workspace_dev,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
+lora_status lora_delta_apply_multi(const lora_projection *projs, int n_proj, const lora_mapping *m,
+                                   lora_stream_t stream)
+{
+    if (!projs || !m || !m->built || n_proj < 1)
+        return LORA_ERR_INVALID_ARG;
+    if (n_proj > LORA_MAX_PROJECTIONS)
+        return LORA_ERR_NOT_SUPPORTED;
+    int zcols = 0;
+    bool decode_ok = m->T <= DECODE_MAX_TOKENS;
+    for (int j = 0; j < n_proj; ++j) {
+        const lora_projection &p = projs[j];
+        if (!p.x_dev || !p.y_dev || !p.pool || p.x_dev == p.y_dev || p.pool->capacity != m->capacity)
+            return LORA_ERR_INVALID_ARG;
+        if (!aligned16(p.x_dev) || !aligned16(p.y_dev))
+            return LORA_ERR_INVALID_ARG;
+        for (int i = 0; i < j; ++i)
+            if (projs[i].y_dev == p.y_dev || projs[i].x_dev == p.y_dev || p.x_dev == projs[i].y_dev)
+                return LORA_ERR_INVALID_ARG;  // one projection's output is another's input or output
+        zcols += z_stride(p.pool->r_max);
+        decode_ok = decode_ok && decode_supported(p.pool->d_in, p.pool->d_out);
+    }
+    if (m->T == 0 || m->P == 0)
+        return LORA_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (decode_ok && zcols <= Z_ROW_FLOATS) {
+        MultiDecArgs a{};
+        a.n = n_proj;
+        a.m = m->dev;
+        a.T = m->T;
+        for (int j = 0; j < n_proj; ++j) {
+            a.p[j].x = static_cast<const __nv_bfloat16 *>(projs[j].x_dev);
+            a.p[j].y = static_cast<__nv_bfloat16 *>(projs[j].y_dev);
+            a.p[j].pool = pool_dev(projs[j].pool);
+            a.p[j].ranks = projs[j].ranks_dev;
+        }
+        const cudaError_t e = launch_decode_multi(a, m->P, st);
+        if (e != cudaErrorNotSupported)
+            return from_cuda(e);
+    }
+    // long batches (or shapes the decode kernels do not take): one apply per
+    // projection, each on the path the dispatch table picks
+    for (int j = 0; j < n_proj; ++j) {
+        const lora_status s =
+            lora_delta_apply(projs[j].x_dev, projs[j].y_dev, projs[j].pool, projs[j].ranks_dev, m, stream);
+        if (s != LORA_OK)
+            return s;
+    }
+    return LORA_OK;
 }
 
 }  // extern "C"

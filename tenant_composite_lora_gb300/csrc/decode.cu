@@ -40,7 +40,8 @@ struct DecShrinkArgs {
     PoolDev pool;
     const int32_t *ranks;
     MapDev m;
-    int zs;
+    int zs;    // z row stride (floats per sorted pair)
+    float *z;  // this projection's first z column: z[q * zs + j]
 };
 
 __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
@@ -128,7 +129,7 @@ __device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *x
     for (int off = 16; off > 0; off >>= 1)
         acc += __shfl_xor_sync(0xffffffffu, acc, off);
     if (live && lane == 0)
-        a.m.z[(size_t)q * a.zs + j] = al * acc;
+        a.z[(size_t)q * a.zs + j] = al * acc;
 }
 
 __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a)
@@ -151,6 +152,7 @@ struct DecExpandArgs {
     const int32_t *ranks;
     MapDev m;
     int T, zs, nc;  // nc: 256-column chunks per row (the last may be partial)
+    const float *z; // the shrink's output for this projection: z[q * zs + j]
 };
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float z, uint4 b)
@@ -241,7 +243,7 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
         const int k = kk[i];
         if (k > 0) {
             wait_pair(pq[i].x);
-            const float *zr = a.m.z + (size_t)pq[i].x * a.zs;
+            const float *zr = a.z + (size_t)pq[i].x * a.zs;
             float zz[DE_PR];
 #pragma unroll
             for (int j = 0; j < DE_PR; ++j)
@@ -260,7 +262,7 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
         const int k = dec_rank(a.pool, a.ranks, v.y);
         if (k > 0) {
             wait_pair(v.x);
-            dec_rows(acc, a.pool.B + (size_t)v.y * r_max * d_out + col, a.m.z + (size_t)v.x * a.zs, 0, k, d_out,
+            dec_rows(acc, a.pool.B + (size_t)v.y * r_max * d_out + col, a.z + (size_t)v.x * a.zs, 0, k, d_out,
                      on);
         }
     }
@@ -341,7 +343,7 @@ __global__ void __launch_bounds__(32 * DW_WARPS, 1) k_dec_expand_wide(const DecE
     for (int i = 0; i < DW_PP; ++i) {
         const int k = kk[i];
         if (k > 0) {
-            const float *zr = a.m.z + (size_t)pq[i].x * a.zs;
+            const float *zr = a.z + (size_t)pq[i].x * a.zs;
             float zz[DW_PR];
 #pragma unroll
             for (int u = 0; u < DW_PR; ++u) {
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(32 * DW_WARPS, 1) k_dec_expand_wide(const DecE
         if (k <= 0)
             continue;
         const __nv_bfloat16 *br = a.pool.B + (size_t)v.y * r_max * d_out + col;
-        const float *zr = a.m.z + (size_t)v.x * a.zs;
+        const float *zr = a.z + (size_t)v.x * a.zs;
         uint4 bb[DW_PR];
         float zz[DW_PR];
 #pragma unroll
@@ -452,6 +454,48 @@ __global__ void __launch_bounds__(256, 1) k_dec_fused(const DecFusedArgs a)
     }
 }
 
+// ------------------------------------------------------------ several projections, one launch each
+
+// The shrink of every projection in one grid: blockIdx.y runs over the
+// projections' row groups (prefix gpre), blockIdx.x over the sorted pairs.
+__global__ void __launch_bounds__(DS_THREADS) k_dec_shrink_multi(const MultiDecArgs a)
+{
+    extern __shared__ __align__(16) uint4 xs[];
+    pdl_wait();               // as k_dec_shrink
+    pdl_launch_dependents();  // the expand reads the mapping and y before its own wait
+    const int yb = blockIdx.y;
+    int j = 0;
+    while (j + 1 < a.n && yb >= a.gpre[j + 1])
+        ++j;
+    const MultiDecProj &pj = a.p[j];
+    const DecShrinkArgs sa{pj.x, pj.pool, pj.ranks, a.m, Z_ROW_FLOATS, a.m.z + pj.zoff};
+    dec_shrink_item(sa, xs, blockIdx.x, (yb - a.gpre[j]) * (blockDim.x >> 5), yb == a.gpre[j]);
+}
+
+// The expand of every projection in one grid: warp g runs (projection j,
+// token, column chunk) with g - wpre[j] = chunk * T + token.
+template <int PP, int MINB>
+__global__ void __launch_bounds__(256, MINB) k_dec_expand_multi(const MultiDecArgs a)
+{
+    pdl_launch_dependents();
+    const int g = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (g >= a.wpre[a.n])
+        return;
+    int j = 0;
+    while (j + 1 < a.n && g >= a.wpre[j + 1])
+        ++j;
+    const MultiDecProj &pj = a.p[j];
+    const DecExpandArgs ea{pj.y, pj.pool, pj.ranks, a.m, a.T, Z_ROW_FLOATS, pj.nc, a.m.z + pj.zoff};
+    const int gl = g - a.wpre[j];
+    bool waited = false;
+    dec_expand_item<PP>(ea, gl % a.T, gl / a.T, [&](int) {
+        if (!waited) {
+            pdl_wait();  // z of the shrink
+            waited = true;
+        }
+    });
+}
+
 }  // namespace
 
 // The x row is staged in shared memory: d_in * 2 bytes of at most 200 KB.
@@ -472,7 +516,7 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
             return e;
         attr_dev = dev;
     }
-    DecShrinkArgs sa{x, pool, ranks, m, z_stride(pool.r_max)};
+    DecShrinkArgs sa{x, pool, ranks, m, z_stride(pool.r_max), m.z};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -491,7 +535,7 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
         return e;
     const int nc = (pool.d_out + 255) / 256;
     const long long warps = (long long)T * nc;
-    DecExpandArgs ea{y, pool, ranks, m, T, z_stride(pool.r_max), nc};
+    DecExpandArgs ea{y, pool, ranks, m, T, z_stride(pool.r_max), nc, m.z};
     if (pool.r_max > 16 && warps <= 2LL * sm_count()) {
         // few (token, chunk) items at large ranks: 8 warps share each item's rows
         cudaLaunchConfig_t wcfg = {};
@@ -541,7 +585,8 @@ cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const 
         return cudaErrorNotSupported;
     const int ng = (pool.r_max + 7) / 8;
     const int nc = (pool.d_out + 255) / 256;
-    DecFusedArgs a{{x, pool, ranks, m, z_stride(pool.r_max)}, {y, pool, ranks, m, T, z_stride(pool.r_max), nc}, ng};
+    DecFusedArgs a{{x, pool, ranks, m, z_stride(pool.r_max), m.z}, {y, pool, ranks, m, T, z_stride(pool.r_max), nc, m.z},
+                   ng};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sm_count(), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
@@ -554,6 +599,72 @@ cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const 
     cfg.numAttrs = 1;
     (void)P;
     return cudaLaunchKernelEx(&cfg, k_dec_fused, a);
+}
+
+cudaError_t launch_decode_multi(const MultiDecArgs &in, int P, cudaStream_t st)
+{
+    MultiDecArgs a = in;
+    if (a.n < 1 || a.n > MULTI_MAX_PROJ)
+        return cudaErrorInvalidValue;
+    int max_din = 0, max_r = 0, zcols = 0;
+    for (int j = 0; j < a.n; ++j) {
+        const PoolDev &pj = a.p[j].pool;
+        if (!decode_supported(pj.d_in, pj.d_out))
+            return cudaErrorNotSupported;
+        max_din = pj.d_in > max_din ? pj.d_in : max_din;
+        max_r = pj.r_max > max_r ? pj.r_max : max_r;
+        a.p[j].zoff = zcols;
+        zcols += z_stride(pj.r_max);
+    }
+    if (zcols > Z_ROW_FLOATS)
+        return cudaErrorNotSupported;
+    static thread_local int attr_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (attr_dev != dev) {
+        cudaError_t e =
+            cudaFuncSetAttribute(k_dec_shrink_multi, cudaFuncAttributeMaxDynamicSharedMemorySize, DS_SMEM_MAX);
+        if (e != cudaSuccess)
+            return e;
+        attr_dev = dev;
+    }
+    // shrink: one row group per rpc rank rows of each projection
+    const int rpc = max_r <= 8 ? 4 : 8;
+    a.gpre[0] = 0;
+    for (int j = 0; j < a.n; ++j)
+        a.gpre[j + 1] = a.gpre[j] + (a.p[j].pool.r_max + rpc - 1) / rpc;
+    // expand: T x column chunks of each projection
+    a.wpre[0] = 0;
+    for (int j = 0; j < a.n; ++j) {
+        a.p[j].nc = (a.p[j].pool.d_out + 255) / 256;
+        a.wpre[j + 1] = a.wpre[j] + a.T * a.p[j].nc;
+    }
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t scfg = {};
+    scfg.gridDim = dim3(P, a.gpre[a.n], 1);
+    scfg.blockDim = dim3(32 * rpc, 1, 1);
+    scfg.dynamicSmemBytes = (size_t)max_din * 2;
+    scfg.stream = st;
+    scfg.attrs = attr;
+    scfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&scfg, k_dec_shrink_multi, a);
+    if (e != cudaSuccess)
+        return e;
+    const long long warps = a.wpre[a.n];
+    int wpc = 8;
+    while (wpc > 1 && (warps + wpc - 1) / wpc < sm_count())
+        wpc >>= 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((warps + wpc - 1) / wpc), 1, 1);
+    cfg.blockDim = dim3(32 * wpc, 1, 1);
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (warps > 8LL * sm_count())
+        return cudaLaunchKernelEx(&cfg, k_dec_expand_multi<2, 2>, a);
+    return cudaLaunchKernelEx(&cfg, k_dec_expand_multi<DE_PP, 1>, a);
 }
 
 }  // namespace tcl

@@ -84,7 +84,7 @@ struct MapDev {
     int32_t *toff;                       // [max_tokens+1] copy of the batch's CSR offsets
     int2 *pq;                            // [max_pairs] per CSR pair: {sorted position, adapter}, -1s if left out
     int32_t *zcnt;                       // [max_pairs] per sorted pair: z row groups written (fused decode)
-    float *z;                            // [max_pairs][LORA_MAX_RANK] shrink output
+    float *z;                            // [max_pairs][Z_ROW_FLOATS] shrink output
     float *partial;                      // [partial_ctas][EXP_TILE_ELEMS] fused-kernel tiles
     int partial_ctas;
     int32_t *ghist;                      // [map_global_hist_words(capacity)] or null: mapping
@@ -97,6 +97,11 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
                                  cudaStream_t st);
 cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int32_t *ranks,
                           const MapDev &m, int P, int grid, cudaStream_t st);
+
+// Floats per sorted pair in the mapping's z buffer: one projection uses the
+// first round4(r_max); several projections applied in one launch place
+// their columns side by side (at most this many in total).
+constexpr int Z_ROW_FLOATS = 256;
 
 // z row stride (floats): r_max rounded up to a multiple of 4 (16-byte rows).
 inline int z_stride(int r_max) { return (r_max + 3) & ~3; }
@@ -123,6 +128,31 @@ bool fused_supported(int T, int d_out);
 bool decode_supported(int d_in, int d_out);
 cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
                           const MapDev &m, int T, int P, cudaStream_t st);
+// Several projections (pools of any shapes, one shared mapping) in one
+// decode launch pair: their z columns sit side by side in the mapping's z
+// rows of Z_ROW_FLOATS floats.
+constexpr int MULTI_MAX_PROJ = 8;
+struct MultiDecProj {
+    const __nv_bfloat16 *x;
+    __nv_bfloat16 *y;
+    PoolDev pool;
+    const int32_t *ranks;
+    int zoff;  // first z column of this projection (set by the launcher)
+    int nc;    // 256-column chunks of d_out (set by the launcher)
+};
+struct MultiDecArgs {
+    MultiDecProj p[MULTI_MAX_PROJ];
+    int n;
+    MapDev m;
+    int T;
+    int gpre[MULTI_MAX_PROJ + 1];  // prefix of the shrink's row groups per projection
+    int wpre[MULTI_MAX_PROJ + 1];  // prefix of the expand's (token, chunk) warps per projection
+};
+cudaError_t launch_decode_multi(const MultiDecArgs &a, int P, cudaStream_t st);
+// The pages' kernel ablation (naive loop, Copy + SGMV, pre-merge).
+size_t ablation_workspace_bytes(int variant, int T, int P, int d_in, int d_out, int r_max);
+cudaError_t run_ablation(int variant, const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool,
+                         const int32_t *ranks, const MapDev &m, int T, int P, void *ws, cudaStream_t st);
 // Dispatch: batches of at most this many tokens take the decode path.
 constexpr int DECODE_MAX_TOKENS = 256;
 // The same decode work as one cooperative launch (a CTA per SM): shrink

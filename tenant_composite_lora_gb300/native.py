@@ -46,8 +46,21 @@ EXPORTS = [
     "lora_mapping_create", "lora_build_mapping", "lora_delta_apply", "lora_delta_apply_path",
     "lora_dispatch_choose", "lora_delta_apply_host", "lora_mapping_status", "lora_mapping_export",
     "lora_mapping_destroy", "lora_status_string", "lora_version", "lora_delta_apply_noalloc",
-    "lora_diag_wait_expiry",
+    "lora_diag_wait_expiry", "lora_delta_apply_multi", "lora_ablation_workspace_bytes",
+    "lora_delta_apply_ablation",
 ]
+
+LORA_ABLATION_NAIVE = 1
+LORA_ABLATION_COPY_SGMV = 2
+LORA_ABLATION_PREMERGE = 3
+
+LORA_MAX_PROJECTIONS = 8
+
+
+class LoraProjection(ctypes.Structure):
+    """lora_projection: one projection of lora_delta_apply_multi."""
+    _fields_ = [("x_dev", ctypes.c_void_p), ("y_dev", ctypes.c_void_p), ("pool", ctypes.c_void_p),
+                ("ranks_dev", ctypes.c_void_p)]
 
 LORA_NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -92,6 +105,9 @@ def load(path: str | None = None):
         "lora_status_string": ([I], ctypes.c_char_p),
         "lora_version": ([], ctypes.c_char_p),
         "lora_diag_wait_expiry": ([I, ctypes.c_longlong, V, V], I),
+        "lora_delta_apply_multi": ([ctypes.POINTER(LoraProjection), I, V, V], I),
+        "lora_ablation_workspace_bytes": ([I, I, I, I, I, I], ctypes.c_size_t),
+        "lora_delta_apply_ablation": ([V, V, V, V, V, I, V, ctypes.c_size_t, V], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -210,6 +226,33 @@ def lora_delta_apply(x, y, pool: int, ranks, m: int, stream=None):
     _check("lora_delta_apply",
            load().lora_delta_apply(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool,
                                    _dptr(ranks, "ranks", "int32"), m, _stream(stream)))
+
+
+def lora_delta_apply_multi(projections, m: int, stream=None):
+    """projections: a sequence of (x, y, pool handle, ranks or None), one per
+    projection, all sharing the mapping m."""
+    n = len(projections)
+    arr = (LoraProjection * max(n, 1))()
+    for i, (x, y, pool, ranks) in enumerate(projections):
+        arr[i] = LoraProjection(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool, _dptr(ranks, "ranks", "int32"))
+    _check("lora_delta_apply_multi", load().lora_delta_apply_multi(arr, n, m, _stream(stream)))
+
+
+def lora_ablation_workspace_bytes(variant: int, T: int, P: int, d_in: int, d_out: int, r_max: int) -> int:
+    return int(load().lora_ablation_workspace_bytes(variant, T, P, d_in, d_out, r_max))
+
+
+def lora_delta_apply_ablation(x, y, pool: int, ranks, m: int, variant: int, workspace, workspace_bytes: int,
+                              stream=None):
+    """workspace: a device buffer (uint8 CUDA tensor or raw address) of at
+    least lora_ablation_workspace_bytes(...) bytes."""
+    ws = workspace if workspace is None or isinstance(workspace, int) else workspace.data_ptr()
+    if workspace is not None and not isinstance(workspace, int) and not workspace.is_cuda:
+        raise ValueError("workspace: a CUDA tensor is expected")
+    _check("lora_delta_apply_ablation",
+           load().lora_delta_apply_ablation(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool,
+                                            _dptr(ranks, "ranks", "int32"), m, variant, ws, workspace_bytes,
+                                            _stream(stream)))
 
 
 def lora_delta_apply_path(x, y, pool: int, ranks, m: int, path: int, stream=None):

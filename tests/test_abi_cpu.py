@@ -66,6 +66,22 @@ def test_bad_arguments_rejected_before_device(lib):
     assert lib.lora_pool_register(None, 0, None, None, 1, None) == 1
     assert lib.lora_pool_destroy(None) == 0
     assert lib.lora_mapping_destroy(None) == 0
+    assert lib.lora_delta_apply_multi(None, 1, None, None) == 1
+    assert lib.lora_delta_apply_ablation(None, None, None, None, None, 1, None, 0, None) == 1
+
+
+def test_ablation_workspace_sizes(lib):
+    """The ablation's scratch, host-computed: z rows and an fp32 y (naive
+    loop), gathered x rows, z rows and per-pair fp32 rows (Copy + SGMV), one
+    fp32 d_in x d_out weight per token (pre-merge); 256-byte pieces."""
+    from tenant_composite_lora_gb300 import native
+    r = lambda b: (b + 255) // 256 * 256
+    T, P, d_in, d_out, r_max = 32, 96, 4096, 4096, 8
+    assert native.lora_ablation_workspace_bytes(1, T, P, d_in, d_out, r_max) == r(P * 8 * 4) + r(T * d_out * 4)
+    assert native.lora_ablation_workspace_bytes(2, T, P, d_in, d_out, r_max) == \
+        r(P * d_in * 2) + r(P * 8 * 4) + r(P * d_out * 4)
+    assert native.lora_ablation_workspace_bytes(3, T, P, d_in, d_out, r_max) == r(T * d_in * d_out * 4)
+    assert native.lora_ablation_workspace_bytes(9, T, P, d_in, d_out, r_max) == 0
 
 
 def test_missing_library_fails_loudly(tmp_path):
