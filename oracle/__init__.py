@@ -52,6 +52,10 @@ def _load():
         lib.orc_build_mapping.restype = I
         lib.orc_round_bf16.argtypes = [ctypes.c_double]
         lib.orc_round_bf16.restype = ctypes.c_uint16
+        lib.orc_gate_logits.argtypes = [I, I, I, P, P, P, P]
+        lib.orc_gate_logits.restype = None
+        lib.orc_gate_topk.argtypes = [I, I, I, P, P, P, P, P]
+        lib.orc_gate_topk.restype = I
         lib.orc_max_threads.argtypes = []
         lib.orc_max_threads.restype = I
         _lib = lib
@@ -125,6 +129,32 @@ def build_mapping(offsets, ids, alpha, *, capacity):
         "seg_adapter": seg_adapter[:U].copy(), "seg_start": seg_start[:U + 1].copy(),
         "U": U, "P_valid": Pv, "status": int(st),
     }
+
+
+def gate_logits(x, Wg, req):
+    """fp64 logits [T, E]: x bf16 bits [T, d_in], Wg bf16 bits [R, E, d_in], req int32 [T]."""
+    x = _c(x, np.uint16)
+    Wg = _c(Wg, np.uint16)
+    req = _c(req, np.int32)
+    T, d_in = x.shape
+    E = Wg.shape[1]
+    out = np.empty((T, E), np.float64)
+    _load().orc_gate_logits(T, E, d_in, _ptr(x), _ptr(Wg), _ptr(req), _ptr(out))
+    return out
+
+
+def gate_topk(logits, cand, top_k: int):
+    """(offsets [T+1], ids [T*top_k], alpha [T*top_k], tokens without a
+    valid candidate) from fp32 logits [T, E] and candidate ids [T, E]
+    (-1 = padding)."""
+    logits = _c(logits, np.float32)
+    cand = _c(cand, np.int32)
+    T, E = logits.shape
+    offsets = np.empty(T + 1, np.int32)
+    ids = np.empty(max(T * top_k, 1), np.int32)
+    alpha = np.empty(max(T * top_k, 1), np.float32)
+    empty = _load().orc_gate_topk(T, E, top_k, _ptr(logits), _ptr(cand), _ptr(offsets), _ptr(ids), _ptr(alpha))
+    return offsets, ids[: T * top_k], alpha[: T * top_k], int(empty)
 
 
 def apply_workload(wl, ranks=None, threads: int = 1, want_acc: bool = True, y_in=None):

@@ -252,6 +252,91 @@ int orc_build_mapping(int T, int P, int capacity, const int32_t *offsets,
     return status;
 }
 
+/*
+ * MoE-LoRA gating that produces the pair lists (DyMerge-LoRA page, code
+ * release notes / Appendix A: per-token adapter weights from padded,
+ * masked candidate lists, batched gate logits, top-k, renormalised).
+ *
+ * orc_gate_logits: logits[t][e] = sum_d x[t][d] * Wg[req[t]][e][d], fp64.
+ *   x bf16 [T][d_in]; Wg bf16 [R][E][d_in] (a router per request); req[t]
+ *   the request of token t.
+ */
+void orc_gate_logits(int T, int E, int d_in, const uint16_t *x, const uint16_t *Wg, const int32_t *req,
+                     double *logits)
+{
+    for (int t = 0; t < T; ++t)
+        for (int e = 0; e < E; ++e) {
+            const uint16_t *w = Wg + ((size_t)req[t] * E + e) * d_in;
+            double s = 0.0;
+            for (int d = 0; d < d_in; ++d)
+                s += bf16_to_double(x[(size_t)t * d_in + d]) * bf16_to_double(w[d]);
+            logits[(size_t)t * E + e] = s;
+        }
+}
+
+/*
+ * orc_gate_topk: per token t, the candidates e with cand[t][e] >= 0 are
+ * ranked by logit, largest first, equal logits by the lower e; the first
+ * top_k are kept and weighted by the softmax over all candidates
+ * renormalised over the kept ones, alpha_i = exp(l_i) / sum_kept exp(l_j)
+ * (the full softmax denominator cancels), computed in fp64 from the given
+ * fp32 logits and rounded to fp32.  Every token emits exactly top_k pairs
+ * (offsets[t] = t * top_k): a token with fewer valid candidates repeats its
+ * best one with alpha = 0; a token with none emits ids -1 (alpha 0).
+ * Returns the number of tokens without any valid candidate.
+ */
+int orc_gate_topk(int T, int E, int top_k, const float *logits, const int32_t *cand, int32_t *offsets, int32_t *ids,
+                  float *alpha)
+{
+    int empty = 0;
+    int *taken = (int *)malloc(sizeof(int) * (size_t)(E > 0 ? E : 1));
+    int *sel = (int *)malloc(sizeof(int) * (size_t)(top_k > 0 ? top_k : 1));
+    for (int t = 0; t <= T; ++t)
+        offsets[t] = t * top_k;
+    for (int t = 0; t < T; ++t) {
+        const float *l = logits + (size_t)t * E;
+        const int32_t *c = cand + (size_t)t * E;
+        for (int e = 0; e < E; ++e)
+            taken[e] = 0;
+        int n = 0;
+        for (int i = 0; i < top_k; ++i) {
+            int best = -1;
+            for (int e = 0; e < E; ++e)
+                if (c[e] >= 0 && !taken[e] && (best < 0 || l[e] > l[best]))
+                    best = e; /* strict >: the lower e wins a tie */
+            if (best < 0)
+                break;
+            taken[best] = 1;
+            sel[n++] = best;
+        }
+        int32_t *id = ids + (size_t)t * top_k;
+        float *al = alpha + (size_t)t * top_k;
+        if (n == 0) {
+            ++empty;
+            for (int i = 0; i < top_k; ++i) {
+                id[i] = -1;
+                al[i] = 0.0f;
+            }
+            continue;
+        }
+        double mx = (double)l[sel[0]], den = 0.0;
+        for (int i = 0; i < n; ++i)
+            den += exp((double)l[sel[i]] - mx);
+        for (int i = 0; i < top_k; ++i) {
+            if (i < n) {
+                id[i] = c[sel[i]];
+                al[i] = (float)(exp((double)l[sel[i]] - mx) / den);
+            } else {
+                id[i] = c[sel[0]];
+                al[i] = 0.0f;
+            }
+        }
+    }
+    free(taken);
+    free(sel);
+    return empty;
+}
+
 int orc_max_threads(void)
 {
 #ifdef _OPENMP

@@ -414,3 +414,65 @@ def test_mapping_bad_offsets_and_empty():
     m = oracle.build_mapping(np.zeros(5, np.int32), np.zeros(0, np.int32),
                              np.zeros(0, np.float32), capacity=4)
     assert m["status"] == 0 and m["U"] == 0 and m["P_valid"] == 0
+
+
+# ---------------------------------------------------------------- MoE-LoRA gating
+def test_gate_topk_worked_examples():
+    """Hand-worked cases (tests/golden/gate_examples.json): ties to the lower
+    candidate, renormalisation over the kept pairs, masking of padding,
+    tokens short of candidates."""
+    import json
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "gate_examples.json")))
+    for case in g["cases"]:
+        off, ids, al, _ = oracle.gate_topk(np.array(case["logits"], np.float32), np.array(case["cand"], np.int32),
+                                           case["top_k"])
+        assert off.tolist() == [0, case["top_k"]], case["name"]
+        assert ids.tolist() == case["ids"], case["name"]
+        np.testing.assert_allclose(al, case["alpha"], rtol=1e-6, atol=1e-7, err_msg=case["name"])
+
+
+def test_gate_topk_against_full_softmax_and_stable_sort():
+    """Random padded candidate lists: the kept ids are those of a stable sort
+    on the negated logits (numpy), and alpha equals the explicit softmax over
+    all valid candidates divided by the kept mass (not the cancelled form the
+    oracle uses)."""
+    rng = np.random.default_rng(21)
+    T, E, k = 400, 8, 3
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[::7, 2] = logits[::7, 5]  # exact ties
+    cand = rng.integers(0, 50, size=(T, E)).astype(np.int32)
+    cand[rng.random((T, E)) < 0.2] = -1
+    off, ids, al, empty = oracle.gate_topk(logits, cand, k)
+    assert off.tolist() == [t * k for t in range(T + 1)]
+    n_empty = 0
+    for t in range(T):
+        valid = np.nonzero(cand[t] >= 0)[0]
+        if valid.size == 0:
+            n_empty += 1
+            assert ids[t * k:(t + 1) * k].tolist() == [-1] * k
+            continue
+        order = valid[np.argsort(-logits[t, valid].astype(np.float64), kind="stable")]
+        kept = order[:k]
+        p = np.exp(logits[t, valid].astype(np.float64))
+        p /= p.sum()
+        pk = np.exp(logits[t, kept].astype(np.float64)) / np.exp(logits[t, valid].astype(np.float64)).sum()
+        want_ids = list(cand[t, kept]) + [cand[t, kept[0]]] * (k - kept.size)
+        want_al = list(pk / pk.sum()) + [0.0] * (k - kept.size)
+        assert ids[t * k:(t + 1) * k].tolist() == want_ids
+        np.testing.assert_allclose(al[t * k:(t + 1) * k], want_al, rtol=2e-7, atol=1e-8)
+    assert empty == n_empty
+
+
+def test_gate_logits_against_einsum():
+    """The batched gate logits (a router per request) against numpy's einsum
+    on the same bf16 values."""
+    rng = np.random.default_rng(4)
+    T, E, d, R = 37, 8, 96, 3
+    x = W.f32_to_bf16_bits(rng.standard_normal((T, d)).astype(np.float32))
+    Wg = W.f32_to_bf16_bits(rng.standard_normal((R, E, d)).astype(np.float32) * 0.1)
+    req = rng.integers(0, R, size=T).astype(np.int32)
+    got = oracle.gate_logits(x, Wg, req)
+    xf = W.bf16_bits_to_f32(x).astype(np.float64)
+    wf = W.bf16_bits_to_f32(Wg).astype(np.float64)
+    want = np.einsum("td,ted->te", xf, wf[req])
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
