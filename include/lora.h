@@ -343,6 +343,42 @@ lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, const lora_
                                      int32_t *status_dev, lora_stream_t stream);
 
 /*
+ * MoE-LoRA gating on the device: the step before the mapping in the sparse
+ * (MoE-LoRA) scenario (DyMerge-LoRA page, MoE-LoRA scenario and code
+ * release notes, paper Sec. 5.3 and Appendix A: each token weights its
+ * request's adapters with a gate over padded, masked candidate lists, keeps
+ * the top-k and renormalises their softmax weights).  The outputs are the
+ * CSR pair lists lora_build_mapping takes, with P = T * top_k.
+ *
+ * lora_gate_logits: logits[t][e] = sum_d x[t][d] * Wg[req[t]][e][d]
+ *   x_dev      : device bf16 [T][d_in] (the tokens' hidden states)
+ *   wg_dev     : device bf16 [R][E][d_in], a router per request
+ *   req_dev    : device int32 [T], the request of each token, in [0, R)
+ *                (not checked: the caller's layout)
+ *   logits_dev : device fp32 [T][E] (written); fp32 accumulation
+ * d_in a multiple of 8, x and Wg 16-byte aligned.
+ *
+ * lora_gate_topk: per token, among the candidates e with cand[t][e] >= 0,
+ * the top_k by logit (largest first; equal logits: the lower e first), with
+ * alpha_i = exp(l_i - l_max) / sum over the kept of exp(l_j - l_max) -- the
+ * softmax over all candidates renormalised over the kept ones, whose full
+ * denominator cancels.
+ *   logits_dev : device fp32 [T][E];  cand_dev : device int32 [T][E]
+ *                (adapter id, or -1 for a padded slot)
+ *   offsets_dev: device int32 [T+1] = t * top_k
+ *   ids_dev, alpha_dev : device [T * top_k]; a token with fewer valid
+ *                candidates repeats its best one with alpha 0 (a no-op
+ *                pair); a token with none emits id -1 (which the mapping
+ *                leaves out, setting LORA_DEV_BAD_ID)
+ *   1 <= top_k <= min(E, 8), E <= 64 (else LORA_ERR_NOT_SUPPORTED).
+ * Both are stream-ordered and allocate nothing.
+ */
+lora_status lora_gate_logits(const void *x_dev, const void *wg_dev, const int32_t *req_dev, int T, int E, int d_in,
+                             float *logits_dev, lora_stream_t stream);
+lora_status lora_gate_topk(const float *logits_dev, const int32_t *cand_dev, int T, int E, int top_k,
+                           int32_t *offsets_dev, int32_t *ids_dev, float *alpha_dev, lora_stream_t stream);
+
+/*
  * lora_diag_wait_expiry: diagnostic.  Every on-chip wait of the library is
  * bounded; this launches one kernel whose single wait can never be
  * satisfied, so that the expiry path can be observed: the wait gives up

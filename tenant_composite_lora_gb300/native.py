@@ -47,7 +47,7 @@ EXPORTS = [
     "lora_dispatch_choose", "lora_delta_apply_host", "lora_mapping_status", "lora_mapping_export",
     "lora_mapping_destroy", "lora_status_string", "lora_version", "lora_delta_apply_noalloc",
     "lora_diag_wait_expiry", "lora_delta_apply_multi", "lora_ablation_workspace_bytes",
-    "lora_delta_apply_ablation",
+    "lora_delta_apply_ablation", "lora_gate_logits", "lora_gate_topk",
 ]
 
 LORA_ABLATION_NAIVE = 1
@@ -108,6 +108,8 @@ def load(path: str | None = None):
         "lora_delta_apply_multi": ([ctypes.POINTER(LoraProjection), I, V, V], I),
         "lora_ablation_workspace_bytes": ([I, I, I, I, I, I], ctypes.c_size_t),
         "lora_delta_apply_ablation": ([V, V, V, V, V, I, V, ctypes.c_size_t, V], I),
+        "lora_gate_logits": ([V, V, V, I, I, I, V, V], I),
+        "lora_gate_topk": ([V, V, I, I, I, V, V, V, V], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -253,6 +255,19 @@ def lora_delta_apply_ablation(x, y, pool: int, ranks, m: int, variant: int, work
            load().lora_delta_apply_ablation(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool,
                                             _dptr(ranks, "ranks", "int32"), m, variant, ws, workspace_bytes,
                                             _stream(stream)))
+
+
+def lora_gate_logits(x, wg, req, T: int, E: int, d_in: int, logits, stream=None):
+    _check("lora_gate_logits",
+           load().lora_gate_logits(_dptr(x, "x", "bf16"), _dptr(wg, "wg", "bf16"), _dptr(req, "req", "int32"), T, E,
+                                   d_in, _dptr(logits, "logits", "float32"), _stream(stream)))
+
+
+def lora_gate_topk(logits, cand, T: int, E: int, top_k: int, offsets, ids, alpha, stream=None):
+    _check("lora_gate_topk",
+           load().lora_gate_topk(_dptr(logits, "logits", "float32"), _dptr(cand, "cand", "int32"), T, E, top_k,
+                                 _dptr(offsets, "offsets", "int32"), _dptr(ids, "ids", "int32"),
+                                 _dptr(alpha, "alpha", "float32"), _stream(stream)))
 
 
 def lora_delta_apply_path(x, y, pool: int, ranks, m: int, path: int, stream=None):
