@@ -379,6 +379,48 @@ lora_status lora_gate_topk(const float *logits_dev, const int32_t *cand_dev, int
                            int32_t *offsets_dev, int32_t *ids_dev, float *alpha_dev, lora_stream_t stream);
 
 /*
+ * Batched recompression of a fleet of adapters (LoRAForge summary page,
+ * "Key contributions" and "Approach" (2)-(3): FlashTSQR factor construction
+ * and the two rank-allocation policies); it produces the sorted factor
+ * prefixes and retained ranks k_m that lora_pool_register takes.
+ *
+ * lora_recompress: for M modules of one shape, dW_m = A_m B_m, computes
+ * singular values sigma_m (descending) and balanced factors F_m, T_m with
+ * F_m T_m = A_m B_m, F_m^T F_m = T_m T_m^T = diag(sigma_m), and the first k
+ * directions equal to the rank-k truncated SVD -- via a tall-skinny QR of
+ * A_m (row tiles as independent leaf QRs, then level-wise merges of the
+ * triangular factors; Q is never formed), H = R B_m, and the
+ * eigen-decomposition of H H^T (fp32 throughout).  Directions with
+ * sigma^2 <= 1e-6 sigma_0^2 are dead: sigma 0, zero column / row.
+ *   A_dev     : device bf16 [M][d_in][r]  (the pool's A layout per adapter)
+ *   B_dev     : device bf16 [M][r][d_out]
+ *   F_dev     : device fp32 [M][d_in][r];  T_dev : device fp32 [M][r][d_out]
+ *   sigma_dev : device fp32 [M][r]
+ *   workspace_dev: device scratch of lora_recompress_workspace_bytes(M, d_in, r)
+ *   1 <= r <= LORA_MAX_RANK, r <= d_in.  Stream-ordered.
+ *
+ * lora_rank_allocate (host only): retained ranks k_m from the sigmas.
+ *   sigma_host : [M][r_stride], each row descending (zeros: dead directions)
+ *   rank_host  : original rank r_m;  cost_host : d_in + d_out of module m
+ *   LORA_RANK_UNIFORM  : k_m = min(max(1, floor(r_m / d)), live directions)
+ *                        (LoRAForge-U);
+ *   LORA_RANK_SPECTRAL : the uniform policy's parameter budget
+ *                        sum k_m cost_m spent greedily: every module keeps
+ *                        min(floor_k, live) directions, then directions are
+ *                        taken by sigma^2 / cost descending (ties: lower m,
+ *                        then lower j) while they extend their module's
+ *                        prefix and fit the budget (LoRAForge-S).
+ */
+#define LORA_RANK_UNIFORM 0
+#define LORA_RANK_SPECTRAL 1
+size_t lora_recompress_workspace_bytes(int M, int d_in, int r);
+lora_status lora_recompress(const void *A_dev, const void *B_dev, int M, int d_in, int d_out, int r, float *F_dev,
+                            float *T_dev, float *sigma_dev, void *workspace_dev, size_t workspace_bytes,
+                            lora_stream_t stream);
+lora_status lora_rank_allocate(const float *sigma_host, int M, int r_stride, const int32_t *rank_host,
+                               const int32_t *cost_host, int policy, int d, int floor_k, int32_t *k_host);
+
+/*
  * lora_diag_wait_expiry: diagnostic.  Every on-chip wait of the library is
  * bounded; this launches one kernel whose single wait can never be
  * satisfied, so that the expiry path can be observed: the wait gives up

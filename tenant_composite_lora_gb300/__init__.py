@@ -16,7 +16,8 @@ from .native import (LoraError, lora_build_mapping, lora_delta_apply, lora_delta
                      lora_mapping_destroy, lora_mapping_export, lora_mapping_status,
                      lora_pool_create, lora_pool_destroy, lora_pool_register,
                      lora_pool_unregister, lora_version, lora_diag_wait_expiry, lora_delta_apply_multi,
-                     lora_ablation_workspace_bytes, lora_delta_apply_ablation, lora_gate_logits, lora_gate_topk)
+                     lora_ablation_workspace_bytes, lora_delta_apply_ablation, lora_gate_logits, lora_gate_topk,
+                     lora_recompress_workspace_bytes, lora_recompress, lora_rank_allocate)
 
 __all__ = [
     "native", "LoraError", "LoraPool", "LoraMapping", "delta_apply",
@@ -25,7 +26,8 @@ __all__ = [
     "lora_dispatch_choose", "lora_delta_apply_host", "lora_mapping_status", "lora_mapping_export",
     "lora_mapping_destroy", "lora_version", "lora_delta_apply_noalloc", "lora_diag_wait_expiry",
     "lora_delta_apply_multi", "lora_ablation_workspace_bytes", "lora_delta_apply_ablation",
-    "lora_gate_logits", "lora_gate_topk",
+    "lora_gate_logits", "lora_gate_topk", "lora_recompress_workspace_bytes", "lora_recompress",
+    "lora_rank_allocate",
 ]
 
 

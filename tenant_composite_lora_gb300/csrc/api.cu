@@ -619,6 +619,45 @@ lora_status lora_delta_apply_ablation(const void *x_dev, void *y_dev, const lora
                                   static_cast<cudaStream_t>(stream)));
 }
 
+size_t lora_recompress_workspace_bytes(int M, int d_in, int r)
+{
+    if (M < 1 || r < 1 || r > LORA_MAX_RANK || d_in < r)
+        return 0;
+    return recompress_workspace_bytes(M, d_in, r);
+}
+
+lora_status lora_recompress(const void *A_dev, const void *B_dev, int M, int d_in, int d_out, int r, float *F_dev,
+                            float *T_dev, float *sigma_dev, void *workspace_dev, size_t workspace_bytes,
+                            lora_stream_t stream)
+{
+    if (!A_dev || !B_dev || !F_dev || !T_dev || !sigma_dev || !workspace_dev || M < 0 || d_in < 1 || d_out < 1)
+        return LORA_ERR_INVALID_ARG;
+    if (r < 1 || r > LORA_MAX_RANK || d_in < r)
+        return LORA_ERR_NOT_SUPPORTED;
+    if (M == 0)
+        return LORA_OK;
+    if (workspace_bytes < recompress_workspace_bytes(M, d_in, r) || !aligned16(workspace_dev))
+        return LORA_ERR_INVALID_ARG;
+    const cudaError_t e =
+        launch_recompress(static_cast<const __nv_bfloat16 *>(A_dev), static_cast<const __nv_bfloat16 *>(B_dev), M,
+                          d_in, d_out, r, F_dev, T_dev, sigma_dev, workspace_dev, static_cast<cudaStream_t>(stream));
+    return e == cudaErrorNotSupported ? LORA_ERR_NOT_SUPPORTED : from_cuda(e);
+}
+
+lora_status lora_rank_allocate(const float *sigma_host, int M, int r_stride, const int32_t *rank_host,
+                               const int32_t *cost_host, int policy, int d, int floor_k, int32_t *k_host)
+{
+    if (!sigma_host || !rank_host || !cost_host || !k_host || M < 0 || r_stride < 1 || d < 1 || floor_k < 0)
+        return LORA_ERR_INVALID_ARG;
+    if (policy != LORA_RANK_UNIFORM && policy != LORA_RANK_SPECTRAL)
+        return LORA_ERR_NOT_SUPPORTED;
+    for (int m = 0; m < M; ++m)
+        if (cost_host[m] < 1 || rank_host[m] < 0)
+            return LORA_ERR_INVALID_ARG;
+    rank_allocate(sigma_host, M, r_stride, rank_host, cost_host, policy, d, floor_k, k_host);
+    return LORA_OK;
+}
+
 lora_status lora_delta_apply_multi(const lora_projection *projs, int n_proj, const lora_mapping *m,
                                    lora_stream_t stream)
 {

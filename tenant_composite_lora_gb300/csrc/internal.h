@@ -153,6 +153,12 @@ cudaError_t launch_decode_multi(const MultiDecArgs &a, int P, cudaStream_t st);
 size_t ablation_workspace_bytes(int variant, int T, int P, int d_in, int d_out, int r_max);
 cudaError_t run_ablation(int variant, const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool,
                          const int32_t *ranks, const MapDev &m, int T, int P, void *ws, cudaStream_t st);
+// Batched recompression (FlashTSQR factor construction) and rank policies.
+size_t recompress_workspace_bytes(int M, int d_in, int r);
+cudaError_t launch_recompress(const __nv_bfloat16 *A, const __nv_bfloat16 *B, int M, int d_in, int d_out, int r,
+                              float *F, float *Tout, float *sigma, void *ws, cudaStream_t st);
+int rank_allocate(const float *sigma, int M, int r_stride, const int32_t *rank, const int32_t *cost, int policy,
+                  int d, int floor_k, int32_t *k_out);
 // Dispatch: batches of at most this many tokens take the decode path.
 constexpr int DECODE_MAX_TOKENS = 256;
 // The same decode work as one cooperative launch (a CTA per SM): shrink

@@ -47,8 +47,12 @@ EXPORTS = [
     "lora_dispatch_choose", "lora_delta_apply_host", "lora_mapping_status", "lora_mapping_export",
     "lora_mapping_destroy", "lora_status_string", "lora_version", "lora_delta_apply_noalloc",
     "lora_diag_wait_expiry", "lora_delta_apply_multi", "lora_ablation_workspace_bytes",
-    "lora_delta_apply_ablation", "lora_gate_logits", "lora_gate_topk",
+    "lora_delta_apply_ablation", "lora_gate_logits", "lora_gate_topk", "lora_recompress_workspace_bytes",
+    "lora_recompress", "lora_rank_allocate",
 ]
+
+LORA_RANK_UNIFORM = 0
+LORA_RANK_SPECTRAL = 1
 
 LORA_ABLATION_NAIVE = 1
 LORA_ABLATION_COPY_SGMV = 2
@@ -110,6 +114,9 @@ def load(path: str | None = None):
         "lora_delta_apply_ablation": ([V, V, V, V, V, I, V, ctypes.c_size_t, V], I),
         "lora_gate_logits": ([V, V, V, I, I, I, V, V], I),
         "lora_gate_topk": ([V, V, I, I, I, V, V, V, V], I),
+        "lora_recompress_workspace_bytes": ([I, I, I], ctypes.c_size_t),
+        "lora_recompress": ([V, V, I, I, I, I, V, V, V, V, ctypes.c_size_t, V], I),
+        "lora_rank_allocate": ([V, I, I, V, V, I, I, I, V], I),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -268,6 +275,38 @@ def lora_gate_topk(logits, cand, T: int, E: int, top_k: int, offsets, ids, alpha
            load().lora_gate_topk(_dptr(logits, "logits", "float32"), _dptr(cand, "cand", "int32"), T, E, top_k,
                                  _dptr(offsets, "offsets", "int32"), _dptr(ids, "ids", "int32"),
                                  _dptr(alpha, "alpha", "float32"), _stream(stream)))
+
+
+def lora_recompress_workspace_bytes(M: int, d_in: int, r: int) -> int:
+    return int(load().lora_recompress_workspace_bytes(M, d_in, r))
+
+
+def lora_recompress(A, B, M: int, d_in: int, d_out: int, r: int, F, T, sigma, workspace, workspace_bytes: int,
+                    stream=None):
+    """A bf16 [M, d_in, r], B bf16 [M, r, d_out] (CUDA); F fp32 [M, d_in, r],
+    T fp32 [M, r, d_out], sigma fp32 [M, r] written; workspace a CUDA byte
+    buffer of lora_recompress_workspace_bytes(M, d_in, r)."""
+    if workspace is not None and not isinstance(workspace, int) and not workspace.is_cuda:
+        raise ValueError("workspace: a CUDA tensor is expected")
+    ws = workspace if workspace is None or isinstance(workspace, int) else workspace.data_ptr()
+    _check("lora_recompress",
+           load().lora_recompress(_dptr(A, "A", "bf16"), _dptr(B, "B", "bf16"), M, d_in, d_out, r,
+                                  _dptr(F, "F", "float32"), _dptr(T, "T", "float32"), _dptr(sigma, "sigma", "float32"),
+                                  ws, workspace_bytes, _stream(stream)))
+
+
+def lora_rank_allocate(sigma, rank, cost, policy: int, d: int, floor_k: int = 1) -> np.ndarray:
+    """Host only: sigma float32 [M, r], rank and cost int32 [M] (numpy);
+    returns the retained ranks k [M]."""
+    sigma = np.ascontiguousarray(sigma, np.float32)
+    rank = np.ascontiguousarray(rank, np.int32)
+    cost = np.ascontiguousarray(cost, np.int32)
+    M, r = sigma.shape
+    k = np.zeros(M, np.int32)
+    _check("lora_rank_allocate",
+           load().lora_rank_allocate(sigma.ctypes.data, M, r, rank.ctypes.data, cost.ctypes.data, policy, d, floor_k,
+                                     k.ctypes.data))
+    return k
 
 
 def lora_delta_apply_path(x, y, pool: int, ranks, m: int, path: int, stream=None):

@@ -263,3 +263,30 @@ def test_noalloc_binding_checks_sizes_before_the_library():
     # everything consistent: the size checks pass and the memory check refuses the host tensors
     with pytest.raises(ValueError, match="x: a CUDA tensor is expected"):
         call(ranks=torch.zeros(8, dtype=torch.int32))
+
+
+def test_rank_allocate_matches_the_oracle(lib):
+    """lora_rank_allocate (host code of the library) against the oracle's
+    policies: the worked example and random fleets with mixed shapes."""
+    import json
+    import numpy as np
+    from oracle import recompress as RC
+    from tenant_composite_lora_gb300 import native
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "rank_allocation_example.json")))
+    sig = np.array(g["sigma"], np.float32)
+    for pol, key in ((native.LORA_RANK_UNIFORM, "U"), (native.LORA_RANK_SPECTRAL, "S")):
+        k = native.lora_rank_allocate(sig, g["rank"], g["cost"], pol, g["d"], g["floor"])
+        assert k.tolist() == g[key]
+    rng = np.random.default_rng(6)
+    for trial in range(20):
+        M, r = int(rng.integers(1, 30)), 16
+        sig = np.sort(rng.random((M, r)).astype(np.float32) ** 3, axis=1)[:, ::-1].copy()
+        sig[rng.random((M, r)) < 0.1] = 0
+        sig = np.sort(sig, axis=1)[:, ::-1].copy()
+        rank = rng.integers(1, r + 1, size=M).astype(np.int32)
+        cost = rng.choice([5120, 8192, 18432], size=M).astype(np.int32)
+        d, fl = int(rng.integers(1, 9)), int(rng.integers(0, 3))
+        for pol, key in ((native.LORA_RANK_UNIFORM, "U"), (native.LORA_RANK_SPECTRAL, "S")):
+            got = native.lora_rank_allocate(sig, rank, cost, pol, d, fl)
+            want = RC.rank_allocate(list(sig.astype(np.float64)), cost, rank, key, d, fl)
+            assert got.tolist() == want, (trial, key)
