@@ -1,8 +1,9 @@
 """Benchmark of the composite multi-LoRA delta on GB300.
 
-One step = one pass of the whole hot path over one batch: build the
-adapter-ordered mapping from the batch's per-token pair lists, then apply the
-fused delta y += sum alpha (x A[:, :k]) B[:k, :] through the C ABI.
+One step = one pass of the whole hot path over one batch: build the mapping
+from the batch's per-token pair lists (its CSR copy; the adapter-ordered
+tuples too where the path reads them), then apply the fused delta
+y += sum alpha (x A[:, :k]) B[:k, :] through the C ABI.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
 
@@ -45,11 +46,13 @@ CONFIG_NAMES = {
     "sweep256": "rank sweep k_i~U{1..64}, k/v_proj 4096->1024, r_max=64, pool 1000, T=256",
 }
 PATH_NAMES = {0: "auto", 1: "split", 2: "fused", 3: "mma", 4: "decode"}
-# kernels of lora_delta_apply per path (the mapping kernel adds one launch per step)
+# kernels of lora_delta_apply per path (the mapping's CSR stage adds one
+# launch per step; the paths that read the adapter-sorted tuples launch the
+# sort stage first, which returns at once when the build is sorted already)
 PATH_KERNELS = {
-    "split": (2, "k_shrink + k_expand (PDL)"),
-    "fused": (1, "k_fused (cooperative, one launch)"),
-    "mma": (2, "k_mma_shrink + k_mma_expand (tcgen05, PDL)"),
+    "split": (3, "k_map_sort + k_shrink + k_expand (PDL)"),
+    "fused": (1, "k_dec_fused (cooperative, one launch)"),
+    "mma": (3, "k_map_sort + k_mma_shrink + k_mma_expand (tcgen05, PDL)"),
     "decode": (2, "k_dec_shrink + k_dec_expand (PDL)"),
 }
 
@@ -704,6 +707,92 @@ def recompress_lines(torch, stream, dev):
                        "(LoRAForge page, Sec. 6.3); random synthetic factors here"}
 
 
+# Dispatch sweep: batches of T tokens with two pairs each, grouped into
+# requests of `share` consecutive tokens that use the same two adapters of
+# their own (share = 1: every token its own adapters, as in a decode batch;
+# larger: prompt-like runs), or two distinct Zipf(1.5) draws over 128
+# adapters per token ("zipf"); q_proj shape, every rank r_max.
+SWEEP_T = [16, 64, 128, 256, 384, 512, 1024, 2048, 4096]
+SWEEP_R = [8, 16, 64]
+SWEEP_SHARE = ["1", "16", "256", "zipf"]
+SWEEP_PATHS = {"decode": 4, "split": 1, "mma": 3}
+SWEEP_CAPACITY = 4096
+
+
+def sweep_ids(T: int, share: str, rng) -> np.ndarray:
+    """Adapter ids [T, 2] of the sweep's batch."""
+    if share == "zipf":
+        w = 1.0 / np.arange(1, 129) ** 1.5
+        w /= w.sum()
+        return np.stack([rng.choice(128, size=2, replace=False, p=w) for _ in range(T)]).astype(np.int32)
+    s = int(share)
+    req = np.arange(T) // s
+    return (np.stack([2 * req, 2 * req + 1], axis=1) % SWEEP_CAPACITY).astype(np.int32)
+
+
+def dispatch_sweep(torch, stream, dev) -> dict:
+    """apply (and build + apply) time of every path on every sweep point,
+    cold L2, with the dispatch table's own pick beside the fastest."""
+    import tenant_composite_lora_gb300 as tcl
+    from tenant_composite_lora_gb300 import native
+    timer = ColdTimer(torch, stream, dev)
+    d_in = d_out = 4096
+    rng = np.random.default_rng(11)
+    g = torch.Generator(device=dev).manual_seed(3)
+    tmax = max(SWEEP_T)
+    points = []
+    with torch.cuda.stream(stream):
+        x = (torch.randn(tmax, d_in, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        y = torch.zeros(tmax, d_out, dtype=torch.bfloat16, device=dev)
+        for r in SWEEP_R:
+            pool = tcl.LoraPool(d_in, d_out, r, SWEEP_CAPACITY)
+            A = (torch.randn(d_in, r, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+            B = (torch.randn(r, d_out, device=dev, generator=g) * 0.02).to(torch.bfloat16)
+            for a in range(SWEEP_CAPACITY):
+                pool.register(a, A, B, r, stream)
+            try:
+                for T in SWEEP_T:
+                    for share in SWEEP_SHARE:
+                        ids = sweep_ids(T, share, rng)
+                        P = 2 * T
+                        off = torch.arange(0, P + 1, 2, dtype=torch.int32, device=dev)
+                        ids_d = torch.from_numpy(ids.reshape(-1)).to(dev)
+                        al_d = torch.full((P,), 0.5, dtype=torch.float32, device=dev)
+                        m = tcl.LoraMapping(T, P, SWEEP_CAPACITY)
+                        xs, ys = x[:T], y[:T]
+                        pt = {"T": T, "r": r, "share": share, "P": P, "U": int(np.unique(ids).size)}
+                        try:
+                            m.build(off, ids_d, al_d, stream)
+                            for name, pid in SWEEP_PATHS.items():
+                                def apply_(pid=pid):
+                                    native.lora_delta_apply_path(xs, ys, pool.handle, None, m.handle, pid, stream)
+
+                                def step_(pid=pid):
+                                    native.lora_build_mapping(m.handle, off, ids_d, al_d, T, P, stream)
+                                    native.lora_delta_apply_path(xs, ys, pool.handle, None, m.handle, pid, stream)
+                                try:
+                                    apply_()
+                                    stream.synchronize()
+                                except Exception as exc:  # a path that does not take this shape
+                                    pt[name] = None
+                                    pt[name + "_error"] = type(exc).__name__
+                                    continue
+                                n = 100 if T <= 512 else 30
+                                pt[name] = round(timer.time_us(apply_, n), 2)
+                                pt[name + "_step"] = round(timer.time_us(step_, n), 2)
+                        finally:
+                            m.close()
+                        timed = {k: pt[k] for k in SWEEP_PATHS if pt.get(k) is not None}
+                        pt["fastest"] = min(timed, key=timed.get)
+                        pt["chosen"] = PATH_NAMES[native.lora_dispatch_choose(T, P, r, d_in, d_out)]
+                        points.append(pt)
+            finally:
+                pool.close()
+    return {"shape": f"{d_in}x{d_out}", "pairs_per_token": 2, "capacity": SWEEP_CAPACITY,
+            "protocol": "cold L2 (256 MB read before every replay, its time subtracted); us per call",
+            "points": points}
+
+
 def cpu_model() -> str:
     """The host CPU's name as the OS reports it ("unknown" when it does not)."""
     try:
@@ -812,6 +901,8 @@ def main():
                     help="skip the per-config, ablation and multi-projection figures")
     ap.add_argument("--path", default="auto", choices=["auto", "split", "fused", "mma", "decode"],
                     help="force an execution path (default: the library's dispatch table)")
+    ap.add_argument("--dispatch-sweep", action="store_true",
+                    help="time every path over tokens x rank x adapter sharing and print that table instead")
     args = ap.parse_args()
     args.path_id = {"auto": 0, "split": 1, "fused": 2, "mma": 3, "decode": 4}[args.path]
     args.warmup = max(3, args.warmup)
@@ -820,6 +911,13 @@ def main():
         # the CPU oracle needs no process group: rank 0 alone runs and prints
         if int(os.environ.get("RANK", "0")) == 0:
             print(json.dumps(bench_reference(args)))
+        return
+
+    if args.dispatch_sweep:
+        import torch
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        print(json.dumps(dispatch_sweep(torch, torch.cuda.Stream(device=dev), dev)))
         return
 
     rank, world, dist = dist_setup(args.gpus)

@@ -155,6 +155,14 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
  * ascending order with their segment starts.  Pairs with an id outside
  * [0, capacity) are left out and set LORA_DEV_BAD_ID; malformed offsets give
  * an empty mapping and set LORA_DEV_BAD_OFFSETS.  Clears the status word.
+ * This call enqueues one kernel that copies the batch into the mapping in
+ * CSR order (token, adapter, alpha per pair) and checks it; the decode path
+ * reads only that copy.  The sorted tuples are produced from the copy by a
+ * second kernel that the first apply needing them (the split, tensor-core
+ * and fused paths, the ablation variants that use them, and
+ * lora_mapping_export) enqueues before its own kernels; later calls on the
+ * same build find them there (a device-side build counter decides, so this
+ * also holds inside CUDA graphs).
  * One mapping serves every lora_delta_apply on the same batch (all
  * projections and layers).  The input arrays need to stay valid only until
  * the stream reaches this call.
@@ -288,7 +296,8 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
 lora_status lora_mapping_status(const lora_mapping *m, lora_stream_t stream, int *device_error);
 
 /*
- * lora_mapping_export: synchronise `stream` and copy the mapping into HOST
+ * lora_mapping_export: sort the mapping's current build if no apply has yet
+ * (on `stream`), synchronise `stream` and copy the mapping into HOST
  * buffers (for checking it; any pointer may be NULL to skip that array):
  *   tok, adapter, alpha, src : [P_valid]   the ordered tuples
  *   pos                      : [P]         inverse permutation (-1 = left out)

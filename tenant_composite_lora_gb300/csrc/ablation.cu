@@ -133,7 +133,7 @@ __global__ void k_ab_scatter(__nv_bfloat16 *y, MapDev m, int T, int d_out, const
         const int t = (int)(i / d_out), c = (int)(i % d_out);
         float acc = __bfloat162float(y[i]);
         for (int p = m.toff[t]; p < m.toff[t + 1]; ++p) {
-            const int q = m.pq[p].x;
+            const int q = m.pos[p];
             if (q >= 0)
                 acc += ys[(size_t)q * d_out + c];
         }
@@ -155,11 +155,11 @@ __global__ void k_ab_merge(PoolDev pool, const int32_t *ranks, MapDev m, int T, 
     for (int r = 0; r < 16; ++r)
         acc[r] = 0.f;
     for (int p = m.toff[t]; p < m.toff[t + 1]; ++p) {
-        const int2 v = m.pq[p];
-        if (v.x < 0)
+        const int2 v = m.pc[p];  // {token, adapter}
+        if (v.y < 0)
             continue;
         const int k = effective_rank(pool, ranks, v.y);
-        const float al = m.alpha[v.x];
+        const float al = m.calpha[p];
         for (int j = 0; j < k; ++j) {
             const float b = al * __bfloat162float(pool.B[((size_t)v.y * pool.r_max + j) * pool.d_out + c]);
             const __nv_bfloat16 *ac = pool.At + ((size_t)v.y * pool.r_max + j) * pool.d_in + i0;
@@ -229,10 +229,14 @@ cudaError_t run_ablation(int variant, const __nv_bfloat16 *x, __nv_bfloat16 *y, 
         k_ab_premerge_apply<<<ag, AB_THREADS, 0, st>>>(x, y, T, pool.d_in, pool.d_out, dw);
         return cudaGetLastError();
     }
-    // both other variants need the number of valid pairs, and the naive loop
-    // its segments, on the host: read them back (this synchronises the stream)
+    // both other variants work on the adapter-sorted tuples; they need the
+    // number of valid pairs, and the naive loop its segments, on the host:
+    // read them back (this synchronises the stream)
+    cudaError_t e = launch_map_sort(m, T, P, pool.capacity, st);
+    if (e != cudaSuccess)
+        return e;
     int32_t hdr[HDR_WORDS];
-    cudaError_t e = cudaMemcpyAsync(hdr, m.hdr, sizeof hdr, cudaMemcpyDeviceToHost, st);
+    e = cudaMemcpyAsync(hdr, m.hdr, sizeof hdr, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(st);
     if (e != cudaSuccess)

@@ -258,7 +258,7 @@ void free_mapping(lora_mapping *m)
         cudaGraphExecDestroy(m->exec);
     MapDev &d = m->dev;
     void *ptrs[] = {d.tok,  d.adapter, d.src, d.pos,     d.alpha, d.seg_adapter, d.seg_start,
-                    d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.pq, d.zcnt, d.z,
+                    d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.pc, d.calpha, d.zcnt, d.z,
                     d.partial, d.ghist, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
@@ -319,6 +319,13 @@ ExpandPlan choose_expand_plan(int T, int d_out)
     return best;
 }
 
+// The adapter-sorted tuples of the mapping's current build (the sort stage
+// returns at once when they are there already).
+cudaError_t sort_mapping(const lora_mapping *m, cudaStream_t st)
+{
+    return launch_map_sort(m->dev, m->T, m->P, m->capacity, st);
+}
+
 lora_status run_fused(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
                       cudaStream_t st)
 {
@@ -332,7 +339,10 @@ lora_status run_fused(const void *x, void *y, const lora_pool *pool, const int32
     if (!fused_supported(m->T, pool->d_out))
         return LORA_ERR_NOT_SUPPORTED;
     const ExpandPlan plan = choose_expand_plan(m->T, pool->d_out);
-    const cudaError_t e = launch_fused(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
+    cudaError_t e = sort_mapping(m, st);
+    if (e != cudaSuccess)
+        return from_cuda(e);
+    e = launch_fused(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
                                        pool_dev(pool), ranks, m->dev, m->T, m->P, plan, sm_count(), st);
     if (e == cudaErrorNotSupported)
         return LORA_ERR_NOT_SUPPORTED;  // the shape does not fit this kernel
@@ -344,7 +354,10 @@ lora_status run_mma(const void *x, void *y, const lora_pool *pool, const int32_t
 {
     if (!pool->maps.ready || !mma_supported(pool->d_in, pool->d_out, pool->r_max))
         return LORA_ERR_NOT_SUPPORTED;
-    const cudaError_t e = launch_mma(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
+    cudaError_t e = sort_mapping(m, st);
+    if (e != cudaSuccess)
+        return from_cuda(e);
+    e = launch_mma(static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(y),
                                      pool_dev(pool), pool->maps, ranks, m->dev, m->T, m->P, st);
     if (e == cudaErrorNotSupported)
         return LORA_ERR_NOT_SUPPORTED;
@@ -366,8 +379,9 @@ lora_status run_split(const void *x, void *y, const lora_pool *pool, const int32
 {
     const PoolDev pd = pool_dev(pool);
     const int grid = sm_count();
-    cudaError_t e =
-        launch_shrink(static_cast<const __nv_bfloat16 *>(x), pd, ranks, m->dev, m->P, grid, st);
+    cudaError_t e = sort_mapping(m, st);
+    if (e == cudaSuccess)
+        e = launch_shrink(static_cast<const __nv_bfloat16 *>(x), pd, ranks, m->dev, m->P, grid, st);
     if (e != cudaSuccess)
         return from_cuda(e);
     const ExpandPlan plan = choose_expand_plan(m->T, pool->d_out);
@@ -523,7 +537,8 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.hdr, (size_t)HDR_WORDS);
     if (e == cudaSuccess) e = dalloc(&d.mtile, (size_t)mma_tile_bound(max_pairs, capacity));
     if (e == cudaSuccess) e = dalloc(&d.toff, (size_t)max_tokens + 1);
-    if (e == cudaSuccess) e = dalloc(&d.pq, P);
+    if (e == cudaSuccess) e = dalloc(&d.pc, P);
+    if (e == cudaSuccess) e = dalloc(&d.calpha, P);
     if (e == cudaSuccess) e = dalloc(&d.zcnt, P);
     if (e == cudaSuccess) e = dalloc(&d.z, P * Z_ROW_FLOATS);
     d.partial_ctas = sm_count();
@@ -548,8 +563,10 @@ lora_status lora_build_mapping(lora_mapping *m, const int32_t *offsets_dev, cons
         return LORA_ERR_INVALID_ARG;
     if (P > 0 && (!ids_dev || !alpha_dev))
         return LORA_ERR_INVALID_ARG;
-    cudaError_t e = launch_build_mapping(m->dev, offsets_dev, ids_dev, alpha_dev, T, P, m->capacity, m->max_pairs,
-                                         static_cast<cudaStream_t>(stream));
+    // the CSR stage only: the paths that read the adapter-sorted tuples sort
+    // them first (once per build)
+    cudaError_t e = launch_map_csr(m->dev, offsets_dev, ids_dev, alpha_dev, T, P, m->capacity,
+                                   static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
         return from_cuda(e);
     m->T = T;
@@ -903,8 +920,10 @@ lora_status lora_mapping_export(const lora_mapping *m, lora_stream_t stream, int
     if (!m)
         return LORA_ERR_INVALID_ARG;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = m->built ? sort_mapping(m, st) : cudaSuccess;
     int32_t hdr[HDR_WORDS];
-    cudaError_t e = cudaMemcpyAsync(hdr, m->dev.hdr, sizeof hdr, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(hdr, m->dev.hdr, sizeof hdr, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess)
         e = cudaStreamSynchronize(st);
     if (e != cudaSuccess)
@@ -950,8 +969,8 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
 
 struct NoallocLayout {
-    size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, pq, zcnt,
-        z, ghist;
+    size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, pc, calpha,
+        zcnt, z, ghist;
     size_t total;
 };
 
@@ -980,7 +999,8 @@ NoallocLayout noalloc_layout(int T, int P, int capacity, int r_max)
     L.hdr = take(4 * (size_t)HDR_WORDS);
     L.mtile = take(16 * mtiles);
     L.toff = take(4 * ((size_t)T + 1));
-    L.pq = take(8 * p);
+    L.pc = take(8 * p);
+    L.calpha = take(4 * p);
     L.zcnt = take(4 * p);
     L.z = take(4 * p * (size_t)z_stride(r_max));
     L.ghist = take(4 * (size_t)map_global_hist_words(capacity));
@@ -1044,7 +1064,8 @@ extern "C" lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, 
     d.hdr = reinterpret_cast<int32_t *>(base + L.hdr);
     d.mtile = reinterpret_cast<int4 *>(base + L.mtile);
     d.toff = reinterpret_cast<int32_t *>(base + L.toff);
-    d.pq = reinterpret_cast<int2 *>(base + L.pq);
+    d.pc = reinterpret_cast<int2 *>(base + L.pc);
+    d.calpha = reinterpret_cast<float *>(base + L.calpha);
     d.zcnt = reinterpret_cast<int32_t *>(base + L.zcnt);
     d.z = reinterpret_cast<float *>(base + L.z);
     d.ghist = map_global_hist_words(pool->capacity) > 0 ? reinterpret_cast<int32_t *>(base + L.ghist) : nullptr;

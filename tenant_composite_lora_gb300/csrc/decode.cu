@@ -2,9 +2,14 @@
 // adapters' factors are read once.  Two launches chained with programmatic
 // dependent launch, every global access a 16-byte coalesced vector:
 //
+// Pairs are taken in CSR order (the mapping's CSR stage: per pair its token,
+// adapter and alpha), so neither kernel needs the adapter-sorted tuples: each
+// pair reads its own A rows here, and the sort only pays off where many
+// tokens share an adapter segment (the split and tensor-core paths).
+//
 // 1. Shrink (LoRAForge page, "Approach" (4): direct reduction for short
 //    decode batches; DyMerge-LoRA page, "Core idea": the weight alpha folded
-//    in).  A CTA owns one sorted pair q and 4 or 8 consecutive rank rows; its x row
+//    in).  A CTA owns one pair q and 4 or 8 consecutive rank rows; its x row
 //    is staged once in shared memory and each warp streams one row of A_a
 //    (stored transposed, contiguous along d_in) against it, reducing with
 //    warp shuffles:  z[q][j] = alpha_q * sum_d x[tok_q][d] * A_a[d][j].
@@ -25,7 +30,9 @@
 // dependent of the mapping kernel (its CTAs are resident when the mapping
 // ends) and releases the expand only once its own wait has returned, since
 // the expand's prologue reads the mapping and y; the expand lets the next
-// kernel in the stream start early (that kernel waits before it writes).
+// kernel in the stream start early (that kernel waits before it writes), and
+// every expand warp waits on the shrink before it exits, so that the expand
+// completes only after the shrink.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -40,8 +47,8 @@ struct DecShrinkArgs {
     PoolDev pool;
     const int32_t *ranks;
     MapDev m;
-    int zs;    // z row stride (floats per sorted pair)
-    float *z;  // this projection's first z column: z[q * zs + j]
+    int zs;    // z row stride (floats per pair)
+    float *z;  // this projection's first z column: z[q * zs + j], q the CSR pair
 };
 
 __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
@@ -57,16 +64,16 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
     return acc;
 }
 
-// One shrink item: pair q, rank rows [j0, j0 + warps of the CTA).  Every
+// One shrink item: CSR pair q, rank rows [j0, j0 + warps of the CTA).  Every
 // thread of the CTA calls it; it returns once the CTA's copies have landed.
 // report: set the status bit of an unusable adapter (one item per pair does).
 __device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *xs, int q, int j0, bool report)
 {
-    // one round trip: the pair (its adapter is used only once q is known valid)
-    const int pvalid = a.m.hdr[HDR_PVALID];
-    const int ad = a.m.adapter[q], tk = a.m.tok[q];
-    const float al = a.m.alpha[q];
-    if (q >= pvalid)
+    // one round trip: the pair's token and adapter, and its alpha
+    const int2 pc = a.m.pc[q];
+    const float al = a.m.calpha[q];
+    const int tk = pc.x, ad = pc.y;
+    if (ad < 0)
         return;  // pairs left out of the mapping (and every pair when its offsets were malformed)
     const int r_max = a.pool.r_max;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -152,7 +159,7 @@ struct DecExpandArgs {
     const int32_t *ranks;
     MapDev m;
     int T, zs, nc;  // nc: 256-column chunks per row (the last may be partial)
-    const float *z; // the shrink's output for this projection: z[q * zs + j]
+    const float *z; // the shrink's output for this projection: z[q * zs + j], q the CSR pair
 };
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float z, uint4 b)
@@ -212,24 +219,23 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
     const int d_out = a.pool.d_out, r_max = a.pool.r_max;
     const int col = c * 256 + lane * 8;
     const bool on = col < d_out;  // the last chunk of a row may be partial
-    // round trip 1: y, the token's pair range, the batch's validity
+    // round trip 1: y, the token's pair range
     __nv_bfloat16 *yp = a.y + (size_t)t * d_out + (on ? col : 0);
     const uint4 yv = on ? *reinterpret_cast<const uint4 *>(yp) : make_uint4(0u, 0u, 0u, 0u);
-    const int pvalid = a.m.hdr[HDR_PVALID];
     const int p0 = a.m.toff[t], p1 = a.m.toff[t + 1];
-    if (pvalid == 0)
-        return;  // nothing valid (also: offsets malformed, the pair range is not defined)
-    // round trip 2: {sorted position, adapter} of the first pairs
-    int2 pq[PP];
+    if (p1 <= p0)
+        return;  // no pair: y stays as it is (every token when the offsets were malformed)
+    // round trip 2: the adapters of the first pairs
+    int pa[PP];
 #pragma unroll
     for (int i = 0; i < PP; ++i)
-        pq[i] = p0 + i < p1 ? a.m.pq[p0 + i] : make_int2(-1, -1);
+        pa[i] = p0 + i < p1 ? a.m.pc[p0 + i].y : -1;
     // round trip 3: their first B rows (whatever the rank turns out to be) and ranks
     uint4 bpre[PP][DE_PR];
     int kk[PP];
 #pragma unroll
     for (int i = 0; i < PP; ++i) {
-        const int ad = pq[i].y;
+        const int ad = pa[i];
         const __nv_bfloat16 *br = a.pool.B + (size_t)(ad < 0 ? 0 : ad) * r_max * d_out + col;
 #pragma unroll
         for (int j = 0; j < DE_PR; ++j)
@@ -242,8 +248,8 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
     for (int i = 0; i < PP; ++i) {
         const int k = kk[i];
         if (k > 0) {
-            wait_pair(pq[i].x);
-            const float *zr = a.z + (size_t)pq[i].x * a.zs;
+            wait_pair(p0 + i);
+            const float *zr = a.z + (size_t)(p0 + i) * a.zs;
             float zz[DE_PR];
 #pragma unroll
             for (int j = 0; j < DE_PR; ++j)
@@ -252,18 +258,17 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
             for (int j = 0; j < DE_PR; ++j)
                 fma8(acc, zz[j], bpre[i][j]);
             if (k > DE_PR)
-                dec_rows(acc, a.pool.B + (size_t)pq[i].y * r_max * d_out + col, zr, DE_PR, k, d_out, on);
+                dec_rows(acc, a.pool.B + (size_t)pa[i] * r_max * d_out + col, zr, DE_PR, k, d_out, on);
         }
     }
     for (int p = p0 + PP; p < p1; ++p) {
-        const int2 v = a.m.pq[p];
-        if (v.y < 0)
+        const int ad = a.m.pc[p].y;
+        if (ad < 0)
             continue;
-        const int k = dec_rank(a.pool, a.ranks, v.y);
+        const int k = dec_rank(a.pool, a.ranks, ad);
         if (k > 0) {
-            wait_pair(v.x);
-            dec_rows(acc, a.pool.B + (size_t)v.y * r_max * d_out + col, a.z + (size_t)v.x * a.zs, 0, k, d_out,
-                     on);
+            wait_pair(p);
+            dec_rows(acc, a.pool.B + (size_t)ad * r_max * d_out + col, a.z + (size_t)p * a.zs, 0, k, d_out, on);
         }
     }
     uint4 o;
@@ -294,6 +299,8 @@ __global__ void __launch_bounds__(256, MINB) k_dec_expand(const DecExpandArgs a)
             waited = true;
         }
     });
+    if (!waited)
+        pdl_wait();  // complete only after the shrink
 }
 
 // Few tokens at large ranks: a CTA of 8 warps per (token, 256 columns), warp
@@ -315,19 +322,20 @@ __global__ void __launch_bounds__(32 * DW_WARPS, 1) k_dec_expand_wide(const DecE
     const bool on = col < d_out;
     __nv_bfloat16 *yp = a.y + (size_t)t * d_out + (on ? col : 0);
     const uint4 yv = on && warp == 0 ? *reinterpret_cast<const uint4 *>(yp) : make_uint4(0u, 0u, 0u, 0u);
-    const int pvalid = a.m.hdr[HDR_PVALID];
     const int p0 = a.m.toff[t], p1 = a.m.toff[t + 1];
-    if (pvalid == 0)
-        return;  // uniform over the CTA
-    int2 pq[DW_PP];
+    if (p1 <= p0) {
+        pdl_wait();  // no pair (uniform over the CTA); complete only after the shrink
+        return;
+    }
+    int pa[DW_PP];
 #pragma unroll
     for (int i = 0; i < DW_PP; ++i)
-        pq[i] = p0 + i < p1 ? a.m.pq[p0 + i] : make_int2(-1, -1);
+        pa[i] = p0 + i < p1 ? a.m.pc[p0 + i].y : -1;
     uint4 bpre[DW_PP][DW_PR];
     int kk[DW_PP];
 #pragma unroll
     for (int i = 0; i < DW_PP; ++i) {
-        const int ad = pq[i].y;
+        const int ad = pa[i];
         const __nv_bfloat16 *br = a.pool.B + (size_t)(ad < 0 ? 0 : ad) * r_max * d_out + col;
 #pragma unroll
         for (int u = 0; u < DW_PR; ++u) {
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(32 * DW_WARPS, 1) k_dec_expand_wide(const DecE
     for (int i = 0; i < DW_PP; ++i) {
         const int k = kk[i];
         if (k > 0) {
-            const float *zr = a.z + (size_t)pq[i].x * a.zs;
+            const float *zr = a.z + (size_t)(p0 + i) * a.zs;
             float zz[DW_PR];
 #pragma unroll
             for (int u = 0; u < DW_PR; ++u) {
@@ -356,14 +364,14 @@ __global__ void __launch_bounds__(32 * DW_WARPS, 1) k_dec_expand_wide(const DecE
         }
     }
     for (int p = p0 + DW_PP; p < p1; ++p) {
-        const int2 v = a.m.pq[p];
-        if (v.y < 0)
+        const int ad = a.m.pc[p].y;
+        if (ad < 0)
             continue;
-        const int k = dec_rank(a.pool, a.ranks, v.y);
+        const int k = dec_rank(a.pool, a.ranks, ad);
         if (k <= 0)
             continue;
-        const __nv_bfloat16 *br = a.pool.B + (size_t)v.y * r_max * d_out + col;
-        const float *zr = a.z + (size_t)v.x * a.zs;
+        const __nv_bfloat16 *br = a.pool.B + (size_t)ad * r_max * d_out + col;
+        const float *zr = a.z + (size_t)p * a.zs;
         uint4 bb[DW_PR];
         float zz[DW_PR];
 #pragma unroll
@@ -403,6 +411,7 @@ struct DecFusedArgs {
     DecShrinkArgs s;
     DecExpandArgs e;
     int ng;  // shrink items per pair: rank rows in groups of 8
+    int P;   // pairs of the batch (CSR)
 };
 
 // Waits until *cnt >= target, for at most WAIT_LIMIT_NS (then LORA_DEV_TIMEOUT).
@@ -424,9 +433,8 @@ __global__ void __launch_bounds__(256, 1) k_dec_fused(const DecFusedArgs a)
     const MapDev &m = a.s.m;
     int32_t *status = m.hdr + HDR_STATUS;
     const int epoch = m.hdr[HDR_EPOCH];
-    const int pvalid = m.hdr[HDR_PVALID];
     const int G = gridDim.x;
-    for (int it = blockIdx.x; it < pvalid * a.ng; it += G) {
+    for (int it = blockIdx.x; it < a.P * a.ng; it += G) {
         const int q = it / a.ng, g = it % a.ng;
         dec_shrink_item(a.s, xs, q, g * (blockDim.x >> 5), g == 0);
         __syncthreads();  // z rows written, x row consumed
@@ -457,7 +465,7 @@ __global__ void __launch_bounds__(256, 1) k_dec_fused(const DecFusedArgs a)
 // ------------------------------------------------------------ several projections, one launch each
 
 // The shrink of every projection in one grid: blockIdx.y runs over the
-// projections' row groups (prefix gpre), blockIdx.x over the sorted pairs.
+// projections' row groups (prefix gpre), blockIdx.x over the CSR pairs.
 __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink_multi(const MultiDecArgs a)
 {
     extern __shared__ __align__(16) uint4 xs[];
@@ -494,6 +502,8 @@ __global__ void __launch_bounds__(256, MINB) k_dec_expand_multi(const MultiDecAr
             waited = true;
         }
     });
+    if (!waited)
+        pdl_wait();  // complete only after the shrink
 }
 
 }  // namespace
@@ -586,7 +596,7 @@ cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const 
     const int ng = (pool.r_max + 7) / 8;
     const int nc = (pool.d_out + 255) / 256;
     DecFusedArgs a{{x, pool, ranks, m, z_stride(pool.r_max), m.z}, {y, pool, ranks, m, T, z_stride(pool.r_max), nc, m.z},
-                   ng};
+                   ng, P};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(sm_count(), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
@@ -597,7 +607,6 @@ cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    (void)P;
     return cudaLaunchKernelEx(&cfg, k_dec_fused, a);
 }
 

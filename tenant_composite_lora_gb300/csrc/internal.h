@@ -51,8 +51,12 @@ constexpr int RANK_TAB_MAX = 2048;
 // HDR_NMTILES: tensor-core shrink tiles (MMA_TM pairs of one segment).
 // HDR_EPOCH, HDR_DEXIT: launches of the fused decode kernel since the mapping
 // was built, and its CTAs that have exited in the current launch.
+// HDR_BUILD: builds of this mapping (advanced by the CSR stage); HDR_SORTED:
+// the build whose tuples the sort stage last produced.  HDR_U, HDR_PVALID,
+// HDR_NTILES and HDR_NMTILES belong to the sort stage.
 enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_BAR = 5, HDR_BAR_BASE = 6,
-       HDR_EXIT = 7, HDR_NMTILES = 8, HDR_EPOCH = 9, HDR_DEXIT = 10, HDR_WORDS = 11 };
+       HDR_EXIT = 7, HDR_NMTILES = 8, HDR_EPOCH = 9, HDR_DEXIT = 10, HDR_BUILD = 11, HDR_SORTED = 12,
+       HDR_WORDS = 13 };
 
 // Tensor-core (tcgen05) prefill path: tiles of MMA_TM rows (pairs of one
 // segment for the shrink, consecutive tokens for the expand).
@@ -72,6 +76,8 @@ struct PoolDev {
     int d_in, d_out, r_max, capacity;
 };
 
+// The mapping on the device.  The CSR stage fills toff, pc, calpha and the
+// header's status; the sort stage the ordered tuples and everything after them.
 struct MapDev {
     int32_t *tok, *adapter, *src, *pos;  // [max_pairs]
     float *alpha;                        // [max_pairs]
@@ -82,9 +88,11 @@ struct MapDev {
     int32_t *hdr;                        // [HDR_WORDS]
     int4 *mtile;                         // [mma_tile_bound] tensor-core shrink tiles {adapter, q0, n, segment}
     int32_t *toff;                       // [max_tokens+1] copy of the batch's CSR offsets
-    int2 *pq;                            // [max_pairs] per CSR pair: {sorted position, adapter}, -1s if left out
-    int32_t *zcnt;                       // [max_pairs] per sorted pair: z row groups written (fused decode)
-    float *z;                            // [max_pairs][Z_ROW_FLOATS] shrink output
+    int2 *pc;                            // [max_pairs] per CSR pair: {token, adapter}, adapter -1 if left out
+    float *calpha;                       // [max_pairs] per CSR pair: alpha
+    int32_t *zcnt;                       // [max_pairs] per CSR pair: z row groups written (fused decode)
+    float *z;                            // [max_pairs][Z_ROW_FLOATS] shrink output: a row per sorted
+                                         // pair (split, tensor-core paths) or per CSR pair (decode)
     float *partial;                      // [partial_ctas][EXP_TILE_ELEMS] fused-kernel tiles
     int partial_ctas;
     int32_t *ghist;                      // [map_global_hist_words(capacity)] or null: mapping
@@ -92,13 +100,19 @@ struct MapDev {
 };
 
 // Launchers (each returns cudaGetLastError()).
+// The mapping's CSR stage (every build) and sort stage (before a path that
+// reads the sorted tuples; it does nothing when the current build is sorted);
+// launch_build_mapping enqueues both.
+cudaError_t launch_map_csr(const MapDev &m, const int32_t *offsets, const int32_t *ids, const float *alpha, int T,
+                           int P, int capacity, cudaStream_t st);
+cudaError_t launch_map_sort(const MapDev &m, int T, int P, int capacity, cudaStream_t st);
 cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const int32_t *ids,
                                  const float *alpha, int T, int P, int capacity, int max_pairs,
                                  cudaStream_t st);
 cudaError_t launch_shrink(const __nv_bfloat16 *x, const PoolDev &pool, const int32_t *ranks,
                           const MapDev &m, int P, int grid, cudaStream_t st);
 
-// Floats per sorted pair in the mapping's z buffer: one projection uses the
+// Floats per pair in the mapping's z buffer: one projection uses the
 // first round4(r_max); several projections applied in one launch place
 // their columns side by side (at most this many in total).
 constexpr int Z_ROW_FLOATS = 256;

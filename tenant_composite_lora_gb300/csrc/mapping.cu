@@ -6,24 +6,33 @@
 // processes the tokens of one adapter back to back and each adapter's A and
 // B are read once.
 //
-// One CTA (1024 threads; 256 for short batches over small pools) performs a
-// stable counting sort on the adapter id
-// (the key range is the pool capacity):
-//   0. stage the offsets, ids and alpha bits in shared memory when they fit
-//      (one coalesced read; every later step works on shared memory);
-//   1. check the CSR offsets;
-//   2. expand the offsets into the token of each pair, and build per-warp
-//      histograms of the ids over contiguous chunks of the pairs (shared
-//      memory atomics into the warp's own row; layout [warp][bin]);
-//   3. block scans over the bins give every warp's first output slot per
+// Two kernels, each a single CTA:
+//
+// k_map_csr (every build) copies the batch into the mapping in CSR order:
+//   the offsets (toff), and per pair {token, adapter} (pc; adapter -1 when
+//   the pair is left out) and alpha (calpha).  It checks the offsets (all
+//   pairs are left out when they are malformed), flags ids outside
+//   [0, capacity), clears the status word and the fused kernels' counters,
+//   and advances the build epoch.  The decode kernels read nothing else:
+//   they index pairs in CSR order.
+//
+// k_map_sort (launched by the paths that read the sorted tuples, before
+// their own kernels; it returns at once when the current build is already
+// sorted) performs a stable counting sort on the adapter id over the CSR
+// copy (the key range is the pool capacity):
+//   0. stage pc and calpha in shared memory when they fit (one coalesced
+//      read; every later step works on shared memory);
+//   1. per-warp histograms of the ids over contiguous chunks of the pairs
+//      (shared memory atomics into the warp's own row; layout [warp][bin]);
+//   2. block scans over the bins give every warp's first output slot per
 //      bin, the segments, the shrink tiles (<= SHRINK_TT pairs of one
 //      segment) and the tensor-core shrink tiles (<= MMA_TM pairs of one
 //      segment); slots up to the host-known bounds get empty sentinels;
-//   4. each warp rescans its chunk and scatters: rank among equal keys =
+//   3. each warp rescans its chunk and scatters: rank among equal keys =
 //      earlier lanes with the same key + the warp's running cursor; the
 //      token also goes to its shrink tile's token list;
-//   5. when the sorted token and source of every position fit in shared
-//      memory, step 4 scatters only there and the sorted arrays are written
+//   4. when the sorted token and source of every position fit in shared
+//      memory, step 3 scatters only there and the sorted arrays are written
 //      afterwards position by position, so that every store is coalesced.
 // Stability: chunks are in CSR order, warps are ranked by chunk, lanes by
 // pair index, so ties keep CSR order -- the tuples come out ordered by
@@ -88,81 +97,64 @@ __device__ Scan4 block_exclusive_scan4(Scan4 v, Scan4 &total, int *sh /* [4 * 32
 
 constexpr int MAP_STAGE_U = 8;  // staged words per thread per round (loads in flight)
 
-struct MapArgs {
+// Stages words in shared memory: n_a words from src_a, then n_b from src_b,
+// then n_c from src_c, one index space.  MAP_STAGE_U loads in flight per
+// thread before any store.
+__device__ __forceinline__ void stage_words(int32_t *dst, const int32_t *src_a, int n_a, const int32_t *src_b,
+                                            int n_b, const int32_t *src_c, int n_c)
+{
+    const int tid = threadIdx.x, nthr = blockDim.x, n_ab = n_a + n_b, n_all = n_ab + n_c;
+    for (int base = 0; base < n_all; base += MAP_STAGE_U * nthr) {
+        int32_t v[MAP_STAGE_U];
+#pragma unroll
+        for (int u = 0; u < MAP_STAGE_U; ++u) {
+            const int i = base + u * nthr + tid;
+            v[u] = 0;
+            if (i < n_a)
+                v[u] = __ldg(src_a + i);
+            else if (i < n_ab)
+                v[u] = __ldg(src_b + (i - n_a));
+            else if (i < n_all)
+                v[u] = __ldg(src_c + (i - n_ab));
+        }
+#pragma unroll
+        for (int u = 0; u < MAP_STAGE_U; ++u) {
+            const int i = base + u * nthr + tid;
+            if (i < n_all)
+                dst[i] = v[u];
+        }
+    }
+}
+
+struct CsrArgs {
     MapDev m;
     const int32_t *off, *ids;
     const float *alpha;
-    int32_t *hist_g;  // histograms and per-bin arrays in global memory (null: shared memory)
-    int T, P, cap, nw, staged, tile_bound, mtile_bound;
-    int sorted_smem;  // the scatter lands in shared memory, the sorted arrays are written coalesced after
+    int T, P, cap, staged;
 };
 
-
-__global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
+__global__ void __launch_bounds__(MAP_THREADS, 1) k_map_csr(const CsrArgs a)
 {
-    extern __shared__ int32_t sh[];
-    __shared__ int s_scan[4 * 32 + 4];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int T = a.T, P = a.P, cap = a.cap, nw = a.nw;
-    const int nthr = blockDim.x;  // 1024, or 256 for short batches
-    MapDev &m = a.m;
+    extern __shared__ __align__(16) int32_t sh[];
+    const int tid = threadIdx.x, nthr = blockDim.x;
+    const int T = a.T, P = a.P, cap = a.cap;
+    const MapDev &m = a.m;
     // Launched as a programmatic dependent of the previous kernel in the
     // stream: the CTA starts and stages the batch's inputs (which no kernel of
     // the library writes) while that kernel finishes, and waits for it before
     // writing anything.  Its own dependents may launch at once: they wait too.
     pdl_launch_dependents();
-
-    const int32_t *off, *ids, *alb;
-    int32_t *tok, *hist;
+    const int32_t *off = a.off, *ids = a.ids, *alb = reinterpret_cast<const int32_t *>(a.alpha);
+    int32_t *tok = m.tmp_tok;
     if (a.staged) {
-        int32_t *s_off = sh, *s_ids = sh + (T + 1), *s_al = s_ids + P;
-        tok = s_al + P;
-        hist = tok + P;
-        // offsets, ids and alpha bits are consecutive in shared memory: one
-        // index space, MAP_STAGE_U loads in flight per thread before any store
-        const int32_t *alg = reinterpret_cast<const int32_t *>(a.alpha);
-        const int n_off = T + 1, n_all = T + 1 + 2 * P;
-        for (int base = 0; base < n_all; base += MAP_STAGE_U * nthr) {
-            int32_t v[MAP_STAGE_U];
-#pragma unroll
-            for (int u = 0; u < MAP_STAGE_U; ++u) {
-                const int i = base + u * nthr + tid;
-                v[u] = 0;
-                if (i < n_off)
-                    v[u] = __ldg(a.off + i);
-                else if (i < n_off + P)
-                    v[u] = __ldg(a.ids + (i - n_off));
-                else if (i < n_all)
-                    v[u] = __ldg(alg + (i - n_off - P));
-            }
-#pragma unroll
-            for (int u = 0; u < MAP_STAGE_U; ++u) {
-                const int i = base + u * nthr + tid;
-                if (i < n_all)
-                    sh[i] = v[u];
-            }
-        }
-        off = s_off;
-        ids = s_ids;
-        alb = s_al;
-    } else {
-        off = a.off;
-        ids = a.ids;
-        alb = reinterpret_cast<const int32_t *>(a.alpha);
-        tok = m.tmp_tok;
-        hist = a.hist_g ? a.hist_g : sh;
+        // offsets, ids and alpha bits consecutive in shared memory, then the token of each pair
+        stage_words(sh, a.off, T + 1, a.ids, P, alb, P);
+        off = sh;
+        ids = sh + T + 1;
+        alb = ids + P;
+        tok = sh + T + 1 + 2 * P;
     }
-    // per bin: first sorted position and first shrink tile of its segment
-    int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
-    // sorted token and source pair per position (with sorted_smem)
-    int32_t *s_stok = bin_tile + cap, *s_ssrc = s_stok + P;
-    if (!a.hist_g)
-        for (int i = tid; i < nw * cap; i += nthr)
-            hist[i] = 0;
     pdl_wait();  // the previous kernel (which may still read this mapping) is done
-    if (a.hist_g)  // global scratch of this mapping: written only after the wait
-        for (int i = tid; i < nw * cap; i += nthr)
-            hist[i] = 0;
     if (tid == 0) {
         m.hdr[HDR_STATUS] = 0;
         m.hdr[HDR_BAR] = 0;  // fused-kernel counters start over with every mapping
@@ -170,36 +162,27 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         m.hdr[HDR_EXIT] = 0;
         m.hdr[HDR_EPOCH] = 0;
         m.hdr[HDR_DEXIT] = 0;
+        m.hdr[HDR_T] = T;
+        m.hdr[HDR_BUILD] = m.hdr[HDR_BUILD] + 1;  // the sorted tuples are stale from here on
     }
-    for (int q = tid; q < P; q += nthr)
-        m.zcnt[q] = 0;
-    __syncthreads();
-
-    // 1. CSR check
+    for (int p = tid; p < P; p += nthr)
+        m.zcnt[p] = 0;
+    // the offsets: off[0] = 0, off[T] = P, non-decreasing
     int bad = (tid == 0) && (off[0] != 0 || off[T] != P);
     for (int t = tid; t < T; t += nthr)
         bad |= off[t + 1] < off[t];
     if (__syncthreads_or(bad)) {
-        for (int p = tid; p < P; p += nthr)
-            m.pos[p] = -1;
-        for (int i = tid; i < a.tile_bound; i += nthr)
-            m.tile[i] = make_int4(0, 0, 0, -1);
-        for (int i = tid; i < a.mtile_bound; i += nthr)
-            m.mtile[i] = make_int4(0, 0, 0, -1);
-        if (tid == 0) {
-            m.hdr[HDR_U] = 0;
-            m.hdr[HDR_PVALID] = 0;
-            m.hdr[HDR_NTILES] = 0;
-            m.hdr[HDR_NMTILES] = 0;
-            m.hdr[HDR_T] = T;
-            m.hdr[HDR_STATUS] = LORA_DEV_BAD_OFFSETS;
-            m.seg_start[0] = 0;
+        // every pair left out: empty pair ranges, no adapter
+        for (int t = tid; t <= T; t += nthr)
+            m.toff[t] = 0;
+        for (int p = tid; p < P; p += nthr) {
+            m.pc[p] = make_int2(-1, -1);
+            m.calpha[p] = 0.f;
         }
+        if (tid == 0)
+            atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_OFFSETS);
         return;
     }
-
-    // 2. token of each pair (and a copy of the offsets for the token-tile
-    // expand); per-warp histograms
     for (int t = tid; t <= T; t += nthr)
         m.toff[t] = off[t];
     for (int t = tid; t < T; t += nthr) {
@@ -207,26 +190,79 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         for (int p = p0; p < p1; ++p)
             tok[p] = t;
     }
-    const int chunk = (P + nw - 1) / nw;
+    __syncthreads();  // tok complete (shared or global memory)
     bool bad_id = false;
+    for (int p = tid; p < P; p += nthr) {
+        const int id = ids[p];
+        const bool ok = id >= 0 && id < cap;
+        bad_id |= !ok;
+        m.pc[p] = make_int2(tok[p], ok ? id : -1);
+        m.calpha[p] = __int_as_float(alb[p]);
+    }
+    if (bad_id)
+        atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_ID);
+}
+
+struct SortArgs {
+    MapDev m;
+    int32_t *hist_g;  // histograms and per-bin arrays in global memory (null: shared memory)
+    int T, P, cap, nw, staged, tile_bound, mtile_bound;
+    int sorted_smem;  // the scatter lands in shared memory, the sorted arrays are written coalesced after
+};
+
+__global__ void __launch_bounds__(MAP_THREADS, 1) k_map_sort(const SortArgs a)
+{
+    extern __shared__ __align__(16) int32_t sh[];
+    __shared__ int s_scan[4 * 32 + 4];
+    __shared__ int s_build, s_skip;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = a.P, cap = a.cap, nw = a.nw;
+    const int nthr = blockDim.x;  // 1024, or 256 for short batches
+    const MapDev &m = a.m;
+    pdl_launch_dependents();  // the dependents wait for this grid
+    // pc as words: [2p] token, [2p + 1] adapter (-1: left out); alpha bits
+    const int32_t *pcw = reinterpret_cast<const int32_t *>(m.pc), *alb = reinterpret_cast<const int32_t *>(m.calpha);
+    int32_t *hist = a.hist_g ? a.hist_g : sh + (a.staged ? 3 * P : 0);
+    // per bin: first sorted position and first shrink tile of its segment
+    int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
+    // sorted token and source pair per position (with sorted_smem)
+    int32_t *s_stok = (a.hist_g ? sh + (a.staged ? 3 * P : 0) : bin_tile + cap), *s_ssrc = s_stok + P;
+    if (!a.hist_g)
+        for (int i = tid; i < nw * cap; i += nthr)
+            hist[i] = 0;
+    pdl_wait();  // the CSR copy is complete, and no earlier kernel reads the sorted tuples any more
+    if (tid == 0) {
+        s_build = m.hdr[HDR_BUILD];
+        s_skip = m.hdr[HDR_SORTED] == s_build;
+    }
+    __syncthreads();
+    if (s_skip)
+        return;  // this build is sorted already
+    if (a.staged) {
+        stage_words(sh, pcw, 2 * P, alb, P, alb, 0);
+        pcw = sh;
+        alb = sh + 2 * P;
+    }
+    if (a.hist_g)
+        for (int i = tid; i < nw * cap; i += nthr)
+            hist[i] = 0;
+    __syncthreads();
+
+    // 1. per-warp histograms
+    const int chunk = (P + nw - 1) / nw;
     if (warp < nw) {
         const int lo = warp * chunk, hi = min(P, lo + chunk);
         int32_t *h = hist + warp * cap;
         for (int base = lo; base < hi; base += 32) {
             const int p = base + lane;
-            const bool valid = p < hi;
-            const int id = valid ? ids[p] : 0;
-            const bool ok = valid && id >= 0 && id < cap;
-            bad_id |= valid && !ok;
-            if (ok)
+            const int id = p < hi ? pcw[2 * p + 1] : -1;
+            if (id >= 0)
                 atomicAdd(&h[id], 1);  // the warp's own histogram: counts only, order is irrelevant here
         }
     }
-    if (bad_id)
-        atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_ID);
     __syncthreads();
 
-    // 3. scan over bins, a CTA's worth of bins per round, bin-ascending
+    // 2. scan over bins, a CTA's worth of bins per round, bin-ascending
     Scan4 carry = {0, 0, 0, 0};
     for (int base = 0; base < cap; base += nthr) {
         const int b = base + tid;
@@ -268,12 +304,11 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         m.hdr[HDR_PVALID] = carry.a;
         m.hdr[HDR_NTILES] = carry.c;
         m.hdr[HDR_NMTILES] = carry.d;
-        m.hdr[HDR_T] = T;
         m.seg_start[carry.b] = carry.a;
     }
     __syncthreads();
 
-    // 4. stable scatter
+    // 3. stable scatter
     if (warp < nw) {
         const int lo = warp * chunk, hi = min(P, lo + chunk);
         int32_t *h = hist + warp * cap;
@@ -281,13 +316,13 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         for (int bse = lo; bse < hi; bse += 32) {
             const int p = bse + lane;
             const bool valid = p < hi;
-            const int id = valid ? ids[p] : 0;
-            const bool ok = valid && id >= 0 && id < cap;
+            const int id = valid ? pcw[2 * p + 1] : -1;
+            const bool ok = id >= 0;
             const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
             const int cur = ok ? h[id] : 0;
             if (ok) {
                 const int dst = cur + __popc(peers & lt);
-                const int t = tok[p];
+                const int t = pcw[2 * p];
                 if (a.sorted_smem) {
                     s_stok[dst] = t;
                     s_ssrc[dst] = p;
@@ -300,10 +335,8 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
                     m.src[dst] = p;
                 }
                 m.pos[p] = dst;
-                m.pq[p] = make_int2(dst, id);
             } else if (valid) {
                 m.pos[p] = -1;
-                m.pq[p] = make_int2(-1, -1);
             }
             __syncwarp();
             if (ok && lane == __ffs(peers) - 1)
@@ -312,11 +345,11 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
         }
     }
     if (a.sorted_smem) {
-        // 5. the sorted arrays, position by position (coalesced stores)
+        // 4. the sorted arrays, position by position (coalesced stores)
         __syncthreads();
         const int pvalid = carry.a;
         for (int d = tid; d < pvalid; d += nthr) {
-            const int p = s_ssrc[d], t = s_stok[d], id = ids[p];
+            const int p = s_ssrc[d], t = s_stok[d], id = pcw[2 * p + 1];
             m.tok[d] = t;
             m.src[d] = p;
             m.adapter[d] = id;
@@ -325,6 +358,40 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_build_mapping(MapArgs a)
             m.tile_tok[(bin_tile[id] + r / SHRINK_TT) * SHRINK_TT + r % SHRINK_TT] = t;
         }
     }
+    if (tid == 0)
+        m.hdr[HDR_SORTED] = s_build;
+}
+
+template <class K>
+cudaError_t map_attrs(K kernel, int &done)
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (done == dev)
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MAP_SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess)
+        done = dev;
+    return e;
+}
+
+template <class Args>
+cudaError_t map_launch(void (*kernel)(Args), const Args &a, int threads, size_t smem, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 }  // namespace
@@ -354,13 +421,26 @@ int map_global_hist_words(int capacity)
     return (MAP_GHIST_WARPS + 2) * capacity;
 }
 
-cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const int32_t *ids,
-                                 const float *alpha, int T, int P, int capacity, int max_pairs,
-                                 cudaStream_t st)
+cudaError_t launch_map_csr(const MapDev &m, const int32_t *offsets, const int32_t *ids, const float *alpha, int T,
+                           int P, int capacity, cudaStream_t st)
 {
-    (void)max_pairs;
     const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
-    const long long staged_words = (long long)(T + 1) + 3LL * P;
+    const long long words = (long long)(T + 1) + 3LL * P;
+    const int staged = words <= budget ? 1 : 0;
+    // a short batch is one staging round of 256 threads (cheaper block-wide steps)
+    const int threads = (T + 1 + 2LL * P <= 256LL * MAP_STAGE_U) ? 256 : MAP_THREADS;
+    static thread_local int attr_done = -1;  // per host thread
+    const cudaError_t e = map_attrs(k_map_csr, attr_done);
+    if (e != cudaSuccess)
+        return e;
+    const CsrArgs a{m, offsets, ids, alpha, T, P, capacity, staged};
+    return map_launch(k_map_csr, a, threads, staged ? 4 * (size_t)words : 0, st);
+}
+
+cudaError_t launch_map_sort(const MapDev &m, int T, int P, int capacity, cudaStream_t st)
+{
+    const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
+    const long long staged_words = 3LL * P;       // pc (two words per pair) and alpha
     // short batches over small pools: one CTA of 256 threads (cheaper
     // block-wide phases, the bins still one scan round); otherwise 1024
     const int threads = (P <= 512 && capacity <= 256) ? 256 : MAP_THREADS;
@@ -376,6 +456,7 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
         hist_g = m.ghist;
         if (nw > MAP_GHIST_WARPS)
             nw = MAP_GHIST_WARPS;
+        staged = staged_words <= budget ? 1 : 0;
     } else if (staged_words + 3LL * capacity <= budget) {
         staged = 1;
         const long long fit = (budget - staged_words) / capacity - 2;
@@ -390,37 +471,27 @@ cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const 
         return cudaErrorInvalidValue;
     // long batches: the sorted positions' token and source pair also in shared
     // memory when they fit (short ones gain less than the extra phase costs)
-    const int sorted_smem =
-        staged && P >= 2048 && staged_words + (long long)(nw + 2) * capacity + 2LL * P <= budget;
-    const size_t smem =
-        4 * ((staged ? (size_t)staged_words : 0) + (hist_g ? 0 : (size_t)(nw + 2) * capacity) +
-             (sorted_smem ? 2 * (size_t)P : 0));
+    const long long hist_words = hist_g ? 0 : (long long)(nw + 2) * capacity;
+    const int sorted_smem = staged && P >= 2048 && staged_words + hist_words + 2LL * P <= budget;
+    const size_t smem = 4 * ((staged ? (size_t)staged_words : 0) + (size_t)hist_words + (sorted_smem ? 2 * (size_t)P : 0));
     static thread_local int attr_done = -1;  // per host thread
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (attr_done != dev) {
-        cudaError_t e =
-            cudaFuncSetAttribute(k_build_mapping, cudaFuncAttributeMaxDynamicSharedMemorySize, MAP_SMEM_BYTES);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_build_mapping, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess)
-            return e;
-        attr_done = dev;
-    }
-    MapArgs a{m, offsets, ids, alpha, hist_g, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity),
-              mma_tile_bound(P, capacity), sorted_smem};
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, 1);
-    cfg.blockDim = dim3(threads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_build_mapping, a);
+    const cudaError_t e = map_attrs(k_map_sort, attr_done);
+    if (e != cudaSuccess)
+        return e;
+    const SortArgs a{m, hist_g, T, P, capacity, nw, staged, shrink_tile_bound(P, capacity),
+                     mma_tile_bound(P, capacity), sorted_smem};
+    return map_launch(k_map_sort, a, threads, smem, st);
+}
+
+cudaError_t launch_build_mapping(const MapDev &m, const int32_t *offsets, const int32_t *ids,
+                                 const float *alpha, int T, int P, int capacity, int max_pairs,
+                                 cudaStream_t st)
+{
+    (void)max_pairs;
+    cudaError_t e = launch_map_csr(m, offsets, ids, alpha, T, P, capacity, st);
+    if (e == cudaSuccess)
+        e = launch_map_sort(m, T, P, capacity, st);
+    return e;
 }
 
 }  // namespace tcl
