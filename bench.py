@@ -712,8 +712,8 @@ def recompress_lines(torch, stream, dev):
 # their own (share = 1: every token its own adapters, as in a decode batch;
 # larger: prompt-like runs), or two distinct Zipf(1.5) draws over 128
 # adapters per token ("zipf"); q_proj shape, every rank r_max.
-SWEEP_T = [16, 64, 128, 256, 384, 512, 1024, 2048, 4096]
-SWEEP_R = [8, 16, 64]
+SWEEP_T = [16, 64, 128, 256, 384, 512, 1024, 2048, 4096, 8192]
+SWEEP_R = [8, 16, 32, 64]
 SWEEP_SHARE = ["1", "16", "256", "zipf"]
 SWEEP_PATHS = {"decode": 4, "split": 1, "mma": 3}
 SWEEP_CAPACITY = 4096
@@ -788,9 +788,60 @@ def dispatch_sweep(torch, stream, dev) -> dict:
                         points.append(pt)
             finally:
                 pool.close()
+        del x, y
+        # the metric's workloads on every path
+        import workloads as W
+        from workloads.device import DeviceWorkload
+        configs = {}
+        for name in ["distinct", "zipf", "prefill", "sweep1", "sweep8", "sweep64", "sweep256"]:
+            wl = W.make(name)
+            dw = DeviceWorkload(wl, stream=stream)
+            res = {"T": wl.T, "P": wl.P, "r": wl.r_max,
+                   "chosen": PATH_NAMES[native.lora_dispatch_choose(wl.T, wl.P, wl.r_max, wl.d_in, wl.d_out)]}
+            try:
+                yb = dw.y0.clone()
+                for pname, pid in SWEEP_PATHS.items():
+                    def apply_(pid=pid):
+                        native.lora_delta_apply_path(dw.x, yb, dw.pool.handle, None, dw.mapping.handle, pid, stream)
+                    apply_()
+                    stream.synchronize()
+                    res[pname] = round(timer.time_us(apply_, 100 if wl.T <= 512 else 30), 2)
+            finally:
+                dw.close()
+            res["fastest"] = min(SWEEP_PATHS, key=lambda k: res[k])
+            configs[name] = res
     return {"shape": f"{d_in}x{d_out}", "pairs_per_token": 2, "capacity": SWEEP_CAPACITY,
             "protocol": "cold L2 (256 MB read before every replay, its time subtracted); us per call",
-            "points": points}
+            "points": points, "configs": configs}
+
+
+def sweep_markdown(d: dict) -> str:
+    """The sweep as the committed table (profiles/dispatch_sweep.md)."""
+    paths = list(SWEEP_PATHS)
+    out = ["# Dispatch sweep: every path's apply time over tokens x rank x adapter sharing", "",
+           "Command (one GB300, after `python -c \"import __graft_entry__ as g; g.build()\"`):",
+           "`python bench.py --dispatch-sweep --markdown > profiles/dispatch_sweep.md`", "",
+           f"Shape {d['shape']} (Llama-3-8B q_proj), {d['pairs_per_token']} pairs per token (alpha 0.5), "
+           f"pool of {d['capacity']} slots, every adapter at k = r.  share = tokens of a request: runs of that "
+           "many consecutive tokens use the same two adapters of their own (1: every token its own, as in "
+           "decode; larger: prompt-like); zipf = two distinct Zipf(1.5) draws over 128 adapters per token.  "
+           f"Times: {d['protocol']}.  U = distinct adapters.", "",
+           "| T | r | share | P | U | " + " | ".join(f"{p} us" for p in paths) + " | fastest | chosen | chosen / fastest |",
+           "|" + "---|" * (8 + len(paths))]
+    for p in d["points"]:
+        t = {k: p.get(k) for k in paths}
+        best = p["fastest"]
+        ratio = (t[p["chosen"]] / t[best]) if t.get(p["chosen"]) and t[best] else None
+        out.append(f"| {p['T']} | {p['r']} | {p['share']} | {p['P']} | {p['U']} | "
+                   + " | ".join("-" if t[k] is None else f"{t[k]:.2f}" for k in paths)
+                   + f" | {best} | {p['chosen']} | " + ("-" if ratio is None else f"{ratio:.2f}") + " |")
+    out += ["", "## The metric's workloads, every path", "",
+            "| workload | T | P | r | " + " | ".join(f"{p} us" for p in paths) + " | fastest | chosen |",
+            "|" + "---|" * (6 + len(paths))]
+    for name, c in d["configs"].items():
+        out.append(f"| {name} | {c['T']} | {c['P']} | {c['r']} | " + " | ".join(f"{c[k]:.2f}" for k in paths)
+                   + f" | {c['fastest']} | {c['chosen']} |")
+    return "\n".join(out) + "\n"
 
 
 def cpu_model() -> str:
@@ -903,6 +954,7 @@ def main():
                     help="force an execution path (default: the library's dispatch table)")
     ap.add_argument("--dispatch-sweep", action="store_true",
                     help="time every path over tokens x rank x adapter sharing and print that table instead")
+    ap.add_argument("--markdown", action="store_true", help="with --dispatch-sweep: the table as Markdown")
     args = ap.parse_args()
     args.path_id = {"auto": 0, "split": 1, "fused": 2, "mma": 3, "decode": 4}[args.path]
     args.warmup = max(3, args.warmup)
@@ -917,7 +969,8 @@ def main():
         import torch
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
         torch.cuda.set_device(dev)
-        print(json.dumps(dispatch_sweep(torch, torch.cuda.Stream(device=dev), dev)))
+        d = dispatch_sweep(torch, torch.cuda.Stream(device=dev), dev)
+        print(sweep_markdown(d) if args.markdown else json.dumps(d), end="" if args.markdown else "\n")
         return
 
     rank, world, dist = dist_setup(args.gpus)

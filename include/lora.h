@@ -204,10 +204,11 @@ lora_status lora_delta_apply(const void *x_dev, void *y_dev, const lora_pool *po
  * the decode path -- the same shrink and the same (token, 256 columns)
  * expand, so the same bits, except where a single call takes the wide-rank
  * expand (r_max > 16 with few (token, column) items), whose summation order
- * differs (last-bit differences, within the stated tolerance).  Decode
- * batches (T <= 256) whose sum of round4(r_max) over the projections is at
- * most 256 take the two shared launches; other batches run one
- * lora_delta_apply per projection, in order.  Stream-ordered; no allocation.
+ * differs (last-bit differences, within the stated tolerance).  Batches for
+ * which the dispatch table picks the decode path for every projection, and
+ * whose sum of round4(r_max) over the projections is at most 256, take the
+ * two shared launches; other batches run one lora_delta_apply per
+ * projection, in order.  Stream-ordered; no allocation.
  * Returns LORA_ERR_INVALID_ARG for NULL or mismatched arguments or aliased
  * outputs, LORA_ERR_NOT_SUPPORTED above LORA_MAX_PROJECTIONS.
  */
@@ -261,7 +262,13 @@ lora_status lora_delta_apply_path(const void *x_dev, void *y_dev, const lora_poo
 /*
  * lora_dispatch_choose: the dispatch table, host only (no device work).
  * Returns the lora_path that lora_delta_apply takes for T tokens, P pairs,
- * the given r_max, d_in and d_out.  (LoRAForge page, "Approach" (5).)
+ * the given r_max, d_in and d_out.  (LoRAForge page, "Approach" (5): the
+ * path fixed by phase, rank and shape.)  The tensor-core path from 8192
+ * tokens at r_max <= 8, 3072 at r_max <= 16 and 384 above (batches that long
+ * are taken for prefill chunks, whose tokens share adapters); otherwise the
+ * decode path; the split path where neither takes the shape.  The thresholds
+ * are the measured crossovers of a sweep of all paths over tokens, rank and
+ * adapter sharing on GB300.
  */
 int lora_dispatch_choose(int T, int P, int r_max, int d_in, int d_out);
 

@@ -267,17 +267,33 @@ void free_mapping(lora_mapping *m)
 }
 
 // Dispatch table (LoRAForge page, "Approach" (5): native path or a special
-// kernel, fixed by phase, rank and shape).
-// Short batches (decode) take the per-pair decode kernels; long batches
-// (prefill) go to the tensor cores, where a 128-token tile touches few
-// adapters and a segment holds many tokens.
+// kernel, fixed by phase, rank and shape), from a sweep of every path over
+// tokens x rank x adapter sharing on this GPU.  The decode kernels (a CTA per
+// pair; shared adapters' rows come from L2) are the fastest at every swept
+// size of decode-like batches and of most others; the tensor-core path wins
+// where long runs of tokens share their adapters (prefill chunks) and the
+// rank is large enough to fill its tiles.  The phase is read from the token
+// count: at least MMA_FROM tokens of a rank class are taken for a prefill
+// batch.  The sharing itself is not known on the host (the pair lists are on
+// the device), so it does not enter the choice.  The split path is never the
+// fastest on the sweep; it serves shapes that neither of the others takes.
+int mma_from_tokens(int r_max)
+{
+    if (r_max <= 8)
+        return MMA_FROM_R8;
+    if (r_max <= 16)
+        return MMA_FROM_R16;
+    return MMA_FROM_R64;
+}
+
 int choose_path(int T, int P, int r_max, int d_in, int d_out)
 {
     (void)P;
-    if (T <= DECODE_MAX_TOKENS && decode_supported(d_in, d_out))
-        return LORA_PATH_DECODE;
-    if (T >= MMA_MIN_TOKENS && mma_supported(d_in, d_out, r_max))
+    const bool mma = mma_supported(d_in, d_out, r_max);
+    if (mma && T >= mma_from_tokens(r_max))
         return LORA_PATH_MMA;
+    if (decode_supported(d_in, d_out))
+        return LORA_PATH_DECODE;
     return LORA_PATH_SPLIT;
 }
 
@@ -683,7 +699,7 @@ lora_status lora_delta_apply_multi(const lora_projection *projs, int n_proj, con
     if (n_proj > LORA_MAX_PROJECTIONS)
         return LORA_ERR_NOT_SUPPORTED;
     int zcols = 0;
-    bool decode_ok = m->T <= DECODE_MAX_TOKENS;
+    bool decode_ok = true;
     for (int j = 0; j < n_proj; ++j) {
         const lora_projection &p = projs[j];
         if (!p.x_dev || !p.y_dev || !p.pool || p.x_dev == p.y_dev || p.pool->capacity != m->capacity)
@@ -694,7 +710,8 @@ lora_status lora_delta_apply_multi(const lora_projection *projs, int n_proj, con
             if (projs[i].y_dev == p.y_dev || projs[i].x_dev == p.y_dev || p.x_dev == projs[i].y_dev)
                 return LORA_ERR_INVALID_ARG;  // one projection's output is another's input or output
         zcols += z_stride(p.pool->r_max);
-        decode_ok = decode_ok && decode_supported(p.pool->d_in, p.pool->d_out);
+        decode_ok = decode_ok && choose_path(m->T, m->P, p.pool->r_max, p.pool->d_in, p.pool->d_out) ==
+                                     LORA_PATH_DECODE;
     }
     if (m->T == 0 || m->P == 0)
         return LORA_OK;
@@ -714,8 +731,9 @@ lora_status lora_delta_apply_multi(const lora_projection *projs, int n_proj, con
         if (e != cudaErrorNotSupported)
             return from_cuda(e);
     }
-    // long batches (or shapes the decode kernels do not take): one apply per
-    // projection, each on the path the dispatch table picks
+    // batches the dispatch table sends elsewhere for some projection (or
+    // shapes the decode kernels do not take): one apply per projection, each
+    // on the path the dispatch table picks
     for (int j = 0; j < n_proj; ++j) {
         const lora_status s =
             lora_delta_apply(projs[j].x_dev, projs[j].y_dev, projs[j].pool, projs[j].ranks_dev, m, stream);

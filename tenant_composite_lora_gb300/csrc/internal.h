@@ -61,8 +61,14 @@ enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR
 // Tensor-core (tcgen05) prefill path: tiles of MMA_TM rows (pairs of one
 // segment for the shrink, consecutive tokens for the expand).
 constexpr int MMA_TM = 128;
-// Dispatch: batches of at least this many tokens take the tensor-core path.
-constexpr int MMA_MIN_TOKENS = 512;
+// Dispatch: batches of at least this many tokens take the tensor-core path,
+// by rank class (r_max <= 8, <= 16, larger): the measured crossovers of the
+// decode and tensor-core paths on prefill-like batches (runs of consecutive
+// tokens sharing their adapters), between the swept sizes 4096 / 8192,
+// 2048 / 3250 (the sparse prefill workload) and 256 / 384 tokens.
+constexpr int MMA_FROM_R8 = 8192;
+constexpr int MMA_FROM_R16 = 3072;
+constexpr int MMA_FROM_R64 = 384;
 
 // Fused decode kernel: one CTA per SM; dynamic shared memory = the expand
 // layout + an entry ring of at most FUSED_RING_MAX bytes (less if the
@@ -173,8 +179,6 @@ cudaError_t launch_recompress(const __nv_bfloat16 *A, const __nv_bfloat16 *B, in
                               float *F, float *Tout, float *sigma, void *ws, cudaStream_t st);
 int rank_allocate(const float *sigma, int M, int r_stride, const int32_t *rank, const int32_t *cost, int policy,
                   int d, int floor_k, int32_t *k_out);
-// Dispatch: batches of at most this many tokens take the decode path.
-constexpr int DECODE_MAX_TOKENS = 256;
 // The same decode work as one cooperative launch (a CTA per SM): shrink
 // items first, then expand warps that wait on per-pair counters.
 cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,

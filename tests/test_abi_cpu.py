@@ -45,11 +45,20 @@ def test_host_only_calls(lib):
     assert native.status_string(0) == "ok"
     assert "not supported" in native.status_string(5)
     assert "sm_103a" in native.lora_version()
-    # the dispatch table: decode batches, long prefill batches, the middle
+    # the dispatch table: decode batches, long prefill batches, the rank
+    # classes' crossovers, and shapes only the split path takes
     assert native.lora_dispatch_choose(32, 96, 8, 4096, 4096) == native.LORA_PATH_DECODE
     assert native.lora_dispatch_choose(256, 512, 64, 4096, 1024) == native.LORA_PATH_DECODE
     assert native.lora_dispatch_choose(3250, 6500, 16, 4096, 4096) == native.LORA_PATH_MMA
-    assert native.lora_dispatch_choose(300, 900, 16, 4096, 4096) == native.LORA_PATH_SPLIT
+    assert native.lora_dispatch_choose(300, 900, 16, 4096, 4096) == native.LORA_PATH_DECODE
+    assert native.lora_dispatch_choose(383, 766, 64, 4096, 4096) == native.LORA_PATH_DECODE
+    assert native.lora_dispatch_choose(384, 768, 64, 4096, 4096) == native.LORA_PATH_MMA
+    assert native.lora_dispatch_choose(3071, 6142, 16, 4096, 4096) == native.LORA_PATH_DECODE
+    assert native.lora_dispatch_choose(8191, 16382, 8, 4096, 4096) == native.LORA_PATH_DECODE
+    assert native.lora_dispatch_choose(8192, 16384, 8, 4096, 4096) == native.LORA_PATH_MMA
+    assert native.lora_dispatch_choose(4096, 8192, 16, 4104, 4096) == native.LORA_PATH_DECODE  # no tensor maps
+    assert native.lora_dispatch_choose(32, 96, 8, 110592, 4096) == native.LORA_PATH_SPLIT    # x row > smem
+    assert native.lora_dispatch_choose(32, 96, 8, 110600, 4096) == native.LORA_PATH_SPLIT
 
 
 def test_bad_arguments_rejected_before_device(lib):
