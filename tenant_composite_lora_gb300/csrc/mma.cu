@@ -255,9 +255,9 @@ __global__ void __launch_bounds__(MS_THREADS, 1)
 
 constexpr int ME_WORKERS = 256;                        // warps 0-7: lists, A operand, epilogue
 constexpr int ME_THREADS = ME_WORKERS + 64;            // warp 8: MMA issue; warp 9: B chunks by TMA
-constexpr int ME_SMAX = 16;                            // slots per A-operand build
-constexpr int ME_Z_BYTES = MMA_TM * ME_SMAX * 16 * 2;  // one of hi / lo: 128 rows x 256 bf16
-constexpr int ME_STAGES = 8;
+constexpr int ME_SMAX = 12;                            // slots per A-operand build (a multiple of 4)
+constexpr int ME_Z_BYTES = MMA_TM * ME_SMAX * 16 * 2;  // one of hi / lo: 128 rows x 16 ME_SMAX bf16
+constexpr int ME_STAGES = 12;
 constexpr int ME_B_BYTES = 16 * 256 * 2;               // 16 rank rows x up to 256 columns
 constexpr int ME_PT_MAX = 512;                         // pairs of a tile cached in shared memory
 constexpr int ME_NU_MAX = 512;                         // adapters listed per window
