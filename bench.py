@@ -414,9 +414,11 @@ def bench_ours(args, rank, world, dist):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        h0 = time.perf_counter()
         for _ in range(e2e_steps):
             native.lora_delta_apply_host(x_h, y_h, off_h, ids_h, al_h, wl.T, wl.P, rep["pool"].handle, None,
                                          rep["mapping"].handle, stream)
+        host_us = (time.perf_counter() - h0) * 1e6 / e2e_steps  # the calls' own host time (enqueue)
         e1.record(stream)
         e1.synchronize()
         ms_e2e = max_over_ranks(e0.elapsed_time(e1), dist, dev) / e2e_steps
@@ -461,7 +463,7 @@ def bench_ours(args, rank, world, dist):
         },
         "e2e": {"value": round(world * wl.T / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 6),
-                "api": "lora_delta_apply_host"},
+                "api": "lora_delta_apply_host", "host_us_per_call": round(host_us, 3)},
         "gpu_launches": (1 + n_apply_kernels) * steps_done,
         "clocks": clocks,
         "step_us_spread": spread_step,

@@ -787,6 +787,19 @@ lora_status host_step(const void *x_host, void *y_host, const int32_t *offsets_h
     const void *ax = al.x, *ay = al.y, *ao = al.off, *ai = al.ids, *aa = al.alpha;
     cudaError_t e = cudaSuccess;
     const bool direct = al.direct;
+    if (direct && aligned16(ax) && aligned16(ay) && ax != ay &&
+        choose_path(T, P, pool->r_max, pool->d_in, pool->d_out) == LORA_PATH_DECODE) {
+        // decode batches: the kernels read the pair lists, x and y straight
+        // from the pinned host buffers and write y back there (the mapping's
+        // CSR stage copies the pair lists; the shrink reads x rows, the expand
+        // y rows) -- the bytes cross the host link inside the step's kernels,
+        // with no copy launches before or after
+        lora_status s = lora_build_mapping(m, static_cast<const int32_t *>(ao), static_cast<const int32_t *>(ai),
+                                           static_cast<const float *>(aa), T, P, stream);
+        if (s == LORA_OK)
+            s = lora_delta_apply(ax, const_cast<void *>(ay), pool, ranks_dev, m, stream);
+        return s;
+    }
     if (direct) {
         CopySet in{};
         const void *srcs[5] = {ao, ai, aa, ax, ay};

@@ -397,9 +397,16 @@ def test_order_invariance():
     delta_gate(y1, acc)
 
 
-def test_host_entry_point_matches_device_path():
+@pytest.mark.parametrize("name", ["zipf", "sweep400"])
+def test_host_entry_point_matches_device_path(name):
+    """The host entry point from pinned buffers gives the device path's bits:
+    a decode batch (the kernels read and write host memory themselves) and a
+    400-token rank-64 batch (tensor-core path, copy kernels around it)."""
     import tenant_composite_lora_gb300 as tcl
-    wl = W.zipf_decode()
+    from tenant_composite_lora_gb300 import native
+    wl = W.zipf_decode() if name == "zipf" else W.rank_sweep(400)
+    want = native.LORA_PATH_DECODE if name == "zipf" else native.LORA_PATH_MMA
+    assert native.lora_dispatch_choose(wl.T, wl.P, wl.r_max, wl.d_in, wl.d_out) == want
     dw = DeviceWorkload(wl)
     try:
         ref = bf16_to_numpy_bits(dw.apply())
