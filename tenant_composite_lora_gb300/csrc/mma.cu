@@ -257,8 +257,10 @@ constexpr int ME_WORKERS = 256;                        // warps 0-7: lists, A op
 constexpr int ME_THREADS = ME_WORKERS + 64;            // warp 8: MMA issue; warp 9: B chunks by TMA
 constexpr int ME_SMAX = 12;                            // slots per A-operand build (a multiple of 4)
 constexpr int ME_Z_BYTES = MMA_TM * ME_SMAX * 16 * 2;  // one of hi / lo: 128 rows x 16 ME_SMAX bf16
-constexpr int ME_STAGES = 12;
-constexpr int ME_B_BYTES = 16 * 256 * 2;               // 16 rank rows x up to 256 columns
+constexpr int ME_B_BYTES = 16 * 256 * 2;               // one chunk: 16 rank rows x up to 256 columns
+constexpr int ME_SPS = 4;                              // chunks (slots) per ring stage: one barrier each way
+constexpr int ME_STAGES = 3;                           // ring stages of ME_SPS chunks (ME_SMAX chunks in all)
+static_assert(ME_SMAX % ME_SPS == 0, "an operand pass fills whole stages");
 constexpr int ME_PT_MAX = 512;                         // pairs of a tile cached in shared memory
 constexpr int ME_NU_MAX = 512;                         // adapters listed per window
 
@@ -281,7 +283,7 @@ struct MeLayout {
         zhi = 0;
         zlo = zhi + ME_Z_BYTES;
         b = zlo + ME_Z_BYTES;
-        cache = b + ME_STAGES * ME_B_BYTES;  // int2 [ME_PT_MAX]: sorted position, adapter (-1: none)
+        cache = b + ME_STAGES * ME_SPS * ME_B_BYTES;  // int2 [ME_PT_MAX]: sorted position, adapter (-1: none)
         list = cache + ME_PT_MAX * 8;        // int [ME_NU_MAX]: adapters of the window, ascending
         lrank = list + ME_NU_MAX * 4;        // int [ME_NU_MAX]: their ranks
         sbase = lrank + ME_NU_MAX * 4;       // int [ME_NU_MAX + 1]: first slot of each
@@ -369,10 +371,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 }
 
 // The B producer warp (lane 0): for each build, streams the B chunks of its
-// (unit, slot) sequence through a ring of ME_STAGES stages -- one 3-D TMA box
-// {64 columns, 16 rank rows, BN / 64 column blocks} per chunk, which lands in
-// the MN-major swizzled operand layout -- refilling a stage as soon as the
-// MMAs that read it complete.  Per-slot rows are resolved once per build.
+// (unit, slot) sequence through a ring of ME_STAGES stages of ME_SPS chunks
+// -- one 3-D TMA box {64 columns, 16 rank rows, BN / 64 column blocks} per
+// chunk, which lands in the MN-major swizzled operand layout, and one
+// barrier per stage, so that each handshake with the MMA warp covers ME_SPS
+// chunks -- refilling a stage as soon as the MMAs that read it complete.
+// Per-slot rows are resolved once per build.
 template <int BN>
 __device__ __forceinline__ void me_producer_warp(const CUtensorMap &map_b, const MmaExpandArgs &a,
                                                  unsigned char *smem, const MeLayout &L, uint64_t *full_b,
@@ -405,13 +409,17 @@ __device__ __forceinline__ void me_producer_warp(const CUtensorMap &map_b, const
         for (int uu = bd.u0; uu < bd.u1; ++uu) {
             const int z0 = (uu % a.n_nt) * (BN / 64);
 #pragma unroll
-            for (int j = 0; j < ME_SMAX; ++j) {
+            for (int j = 0; j < ME_SMAX; j += ME_SPS) {
                 if (j < nsl) {
                     const int gs = g++, st = gs % ME_STAGES;
                     if (gs >= ME_STAGES && !mbar_wait_bounded(&empty_b[st], ((gs / ME_STAGES) - 1) & 1, status))
                         return;
-                    mbar_arrive_expect_tx(&full_b[st], 16 * BN * 2);
-                    tma_load_3d(sb + st * ME_B_BYTES, &map_b, 0, rows[j], z0, &full_b[st]);
+                    const int nch = min(ME_SPS, nsl - j);  // chunks of this stage
+                    mbar_arrive_expect_tx(&full_b[st], (uint32_t)(nch * 16 * BN * 2));
+#pragma unroll
+                    for (int h = 0; h < ME_SPS; ++h)
+                        if (h < nch)
+                            tma_load_3d(sb + (st * ME_SPS + h) * ME_B_BYTES, &map_b, 0, rows[j + h], z0, &full_b[st]);
                 }
             }
         }
@@ -460,32 +468,41 @@ __device__ __forceinline__ void me_mma_warp(unsigned char *smem, const MeLayout 
             }
             const uint32_t dt = taddr + (uint32_t)(b * BN);
 #pragma unroll
-            for (int j = 0; j < ME_SMAX; ++j) {
+            for (int j = 0; j < ME_SMAX; j += ME_SPS) {
                 if (j < nsl && ok) {
                     const int gs = g++, st = gs % ME_STAGES;
                     ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full_b[st], (gs / ME_STAGES) & 1, status));
                     if (ok) {
-                        unsigned char *bs = sb + st * ME_B_BYTES;
-                        const int kr = krs[j];
-                        if (kr < 16) {
-                            const int nz = (16 - kr) * (BN / 64) * 8;  // 16-byte pieces of rank rows kr..15
-                            for (int e = lane; e < nz; e += 32) {
-                                const int piece = e & 7, rest = e >> 3;
-                                const int at = rest % (BN / 64), rr = kr + rest / (BN / 64);
-                                *reinterpret_cast<uint4 *>(bs + at * 2048 + (rr >> 3) * 1024 + (rr & 7) * 128 +
-                                                           piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int h = 0; h < ME_SPS; ++h) {
+                            const int jj = j + h;
+                            if (jj >= nsl)
+                                break;
+                            unsigned char *bs = sb + (st * ME_SPS + h) * ME_B_BYTES;
+                            const int kr = krs[jj];
+                            if (kr < 16) {
+                                const int nz = (16 - kr) * (BN / 64) * 8;  // 16-byte pieces of rank rows kr..15
+                                for (int e = lane; e < nz; e += 32) {
+                                    const int piece = e & 7, rest = e >> 3;
+                                    const int at = rest % (BN / 64), rr = kr + rest / (BN / 64);
+                                    *reinterpret_cast<uint4 *>(bs + at * 2048 + (rr >> 3) * 1024 + (rr & 7) * 128 +
+                                                               piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+                                }
+                                fence_proxy_async_smem();
                             }
-                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tc_fence_after();
+                                const uint64_t bdesc = umma_desc_sw128_mn(smem_u32(bs), 2048, 1024);
+                                const uint32_t zo = (uint32_t)((jj >> 2) * (MMA_TM * 128) + (jj & 3) * 32);
+                                umma_bf16(dt, umma_desc_sw128(zhi + zo), bdesc, idesc, !(bd.first && jj == 0));
+                                umma_bf16(dt, umma_desc_sw128(zlo + zo), bdesc, idesc, true);
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
                         if (lane == 0) {
-                            tc_fence_after();
-                            const uint64_t bdesc = umma_desc_sw128_mn(smem_u32(bs), 2048, 1024);
-                            const uint32_t zo = (uint32_t)((j >> 2) * (MMA_TM * 128) + (j & 3) * 32);
-                            umma_bf16(dt, umma_desc_sw128(zhi + zo), bdesc, idesc, !(bd.first && j == 0));
-                            umma_bf16(dt, umma_desc_sw128(zlo + zo), bdesc, idesc, true);
-                            umma_commit(&empty_b[st]);
-                            if (bd.last && j == nsl - 1)
+                            umma_commit(&empty_b[st]);  // the stage is free once its MMAs complete
+                            if (bd.last && j + ME_SPS >= nsl)
                                 umma_commit(&acc_full[b]);
                         }
                         __syncwarp();
