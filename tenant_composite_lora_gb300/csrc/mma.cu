@@ -254,7 +254,9 @@ __global__ void __launch_bounds__(MS_THREADS, 1)
 // ---------------------------------------------------------------- expand
 
 constexpr int ME_WORKERS = 256;                        // warps 0-7: lists, A operand, epilogue
-constexpr int ME_THREADS = ME_WORKERS + 64;            // warp 8: MMA issue; warp 9: B chunks by TMA
+constexpr int ME_EPI = 128;                            // warps 10-13: epilogue (one TMEM lane quarter each)
+constexpr int ME_THREADS = ME_WORKERS + 64 + ME_EPI;   // warp 8: MMA issue; warp 9: B chunks by TMA
+constexpr int ME_JOBS = 4;                             // epilogue jobs queued by the workers
 constexpr int ME_SMAX = 12;                            // slots per A-operand build (a multiple of 4)
 constexpr int ME_Z_BYTES = MMA_TM * ME_SMAX * 16 * 2;  // one of hi / lo: 128 rows x 16 ME_SMAX bf16
 constexpr int ME_B_BYTES = 16 * 256 * 2;               // one chunk: 16 rank rows x up to 256 columns
@@ -292,6 +294,11 @@ struct MeLayout {
         wpre = bitmap + words * 4;           // int [words]: set bits before each word
         total = wpre + words * 4 + 1024;
     }
+};
+
+// One unit's epilogue, handed from the workers to the epilogue warps.
+struct MeJob {
+    int uu, t0, nrows, gi, done;
 };
 
 // One A-operand build, handed from the workers to the MMA warp.
@@ -527,6 +534,8 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                                                             ~static_cast<uintptr_t>(1023));
     const MeLayout L(a.pool.capacity);
     __shared__ uint64_t full_b[ME_STAGES], empty_b[ME_STAGES], zready, zfree, acc_full[2], acc_empty[2];
+    __shared__ uint64_t job_full[ME_JOBS], job_empty[ME_JOBS];
+    __shared__ MeJob s_jobs[ME_JOBS];
     __shared__ uint32_t s_taddr;
     __shared__ int s_scan[ME_WORKERS / 32 + 1];
     __shared__ MeBuild s_build;
@@ -547,7 +556,11 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
         mbar_init(&zfree, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], ME_WORKERS);
+            mbar_init(&acc_empty[b], ME_EPI);
+        }
+        for (int j = 0; j < ME_JOBS; ++j) {
+            mbar_init(&job_full[j], 1);
+            mbar_init(&job_empty[j], ME_EPI / 32);
         }
         fence_mbar_init();
     }
@@ -576,6 +589,70 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
         __syncthreads();  // (B)
         return;
     }
+    if (warp >= ME_WORKERS / 32 + 2) {
+        // epilogue warps: each unit's y + D, rounded once, in the order the
+        // workers queue them; warp w reads accumulator lanes 32 (w % 4).. (its
+        // TMEM lane quarter), every column of the unit in two halves
+        __syncthreads();  // (A)
+        tc_fence_after();
+        const uint32_t taddr = s_taddr;
+        const int lq = warp & 3, row = lq * 32 + lane;
+        const int d_out = a.pool.d_out;
+        constexpr int HALF = BN / 2, NV = HALF / 8;
+        for (int j = 0;; ++j) {
+            const int slot = j % ME_JOBS;
+            if (!mbar_wait_bounded(&job_full[slot], (j / ME_JOBS) & 1, status))
+                break;
+            const MeJob jb = s_jobs[slot];
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&job_empty[slot]);  // copied: the slot may be refilled
+            if (jb.done)
+                break;
+            const int b = jb.gi & 1;
+            const bool live = row < jb.nrows;
+            __nv_bfloat16 *yr = a.y + (size_t)(jb.t0 + (live ? row : 0)) * d_out + (jb.uu % a.n_nt) * BN;
+            bool ok = true;
+#pragma unroll 1
+            for (int hf = 0; hf < 2; ++hf) {
+                uint4 yv[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    yv[v] = live ? *reinterpret_cast<const uint4 *>(yr + hf * HALF + 8 * v)
+                                 : make_uint4(0u, 0u, 0u, 0u);
+                if (hf == 0) {
+                    ok = mbar_wait_bounded(&acc_full[b], (jb.gi >> 1) & 1, status);
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int c = 0; c < HALF; c += 16) {
+                    float v[16];
+                    tmem_ld16(taddr + ((uint32_t)(lq * 32) << 16) + (uint32_t)(b * BN + hf * HALF + c), v);
+                    if (live && ok) {
+                        uint4 o[2];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const uint4 w = yv[c / 8 + hh];
+                            const float *d = v + 8 * hh;
+                            o[hh] = make_uint4(pack_bf16x2(bf16lo(w.x) + d[0], bf16hi(w.x) + d[1]),
+                                               pack_bf16x2(bf16lo(w.y) + d[2], bf16hi(w.y) + d[3]),
+                                               pack_bf16x2(bf16lo(w.z) + d[4], bf16hi(w.z) + d[5]),
+                                               pack_bf16x2(bf16lo(w.w) + d[6], bf16hi(w.w) + d[7]));
+                        }
+                        *reinterpret_cast<uint4 *>(yr + hf * HALF + c) = o[0];
+                        *reinterpret_cast<uint4 *>(yr + hf * HALF + c + 8) = o[1];
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&acc_empty[b]);
+            if (!ok)
+                break;
+        }
+        __syncwarp();
+        __syncthreads();  // (B)
+        return;
+    }
 
     // ------------------------------------------------------------ workers
     unsigned char *zhi = smem + L.zhi, *zlo = smem + L.zlo;
@@ -587,10 +664,8 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
     uint32_t *bitmap = reinterpret_cast<uint32_t *>(smem + L.bitmap);
     int *wpre = reinterpret_cast<int *>(smem + L.wpre);
     const int nwords = (a.pool.capacity + 31) / 32;
-    const int d_out = a.pool.d_out;
 
     bool synced = false;
-    uint32_t taddr = 0;
     int nb = 0, freed = 0, gi = 0;
     auto wait_free = [&]() {  // every build handed over so far has been consumed
         while (freed < nb) {
@@ -715,43 +790,19 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
         }
     };
 
-    // epilogue of unit uu (running index gi): y + D, rounded once; warp w reads
-    // lanes 32 (w % 4).. of the accumulator, column half w / 4
-    auto epilogue = [&](int uu) {
-        constexpr int HALF = BN / 2, NV = HALF / 8;
-        const int b = gi & 1;
-        const int lq = warp & 3, hf = warp >> 2;
-        const int row = lq * 32 + lane;
-        const bool live = row < nrows;
-        __nv_bfloat16 *yr = a.y + (size_t)(t0 + (live ? row : 0)) * d_out + (uu % a.n_nt) * BN + hf * HALF;
-        uint4 yv[NV];
-#pragma unroll
-        for (int v = 0; v < NV; ++v)
-            yv[v] = live ? *reinterpret_cast<const uint4 *>(yr + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
-        const bool ok = mbar_wait_bounded(&acc_full[b], (gi >> 1) & 1, status);
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < HALF; c += 16) {
-            float v[16];
-            tmem_ld16(taddr + ((uint32_t)(lq * 32) << 16) + (uint32_t)(b * BN + hf * HALF + c), v);
-            if (live && ok) {
-                uint4 o[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint4 w = yv[c / 8 + hh];
-                    const float *d = v + 8 * hh;
-                    o[hh] = make_uint4(pack_bf16x2(bf16lo(w.x) + d[0], bf16hi(w.x) + d[1]),
-                                       pack_bf16x2(bf16lo(w.y) + d[2], bf16hi(w.y) + d[3]),
-                                       pack_bf16x2(bf16lo(w.z) + d[4], bf16hi(w.z) + d[5]),
-                                       pack_bf16x2(bf16lo(w.w) + d[6], bf16hi(w.w) + d[7]));
-                }
-                *reinterpret_cast<uint4 *>(yr + c) = o[0];
-                *reinterpret_cast<uint4 *>(yr + c + 8) = o[1];
-            }
+    // queues unit uu (running index gi) for the epilogue warps
+    int njob = 0;
+    auto push_job = [&](int uu, int done) {
+        const int slot = njob % ME_JOBS;
+        if (tid == 0) {
+            if (njob >= ME_JOBS)
+                mbar_wait_bounded(&job_empty[slot], ((njob / ME_JOBS) - 1) & 1, status);
+            s_jobs[slot] = MeJob{uu, t0, nrows, gi, done};
+            mbar_arrive(&job_full[slot]);  // release: the job is visible to the waiting warps
         }
-        tc_fence_before();
-        mbar_arrive(&acc_empty[b]);
-        ++gi;
+        ++njob;
+        if (!done)
+            ++gi;
     };
 
     for (int u = u_begin; u < u_end;) {
@@ -794,7 +845,6 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
             pdl_wait();  // z of the shrink is complete from here on
             __syncthreads();  // (A)
             tc_fence_after();
-            taddr = s_taddr;
             synced = true;
         }
         if (nu_total > 0) {
@@ -807,7 +857,7 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                     build_zsel(0, nu, 0, ns);  // one operand for every column tile of the token tile
                     publish(u, ut_end, 0, ns, nu, 1, 1, 0);
                     for (int uu = u; uu < ut_end; ++uu)
-                        epilogue(uu);
+                        push_job(uu, 0);
                 } else {
                     // several passes: two units at a time (one per accumulator) share each pass
                     for (int uu = u; uu < ut_end; uu += 2) {
@@ -819,7 +869,7 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                             publish(uu, u2, s0, s1, nu, p == 0, p == npass - 1, 0);
                         }
                         for (int v = uu; v < u2; ++v)
-                            epilogue(v);
+                            push_job(v, 0);
                     }
                 }
             } else {
@@ -839,7 +889,7 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                         }
                     }
                     for (int v = uu; v < u2; ++v)
-                        epilogue(v);
+                        push_job(v, 0);
                 }
             }
         }
@@ -852,6 +902,7 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
     }
     wait_free();
     publish(0, 0, 0, 0, 0, 0, 0, 1);
+    push_job(0, 1);
     tc_fence_before();
     __syncthreads();  // (B)
 }
