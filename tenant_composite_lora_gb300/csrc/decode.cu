@@ -49,6 +49,7 @@ struct DecShrinkArgs {
     MapDev m;
     int zs;    // z row stride (floats per pair)
     float *z;  // this projection's first z column: z[q * zs + j], q the CSR pair
+    int ngroups, gpc;  // row groups per pair, and groups per CTA (k_dec_shrink)
 };
 
 __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
@@ -64,11 +65,17 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
     return acc;
 }
 
-// One shrink item: CSR pair q, rank rows [j0, j0 + warps of the CTA).  Every
-// thread of the CTA calls it; it returns once the CTA's copies have landed.
-// report: set the status bit of an unusable adapter (one item per pair does).
-__device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *xs, int q, int j0, bool report)
+// One shrink item: CSR pair q, rank rows [j0, j0 + warps of the CTA), or with
+// GROUPS, ngrp such groups one after the other (warp w takes row w of each,
+// the x row staged once).  Every thread of the CTA calls it; it returns once
+// the CTA's copies have landed.  report: set the status bit of an unusable
+// adapter (one item per pair does).
+template <bool GROUPS>
+__device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *xs, int q, int j0, int ngrp,
+                                                bool report)
 {
+    if (!GROUPS)
+        ngrp = 1;
     // one round trip: the pair's token and adapter, and its alpha
     const int2 pc = a.m.pc[q];
     const float al = a.m.calpha[q];
@@ -108,35 +115,49 @@ __device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *x
         cp_async_wait_all();
         return;
     }
-    const bool live = j < k;
     cp_async_wait_all();
     __syncthreads();
-    float acc = 0.f;
+    const int W = blockDim.x >> 5;
+    for (int g = 0; g < ngrp; ++g) {
+        const int jw = j + g * W;  // this warp's row of group g
+        if (j0 + g * W >= k)
+            break;  // uniform: no row of this group is used
+        const bool live = jw < k;
+        const uint4 *arw = reinterpret_cast<const uint4 *>(a.pool.At + ((size_t)ad * r_max + (live ? jw : 0)) * d_in);
+        if (GROUPS && g > 0) {  // the first group's rows were fetched above
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-        const int i = u * 32 + lane;
-        if (i < nv)
-            acc = dot8(av[u], xs[i], acc);
-    }
-    // longer rows: further batches of 16 vectors per lane
-    for (int base = 32 * 16; base < nv; base += 32 * 16) {
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int i = base + u * 32 + lane;
-            av[u] = live && i < nv ? __ldcs(&ar[i]) : make_uint4(0u, 0u, 0u, 0u);
+            for (int u = 0; u < 16; ++u) {
+                const int i = u * 32 + lane;
+                av[u] = live && i < nv ? __ldcs(&arw[i]) : make_uint4(0u, 0u, 0u, 0u);
+            }
         }
+        float acc = 0.f;
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-            const int i = base + u * 32 + lane;
+            const int i = u * 32 + lane;
             if (i < nv)
                 acc = dot8(av[u], xs[i], acc);
         }
-    }
+        // longer rows: further batches of 16 vectors per lane
+        for (int base = 32 * 16; base < nv; base += 32 * 16) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1)
-        acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && lane == 0)
-        a.z[(size_t)q * a.zs + j] = al * acc;
+            for (int u = 0; u < 16; ++u) {
+                const int i = base + u * 32 + lane;
+                av[u] = live && i < nv ? __ldcs(&arw[i]) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int i = base + u * 32 + lane;
+                if (i < nv)
+                    acc = dot8(av[u], xs[i], acc);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (live && lane == 0)
+            a.z[(size_t)q * a.zs + jw] = al * acc;
+    }
 }
 
 __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a)
@@ -150,7 +171,18 @@ __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a
     // included -- must have completed.  Its prologue still overlaps the work
     // below.
     pdl_launch_dependents();
-    dec_shrink_item(a, xs, blockIdx.x, blockIdx.y * (blockDim.x >> 5), blockIdx.y == 0);
+    dec_shrink_item<false>(a, xs, blockIdx.x, blockIdx.y * (blockDim.x >> 5), 1, blockIdx.y == 0);
+}
+
+// The same over several row groups of its pair per CTA (long batches at large ranks).
+__global__ void __launch_bounds__(DS_THREADS) k_dec_shrink_groups(const DecShrinkArgs a)
+{
+    extern __shared__ __align__(16) uint4 xs[];  // the pair's x row
+    pdl_wait();               // as k_dec_shrink
+    pdl_launch_dependents();  // as k_dec_shrink
+    const int W = blockDim.x >> 5;
+    dec_shrink_item<true>(a, xs, blockIdx.x, blockIdx.y * a.gpc * W, min(a.gpc, a.ngroups - (int)blockIdx.y * a.gpc),
+                          blockIdx.y == 0);
 }
 
 struct DecExpandArgs {
@@ -436,7 +468,7 @@ __global__ void __launch_bounds__(256, 1) k_dec_fused(const DecFusedArgs a)
     const int G = gridDim.x;
     for (int it = blockIdx.x; it < a.P * a.ng; it += G) {
         const int q = it / a.ng, g = it % a.ng;
-        dec_shrink_item(a.s, xs, q, g * (blockDim.x >> 5), g == 0);
+        dec_shrink_item<false>(a.s, xs, q, g * (blockDim.x >> 5), 1, g == 0);
         __syncthreads();  // z rows written, x row consumed
         if (threadIdx.x == 0) {
             __threadfence();
@@ -477,7 +509,7 @@ __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink_multi(const MultiDecA
         ++j;
     const MultiDecProj &pj = a.p[j];
     const DecShrinkArgs sa{pj.x, pj.pool, pj.ranks, a.m, Z_ROW_FLOATS, a.m.z + pj.zoff};
-    dec_shrink_item(sa, xs, blockIdx.x, (yb - a.gpre[j]) * (blockDim.x >> 5), yb == a.gpre[j]);
+    dec_shrink_item<false>(sa, xs, blockIdx.x, (yb - a.gpre[j]) * (blockDim.x >> 5), 1, yb == a.gpre[j]);
 }
 
 // The expand of every projection in one grid: warp g runs (projection j,
@@ -522,6 +554,8 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     cudaGetDevice(&dev);
     if (attr_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(k_dec_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, DS_SMEM_MAX);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_dec_shrink_groups, cudaFuncAttributeMaxDynamicSharedMemorySize, DS_SMEM_MAX);
         if (e != cudaSuccess)
             return e;
         attr_dev = dev;
@@ -530,17 +564,30 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    // rows per CTA: 8, or 4 when r_max is small, so that a short batch's A
-    // rows spread over more SMs
+    // rows per group: 8, or 4 when r_max is small, so that a short batch's A
+    // rows spread over more SMs.  A CTA takes g of its pair's groups one after
+    // the other: the time goes as g (the CTA's chain) plus the waves of
+    // resident CTAs, items / (g * resident), least at g = sqrt(items /
+    // resident) -- one group per CTA for decode batches, several for long
+    // batches at large ranks (fewer CTAs that stop at the rank, the x row
+    // staged once for all of their groups)
     const int rpc = pool.r_max <= 8 ? 4 : 8;
+    sa.ngroups = (pool.r_max + rpc - 1) / rpc;
+    const long long resident = (long long)sm_count() * (rpc == 8 ? 3 : 6);
+    const long long items = (long long)P * sa.ngroups;
+    int g = 1;
+    while (g < sa.ngroups && (long long)g * g * resident < items)
+        ++g;
+    sa.gpc = g;
     cudaLaunchConfig_t scfg = {};
-    scfg.gridDim = dim3(P, (pool.r_max + rpc - 1) / rpc, 1);
+    scfg.gridDim = dim3(P, (sa.ngroups + sa.gpc - 1) / sa.gpc, 1);
     scfg.blockDim = dim3(32 * rpc, 1, 1);
     scfg.dynamicSmemBytes = (size_t)pool.d_in * 2;
     scfg.stream = st;
     scfg.attrs = attr;
     scfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&scfg, k_dec_shrink, sa);
+    cudaError_t e = sa.gpc > 1 ? cudaLaunchKernelEx(&scfg, k_dec_shrink_groups, sa)
+                               : cudaLaunchKernelEx(&scfg, k_dec_shrink, sa);
     if (e != cudaSuccess)
         return e;
     const int nc = (pool.d_out + 255) / 256;
