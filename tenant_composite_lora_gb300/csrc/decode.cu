@@ -222,29 +222,31 @@ __device__ __forceinline__ int dec_rank(const PoolDev &pool, const int32_t *rank
     return k > 0 ? k : 0;
 }
 
-// acc += sum_{j in [jb, k)} z[j] * B row j, 8 rows in flight at a time.
+// acc += sum_{j in [jb, k)} z[j] * B row j, R rows in flight at a time (rows
+// ascending whatever R: the same sums in the same order).
+template <int R>
 __device__ __forceinline__ void dec_rows(float (&acc)[8], const __nv_bfloat16 *br, const float *zr, int jb, int k,
                                          int d_out, bool on)
 {
-    for (int j = jb; j < k; j += 8) {
-        uint4 bb[8];
-        float zz[8];
+    for (int j = jb; j < k; j += R) {
+        uint4 bb[R];
+        float zz[R];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < R; ++u) {
             const bool v = j + u < k;
             bb[u] = v && on ? __ldg(reinterpret_cast<const uint4 *>(br + (size_t)(j + u) * d_out))
                             : make_uint4(0u, 0u, 0u, 0u);
             zz[u] = v ? __ldcg(zr + j + u) : 0.f;
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
+        for (int u = 0; u < R; ++u)
             fma8(acc, zz[u], bb[u]);
     }
 }
 
 // One expand item: token t, 256-column chunk c, on one warp.  wait_pair(q)
 // is called before the first read of pair q's z (the shrink's output).
-template <int PP, class WaitPair>
+template <int PP, int R, class WaitPair>
 __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, int c, WaitPair wait_pair)
 {
     const int lane = threadIdx.x & 31;
@@ -290,7 +292,7 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
             for (int j = 0; j < DE_PR; ++j)
                 fma8(acc, zz[j], bpre[i][j]);
             if (k > DE_PR)
-                dec_rows(acc, a.pool.B + (size_t)pa[i] * r_max * d_out + col, zr, DE_PR, k, d_out, on);
+                dec_rows<R>(acc, a.pool.B + (size_t)pa[i] * r_max * d_out + col, zr, DE_PR, k, d_out, on);
         }
     }
     for (int p = p0 + PP; p < p1; ++p) {
@@ -300,7 +302,7 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
         const int k = dec_rank(a.pool, a.ranks, ad);
         if (k > 0) {
             wait_pair(p);
-            dec_rows(acc, a.pool.B + (size_t)ad * r_max * d_out + col, a.z + (size_t)p * a.zs, 0, k, d_out, on);
+            dec_rows<R>(acc, a.pool.B + (size_t)ad * r_max * d_out + col, a.z + (size_t)p * a.zs, 0, k, d_out, on);
         }
     }
     uint4 o;
@@ -314,8 +316,10 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
 
 // PP pairs' rows are fetched before the dependency wait; MINB CTAs per SM
 // (two when the batch needs more than one wave of warps, at the price of one
-// fewer prefetched pair).
-template <int PP, int MINB>
+// fewer prefetched pair).  Past the prefetched rows, a pair's rows come RF at
+// a time: 16 for ranks above 16 on one CTA per SM (a shorter chain of round
+// trips per pair), else 8.
+template <int PP, int MINB, int RF>
 __global__ void __launch_bounds__(256, MINB) k_dec_expand(const DecExpandArgs a)
 {
     pdl_launch_dependents();  // the next kernel in the stream may start its prologue
@@ -325,7 +329,7 @@ __global__ void __launch_bounds__(256, MINB) k_dec_expand(const DecExpandArgs a)
     // consecutive warps: consecutive tokens on one column chunk, so the B rows
     // of an adapter several of them use come from L1 after the first
     bool waited = false;
-    dec_expand_item<PP>(a, g % a.T, g / a.T, [&](int) {
+    dec_expand_item<PP, RF>(a, g % a.T, g / a.T, [&](int) {
         if (!waited) {
             pdl_wait();  // z of the shrink
             waited = true;
@@ -479,7 +483,7 @@ __global__ void __launch_bounds__(256, 1) k_dec_fused(const DecFusedArgs a)
     const int nw = blockDim.x >> 5;
     bool ok = true;
     for (int wi = blockIdx.x * nw + (threadIdx.x >> 5); wi < a.e.T * a.e.nc; wi += G * nw)
-        dec_expand_item<DE_PP>(a.e, wi % a.e.T, wi / a.e.T, [&](int q) {
+        dec_expand_item<DE_PP, 8>(a.e, wi % a.e.T, wi / a.e.T, [&](int q) {
             if (ok)
                 ok = wait_count(m.zcnt + q, target, status);
         });
@@ -528,7 +532,7 @@ __global__ void __launch_bounds__(256, MINB) k_dec_expand_multi(const MultiDecAr
     const DecExpandArgs ea{pj.y, pj.pool, pj.ranks, a.m, a.T, Z_ROW_FLOATS, pj.nc, a.m.z + pj.zoff};
     const int gl = g - a.wpre[j];
     bool waited = false;
-    dec_expand_item<PP>(ea, gl % a.T, gl / a.T, [&](int) {
+    dec_expand_item<PP, 8>(ea, gl % a.T, gl / a.T, [&](int) {
         if (!waited) {
             pdl_wait();  // z of the shrink
             waited = true;
@@ -613,8 +617,10 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (warps > 8LL * sm_count())  // more than one wave at one 8-warp CTA per SM
-        return cudaLaunchKernelEx(&cfg, k_dec_expand<2, 2>, ea);
-    return cudaLaunchKernelEx(&cfg, k_dec_expand<DE_PP, 1>, ea);
+        return cudaLaunchKernelEx(&cfg, k_dec_expand<2, 2, 8>, ea);
+    if (pool.r_max > 16)
+        return cudaLaunchKernelEx(&cfg, k_dec_expand<DE_PP, 1, 16>, ea);
+    return cudaLaunchKernelEx(&cfg, k_dec_expand<DE_PP, 1, 8>, ea);
 }
 
 cudaError_t launch_decode_fused(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDev &pool, const int32_t *ranks,
