@@ -258,7 +258,7 @@ void free_mapping(lora_mapping *m)
         cudaGraphExecDestroy(m->exec);
     MapDev &d = m->dev;
     void *ptrs[] = {d.tok,  d.adapter, d.src, d.pos,     d.alpha, d.seg_adapter, d.seg_start,
-                    d.tile, d.tile_tok, d.tmp_tok, d.hdr, d.mtile, d.toff,     d.pc, d.calpha, d.zcnt, d.z,
+                    d.tile, d.tile_tok, d.hdr, d.mtile, d.toff,     d.pc, d.calpha, d.zcnt, d.z,
                     d.partial, d.ghist, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
@@ -549,7 +549,6 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.seg_start, (size_t)capacity + 1);
     if (e == cudaSuccess) e = dalloc(&d.tile, P);
     if (e == cudaSuccess) e = dalloc(&d.tile_tok, P * SHRINK_TT);
-    if (e == cudaSuccess) e = dalloc(&d.tmp_tok, P);
     if (e == cudaSuccess) e = dalloc(&d.hdr, (size_t)HDR_WORDS);
     if (e == cudaSuccess) e = dalloc(&d.mtile, (size_t)mma_tile_bound(max_pairs, capacity));
     if (e == cudaSuccess) e = dalloc(&d.toff, (size_t)max_tokens + 1);
@@ -1000,7 +999,7 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LORA_NOALLOC_SCRATCH_BYTES];
 
 struct NoallocLayout {
-    size_t tok, adapter, src, pos, alpha, tmp_tok, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, pc, calpha,
+    size_t tok, adapter, src, pos, alpha, seg_adapter, seg_start, tile, tile_tok, hdr, mtile, toff, pc, calpha,
         zcnt, z, ghist;
     size_t total;
 };
@@ -1022,7 +1021,6 @@ NoallocLayout noalloc_layout(int T, int P, int capacity, int r_max)
     L.src = take(4 * p);
     L.pos = take(4 * p);
     L.alpha = take(4 * p);
-    L.tmp_tok = take(4 * p);
     L.seg_adapter = take(4 * (size_t)capacity);
     L.seg_start = take(4 * ((size_t)capacity + 1));
     L.tile = take(16 * tiles);
@@ -1087,7 +1085,6 @@ extern "C" lora_status lora_delta_apply_noalloc(const void *x_dev, void *y_dev, 
     d.src = reinterpret_cast<int32_t *>(base + L.src);
     d.pos = reinterpret_cast<int32_t *>(base + L.pos);
     d.alpha = reinterpret_cast<float *>(base + L.alpha);
-    d.tmp_tok = reinterpret_cast<int32_t *>(base + L.tmp_tok);
     d.seg_adapter = reinterpret_cast<int32_t *>(base + L.seg_adapter);
     d.seg_start = reinterpret_cast<int32_t *>(base + L.seg_start);
     d.tile = reinterpret_cast<int4 *>(base + L.tile);

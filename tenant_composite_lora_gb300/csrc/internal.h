@@ -90,7 +90,6 @@ struct MapDev {
     int32_t *seg_adapter, *seg_start;    // [capacity], [capacity+1]
     int4 *tile;                          // [max_pairs] shrink tiles {adapter, q0, n, segment}
     int32_t *tile_tok;                   // [max_pairs][SHRINK_TT] tokens of each tile's pairs
-    int32_t *tmp_tok;                    // [max_pairs] scratch
     int32_t *hdr;                        // [HDR_WORDS]
     int4 *mtile;                         // [mma_tile_bound] tensor-core shrink tiles {adapter, q0, n, segment}
     int32_t *toff;                       // [max_tokens+1] copy of the batch's CSR offsets

@@ -145,14 +145,12 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_csr(const CsrArgs a)
     // writing anything.  Its own dependents may launch at once: they wait too.
     pdl_launch_dependents();
     const int32_t *off = a.off, *ids = a.ids, *alb = reinterpret_cast<const int32_t *>(a.alpha);
-    int32_t *tok = m.tmp_tok;
     if (a.staged) {
-        // offsets, ids and alpha bits consecutive in shared memory, then the token of each pair
+        // offsets, ids and alpha bits consecutive in shared memory
         stage_words(sh, a.off, T + 1, a.ids, P, alb, P);
         off = sh;
         ids = sh + T + 1;
         alb = ids + P;
-        tok = sh + T + 1 + 2 * P;
     }
     pdl_wait();  // the previous kernel (which may still read this mapping) is done
     if (tid == 0) {
@@ -183,21 +181,20 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_csr(const CsrArgs a)
             atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_OFFSETS);
         return;
     }
-    for (int t = tid; t <= T; t += nthr)
-        m.toff[t] = off[t];
-    for (int t = tid; t < T; t += nthr) {
-        const int p0 = off[t], p1 = off[t + 1];
-        for (int p = p0; p < p1; ++p)
-            tok[p] = t;
-    }
-    __syncthreads();  // tok complete (shared or global memory)
+    // a thread per token writes its pairs: {token, adapter} and alpha
     bool bad_id = false;
-    for (int p = tid; p < P; p += nthr) {
-        const int id = ids[p];
-        const bool ok = id >= 0 && id < cap;
-        bad_id |= !ok;
-        m.pc[p] = make_int2(tok[p], ok ? id : -1);
-        m.calpha[p] = __int_as_float(alb[p]);
+    for (int t = tid; t <= T; t += nthr) {
+        m.toff[t] = off[t];
+        if (t == T)
+            continue;
+        const int p0 = off[t], p1 = off[t + 1];
+        for (int p = p0; p < p1; ++p) {
+            const int id = ids[p];
+            const bool ok = id >= 0 && id < cap;
+            bad_id |= !ok;
+            m.pc[p] = make_int2(t, ok ? id : -1);
+            m.calpha[p] = __int_as_float(alb[p]);
+        }
     }
     if (bad_id)
         atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_ID);
@@ -425,7 +422,7 @@ cudaError_t launch_map_csr(const MapDev &m, const int32_t *offsets, const int32_
                            int P, int capacity, cudaStream_t st)
 {
     const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
-    const long long words = (long long)(T + 1) + 3LL * P;
+    const long long words = (long long)(T + 1) + 2LL * P;
     const int staged = words <= budget ? 1 : 0;
     // a short batch is one staging round of 256 threads (cheaper block-wide steps)
     const int threads = (T + 1 + 2LL * P <= 256LL * MAP_STAGE_U) ? 256 : MAP_THREADS;
