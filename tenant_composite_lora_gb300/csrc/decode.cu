@@ -616,6 +616,8 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (warps > 16LL * sm_count())  // more than one wave at two 8-warp CTAs per SM: three, one prefetched pair
+        return cudaLaunchKernelEx(&cfg, k_dec_expand<1, 3, 8>, ea);
     if (warps > 8LL * sm_count())  // more than one wave at one 8-warp CTA per SM
         return cudaLaunchKernelEx(&cfg, k_dec_expand<2, 2, 8>, ea);
     if (pool.r_max > 16)
