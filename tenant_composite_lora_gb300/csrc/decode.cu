@@ -1,5 +1,7 @@
-// Decode path: short batches, where every pair has its own x row and the
-// adapters' factors are read once.  Two launches chained with programmatic
+// Decode path: every batch below the dispatch table's prefill threshold (all
+// decode batches, and long batches at small ranks).  Every pair reads its own
+// x row and its adapter's factor rows (an adapter shared by several pairs
+// comes from L2 after the first).  Two launches chained with programmatic
 // dependent launch, every global access a 16-byte coalesced vector:
 //
 // Pairs are taken in CSR order (the mapping's CSR stage: per pair its token,
@@ -9,10 +11,11 @@
 //
 // 1. Shrink (LoRAForge page, "Approach" (4): direct reduction for short
 //    decode batches; DyMerge-LoRA page, "Core idea": the weight alpha folded
-//    in).  A CTA owns one pair q and 4 or 8 consecutive rank rows; its x row
-//    is staged once in shared memory and each warp streams one row of A_a
-//    (stored transposed, contiguous along d_in) against it, reducing with
-//    warp shuffles:  z[q][j] = alpha_q * sum_d x[tok_q][d] * A_a[d][j].
+//    in).  A CTA owns one pair q and 4 or 8 consecutive rank rows (long
+//    batches at large ranks: several such row groups of its pair in turn);
+//    its x row is staged once in shared memory and each warp streams one row
+//    of A_a (stored transposed, contiguous along d_in) against it, reducing
+//    with warp shuffles:  z[q][j] = alpha_q * sum_d x[tok_q][d] * A_a[d][j].
 //
 // 2. Expand (RowExpand, LoRAForge page, "Approach" (4)): a warp owns one
 //    token and 256 output columns (8 per lane); a CTA's warps are
@@ -21,8 +24,11 @@
 //    shrink it reads the token's pair list and issues the loads of y and of
 //    the first B rows (they do not depend on z; rows are fetched before the
 //    rank is known and used only below it); then it adds
-//    sum_pairs sum_j z[q][j] * B_a[j][cols] in fp32, 8 rows in flight at a
-//    time, and rounds once to bf16.
+//    sum_pairs sum_j z[q][j] * B_a[j][cols] in fp32, 8 or 16 rows in flight
+//    at a time, and rounds once to bf16.  The launch picks the instance that
+//    keeps the batch's warps in one wave where it can (fewer registers, more
+//    CTAs per SM, for long batches) and a CTA of 8 warps per (token, 256
+//    columns) for few tokens at large ranks.
 //
 // Both kernels order their loads so that each waits on as few dependent
 // round trips to memory as possible: a decode batch moves little data, and

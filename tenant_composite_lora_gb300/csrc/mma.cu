@@ -25,10 +25,12 @@
 //    MN-major 128-byte swizzled layout (B is stored row-major, d_out
 //    contiguous).  D (128 x BN fp32) accumulates in tensor memory over all
 //    slots, in two buffers so that one unit's epilogue (y + D, rounded once
-//    to bf16) overlaps the next unit's MMAs; one warp streams B and issues
-//    the MMAs, eight build the operand and run the epilogue.  Rank rows at
-//    or beyond k of a partial chunk are zeroed in shared memory before use,
-//    so padding never reaches the sum.
+//    to bf16) overlaps the next unit's MMAs.  Warp roles: one streams B by
+//    TMA through a ring of stages of ME_SPS chunks (one barrier per stage),
+//    one issues the MMAs, eight list the tile's adapters and build the
+//    operand (ME_SMAX slots per pass), four run the epilogues of the units
+//    the workers queue.  Rank rows at or beyond k of a partial chunk are
+//    zeroed in shared memory before use, so padding never reaches the sum.
 //
 // LoRAForge page, "Approach" (5) (a path fixed per phase and shape) and the
 // DyMerge-LoRA page, "Core idea" (tuples reordered by adapter so that one CTA
