@@ -389,8 +389,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 template <int BN>
 __device__ __forceinline__ void me_producer_warp(const CUtensorMap &map_b, const MmaExpandArgs &a,
                                                  unsigned char *smem, const MeLayout &L, uint64_t *full_b,
-                                                 uint64_t *empty_b, uint64_t *zready, const MeBuild *s_build,
-                                                 int32_t *status)
+                                                 uint64_t *empty_b, uint64_t *lready, uint64_t *lack,
+                                                 const MeBuild *s_build, int32_t *status)
 {
     if ((threadIdx.x & 31) != 0)
         return;
@@ -400,9 +400,12 @@ __device__ __forceinline__ void me_producer_warp(const CUtensorMap &map_b, const
     const int r_max = a.pool.r_max;
     int g = 0;  // ring sequence
     for (int nb = 0;; ++nb) {
-        if (!mbar_wait_bounded(zready, nb & 1, status))
+        // a build's slots are listed before its operand is built: its B
+        // chunks stream while the workers build
+        if (!mbar_wait_bounded(lready, nb & 1, status))
             return;
-        const MeBuild bd = *s_build;
+        const MeBuild bd = s_build[nb & 1];
+        mbar_arrive(lack);  // read: the workers may announce the next build
         if (bd.done)
             return;
         const int nsl = bd.s1 - bd.s0;
@@ -454,7 +457,7 @@ __device__ __forceinline__ void me_mma_warp(unsigned char *smem, const MeLayout 
     for (int nb = 0;; ++nb) {
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(zready, nb & 1, status)))
             return;
-        const MeBuild bd = *s_build;
+        const MeBuild bd = s_build[nb & 1];
         if (bd.done)
             return;
         const int nsl = bd.s1 - bd.s0;
@@ -536,11 +539,11 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                                                             ~static_cast<uintptr_t>(1023));
     const MeLayout L(a.pool.capacity);
     __shared__ uint64_t full_b[ME_STAGES], empty_b[ME_STAGES], zready, zfree, acc_full[2], acc_empty[2];
-    __shared__ uint64_t job_full[ME_JOBS], job_empty[ME_JOBS];
+    __shared__ uint64_t job_full[ME_JOBS], job_empty[ME_JOBS], lready, lack;
     __shared__ MeJob s_jobs[ME_JOBS];
     __shared__ uint32_t s_taddr;
     __shared__ int s_scan[ME_WORKERS / 32 + 1];
-    __shared__ MeBuild s_build;
+    __shared__ MeBuild s_build[2];  // build n in slot n % 2: the next one may be announced early
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *status = a.m.hdr + HDR_STATUS;
@@ -555,6 +558,8 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
             mbar_init(&empty_b[s], 1);
         }
         mbar_init(&zready, ME_WORKERS);
+        mbar_init(&lready, 1);
+        mbar_init(&lack, 1);
         mbar_init(&zfree, 1);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -577,7 +582,7 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
         __syncthreads();  // (A) accumulator address visible
         tc_fence_after();
         const uint32_t taddr = s_taddr;
-        me_mma_warp<BN>(smem, L, full_b, empty_b, &zready, &zfree, acc_full, acc_empty, &s_build, taddr, status);
+        me_mma_warp<BN>(smem, L, full_b, empty_b, &zready, &zfree, acc_full, acc_empty, s_build, taddr, status);
         __syncwarp();
         __syncthreads();  // (B) every epilogue has read its accumulator
         tc_fence_after();
@@ -586,7 +591,7 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
     }
     if (warp == ME_WORKERS / 32 + 1) {
         __syncthreads();  // (A)
-        me_producer_warp<BN>(map_b, a, smem, L, full_b, empty_b, &zready, &s_build, status);
+        me_producer_warp<BN>(map_b, a, smem, L, full_b, empty_b, &lready, &lack, s_build, status);
         __syncwarp();
         __syncthreads();  // (B)
         return;
@@ -675,9 +680,21 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
             ++freed;
         }
     };
-    auto publish = [&](int u0, int u1, int s0, int s1, int nu, int first, int last, int done) {
-        if (tid == 0)
-            s_build = MeBuild{u0, u1, s0, s1, nu, first, last, gi, done};
+    // a build in two steps: announce (its slots, for the B producer) once the
+    // lists are in place and the build before the previous one is consumed,
+    // then ready (the operand, for the MMA warp) once it is built
+    auto announce = [&](int u0, int u1, int s0, int s1, int nu, int first, int last, int done) {
+        if (tid == 0) {
+            // at most one announcement outstanding: the producer has read the
+            // previous one (so a barrier phase is never passed unseen, and the
+            // slot reused here was read two builds ago)
+            if (nb > 0)
+                mbar_wait_bounded(&lack, (nb - 1) & 1, status);
+            s_build[nb & 1] = MeBuild{u0, u1, s0, s1, nu, first, last, gi, done};
+            mbar_arrive(&lready);
+        }
+    };
+    auto ready = [&]() {
         fence_proxy_async_smem();
         mbar_arrive(&zready);
         ++nb;
@@ -856,8 +873,9 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                 const int nu = nu_total;
                 const int npass = (ns + ME_SMAX - 1) / ME_SMAX;
                 if (npass == 1) {
+                    announce(u, ut_end, 0, ns, nu, 1, 1, 0);
                     build_zsel(0, nu, 0, ns);  // one operand for every column tile of the token tile
-                    publish(u, ut_end, 0, ns, nu, 1, 1, 0);
+                    ready();
                     for (int uu = u; uu < ut_end; ++uu)
                         push_job(uu, 0);
                 } else {
@@ -866,9 +884,12 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                         const int u2 = min(uu + 2, ut_end);
                         for (int p = 0; p < npass; ++p) {
                             const int s0 = p * ME_SMAX, s1 = min(ns, s0 + ME_SMAX);
+                            // the pass's B chunks stream while the previous
+                            // pass's MMAs finish and this operand is built
+                            announce(uu, u2, s0, s1, nu, p == 0, p == npass - 1, 0);
                             wait_free();
                             build_zsel(0, nu, s0, s1);
-                            publish(uu, u2, s0, s1, nu, p == 0, p == npass - 1, 0);
+                            ready();
                         }
                         for (int v = uu; v < u2; ++v)
                             push_job(v, 0);
@@ -886,8 +907,9 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
                         for (int p = 0; p < npass; ++p) {
                             const int s0 = p * ME_SMAX, s1 = min(ns, s0 + ME_SMAX);
                             wait_free();
+                            announce(uu, u2, s0, s1, nu, w == 0 && p == 0, w == nwin - 1 && p == npass - 1, 0);
                             build_zsel(w0, nu, s0, s1);
-                            publish(uu, u2, s0, s1, nu, w == 0 && p == 0, w == nwin - 1 && p == npass - 1, 0);
+                            ready();
                         }
                     }
                     for (int v = uu; v < u2; ++v)
@@ -903,7 +925,8 @@ __global__ void __launch_bounds__(ME_THREADS, 1)
         synced = true;
     }
     wait_free();
-    publish(0, 0, 0, 0, 0, 0, 0, 1);
+    announce(0, 0, 0, 0, 0, 0, 0, 1);
+    ready();
     push_job(0, 1);
     tc_fence_before();
     __syncthreads();  // (B)
