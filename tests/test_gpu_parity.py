@@ -225,12 +225,14 @@ def _prefill_reference(y_zero: bool):
     return _PREFILL_REF[y_zero]
 
 
-@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA, PATH_SPLIT])
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA, PATH_SPLIT, PATH_DECODE])
 def test_prefill_full_size_every_token(path):
     """The whole sparse-prefill batch (3250 tokens, 6500 pairs) in the
     benchmark's launch configuration (the dispatch table sends it to the
     tensor-core path), every element of every token against the oracle's
-    delta: a tile-boundary or scheduling slip anywhere in the batch fails."""
+    delta: a tile-boundary or scheduling slip anywhere in the batch fails.
+    Forced onto the decode path the batch takes the long-batch instances
+    (two row groups per shrink CTA, the one-wave expand)."""
     wl, _, acc = _prefill_reference(True)
     y, st = run_gpu(wl, path=path)
     assert st == 0
