@@ -280,11 +280,14 @@ int lora_dispatch_choose(int T, int P, int r_max, int d_in, int d_out);
  * and reused after.  Stream-ordered: y_host is valid after the stream
  * synchronises.  Same element layouts as the device calls.
  * When all five host buffers are page-locked (device-addressable) and the
- * dispatch table picks the decode path, the step's own kernels read the pair
- * lists, x and y from host memory and write y back there (no copy launch);
+ * dispatch table picks the decode path, one copy kernel brings x into the
+ * device staging (each byte crosses the host link once, overlapped by the
+ * mapping stage) and the step's own kernels read the pair lists and y from
+ * host memory and write y back there (no copy launch after the step);
  * other page-locked steps move the buffers with two launches of a copy
  * kernel that reads and writes host memory directly (one in, one out);
- * pageable buffers take one cudaMemcpyAsync each.
+ * pageable buffers take one cudaMemcpyAsync each.  A step may take as x the
+ * y of the step before it on the same stream.
  * A call that repeats the previous call's arguments exactly (pointers, T, P,
  * pool, ranks, stream) is captured into a CUDA graph of the whole step, and
  * later calls with those arguments replay it (one graph launch instead of

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 struct lora_pool {
     int d_in, d_out, r_max, capacity, device;
@@ -140,6 +141,53 @@ __global__ void __launch_bounds__(256) k_copy_set(const CopySet c)
         for (unsigned long long j = nv * 16 + tid; j < n; j += nthr)
             d[j] = s[j];
     }
+}
+
+// A decode step's x rows from pinned host memory into the device staging,
+// once per step: the shrink reads a token's row once per pair and rank-row
+// group, and those repeats stay in device memory instead of crossing the
+// host link again.  Launched as a programmatic dependent, it lets the
+// mapping stage behind it start at once (that stage stages its own inputs,
+// then waits for this grid); it reads the host buffer only after its own
+// wait, since the kernel ahead (the previous step's expand) may still be
+// writing a y that is this step's x.  Both ends 16-byte aligned, n16 vectors.
+constexpr int HI_UNROLL = 2;  // 16-byte loads a thread keeps in flight: 8 KB per CTA
+
+__global__ void __launch_bounds__(256) k_host_in(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                                                 unsigned long long n16)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const unsigned long long i0 = (unsigned long long)blockIdx.x * 256 * HI_UNROLL + threadIdx.x;
+    uint4 v[HI_UNROLL];
+#pragma unroll
+    for (int u = 0; u < HI_UNROLL; ++u) {
+        const unsigned long long i = i0 + 256ull * u;
+        v[u] = i < n16 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < HI_UNROLL; ++u) {
+        const unsigned long long i = i0 + 256ull * u;
+        if (i < n16)
+            dst[i] = v[u];
+    }
+}
+
+cudaError_t launch_host_in(const void *src, void *dst, size_t bytes, cudaStream_t st)
+{
+    const unsigned long long n16 = bytes / 16;
+    if (n16 == 0)
+        return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((n16 + 256ull * HI_UNROLL - 1) / (256ull * HI_UNROLL)), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_host_in, static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), n16);
 }
 
 // SM count of the current device, cached per host thread (device and count
@@ -786,17 +834,20 @@ lora_status host_step(const void *x_host, void *y_host, const int32_t *offsets_h
     const void *ax = al.x, *ay = al.y, *ao = al.off, *ai = al.ids, *aa = al.alpha;
     cudaError_t e = cudaSuccess;
     const bool direct = al.direct;
-    if (direct && aligned16(ax) && aligned16(ay) && ax != ay &&
+    if (direct && aligned16(ax) && aligned16(ay) && ax != ay && xb % 16 == 0 &&
         choose_path(T, P, pool->r_max, pool->d_in, pool->d_out) == LORA_PATH_DECODE) {
-        // decode batches: the kernels read the pair lists, x and y straight
-        // from the pinned host buffers and write y back there (the mapping's
-        // CSR stage copies the pair lists; the shrink reads x rows, the expand
-        // y rows) -- the bytes cross the host link inside the step's kernels,
-        // with no copy launches before or after
+        // decode batches: x crosses the host link once, into the device
+        // staging, by one copy kernel that the mapping's CSR stage overlaps;
+        // the CSR stage reads the pair lists and the expand reads and writes
+        // y straight from and to the pinned host buffers (each byte crosses
+        // once): no copy launch after the step
+        e = launch_host_in(ax, m->sx, xb, st);
+        if (e != cudaSuccess)
+            return from_cuda(e);
         lora_status s = lora_build_mapping(m, static_cast<const int32_t *>(ao), static_cast<const int32_t *>(ai),
                                            static_cast<const float *>(aa), T, P, stream);
         if (s == LORA_OK)
-            s = lora_delta_apply(ax, const_cast<void *>(ay), pool, ranks_dev, m, stream);
+            s = lora_delta_apply(m->sx, const_cast<void *>(ay), pool, ranks_dev, m, stream);
         return s;
     }
     if (direct) {

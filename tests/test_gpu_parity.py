@@ -402,8 +402,9 @@ def test_order_invariance():
 @pytest.mark.parametrize("name", ["zipf", "sweep400"])
 def test_host_entry_point_matches_device_path(name):
     """The host entry point from pinned buffers gives the device path's bits:
-    a decode batch (the kernels read and write host memory themselves) and a
-    400-token rank-64 batch (tensor-core path, copy kernels around it)."""
+    a decode batch (x brought over once by a copy kernel, the pair lists and
+    y read and written in host memory by the step's kernels) and a 400-token
+    rank-64 batch (tensor-core path, copy kernels around it)."""
     import tenant_composite_lora_gb300 as tcl
     from tenant_composite_lora_gb300 import native
     wl = W.zipf_decode() if name == "zipf" else W.rank_sweep(400)
@@ -424,6 +425,45 @@ def test_host_entry_point_matches_device_path(name):
     finally:
         dw.close()
     np.testing.assert_array_equal(got, ref)
+
+
+def test_host_entry_point_chained_steps():
+    """Each step's x is the previous step's y (a square pool, d_in = d_out),
+    host steps enqueued back to back on one stream: the step that brings x
+    over the host link must not read it before the step ahead has written
+    it.  The chain's bits equal the same chain on device buffers."""
+    import tenant_composite_lora_gb300 as tcl
+    from tenant_composite_lora_gb300 import native
+    wl = W.make("distinct")
+    assert wl.d_in == wl.d_out
+    assert native.lora_dispatch_choose(wl.T, wl.P, wl.r_max, wl.d_in, wl.d_out) == native.LORA_PATH_DECODE
+    n = 5
+    rng = np.random.default_rng(12)
+    starts = [W.f32_to_bf16_bits(rng.standard_normal(wl.x.shape).astype(np.float32)) for _ in range(n + 1)]
+    dw = DeviceWorkload(wl)
+    s = torch.cuda.Stream()
+    try:
+        dev = [torch.from_numpy(v.view(np.int16).copy()).cuda() for v in starts]
+        hst = [torch.from_numpy(v.view(np.int16).copy()).pin_memory() for v in starts]
+        off = torch.from_numpy(wl.offsets).pin_memory()
+        ids = torch.from_numpy(wl.ids).pin_memory()
+        al = torch.from_numpy(wl.alpha).pin_memory()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            for i in range(n):
+                native.lora_delta_apply(dev[i], dev[i + 1], dw.pool.handle, None, dw.mapping.handle, s)
+            for i in range(n):
+                tcl.lora_delta_apply_host(hst[i], hst[i + 1], off, ids, al, wl.T, wl.P, dw.pool.handle, None,
+                                          dw.mapping.handle, s)
+        s.synchronize()
+        assert dw.mapping.status(s) == 0
+        want = [t.cpu().numpy().view(np.uint16) for t in dev]
+        got = [t.numpy().view(np.uint16) for t in hst]
+    finally:
+        dw.close()
+    for i in range(1, n + 1):
+        np.testing.assert_array_equal(got[i], want[i], err_msg=f"step {i}")
+    assert not np.array_equal(want[n], starts[n])
 
 
 def _host_calls(wl, dw, x_host, y_host, off, ids, al, n_calls, before_call=None):
