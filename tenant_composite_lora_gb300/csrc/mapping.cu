@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_csr(const CsrArgs a)
         off = sh;
         ids = sh + T + 1;
         alb = ids + P;
+        __syncthreads();  // every thread reads words that others staged
     }
     pdl_wait();  // the previous kernel (which may still read this mapping) is done
     if (tid == 0) {
@@ -161,7 +162,7 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_csr(const CsrArgs a)
         m.hdr[HDR_EPOCH] = 0;
         m.hdr[HDR_DEXIT] = 0;
         m.hdr[HDR_T] = T;
-        m.hdr[HDR_BUILD] = m.hdr[HDR_BUILD] + 1;  // the sorted tuples are stale from here on
+        atomicAdd(&m.hdr[HDR_BUILD], 1);  // the sorted tuples are stale from here on (no round trip)
     }
     for (int p = tid; p < P; p += nthr)
         m.zcnt[p] = 0;
