@@ -20,8 +20,8 @@
 // their own kernels; it returns at once when the current build is already
 // sorted) performs a stable counting sort on the adapter id over the CSR
 // copy (the key range is the pool capacity):
-//   0. stage pc and calpha in shared memory when they fit (one coalesced
-//      read; every later step works on shared memory);
+//   0. stage pc and calpha in shared memory when they fit (two bulk copies;
+//      every later step works on shared memory);
 //   1. per-warp histograms of the ids over contiguous chunks of the pairs
 //      (shared memory atomics into the warp's own row; layout [warp][bin]);
 //   2. block scans over the bins give every warp's first output slot per
@@ -213,6 +213,7 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_sort(const SortArgs a)
     extern __shared__ __align__(16) int32_t sh[];
     __shared__ int s_scan[4 * 32 + 4];
     __shared__ int s_build, s_skip;
+    __shared__ __align__(8) uint64_t s_bar;  // the staging copies
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = a.P, cap = a.cap, nw = a.nw;
     const int nthr = blockDim.x;  // 1024, or 256 for short batches
@@ -220,11 +221,14 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_sort(const SortArgs a)
     pdl_launch_dependents();  // the dependents wait for this grid
     // pc as words: [2p] token, [2p + 1] adapter (-1: left out); alpha bits
     const int32_t *pcw = reinterpret_cast<const int32_t *>(m.pc), *alb = reinterpret_cast<const int32_t *>(m.calpha);
-    int32_t *hist = a.hist_g ? a.hist_g : sh + (a.staged ? 3 * P : 0);
+    // staged: pc words [0, 2 P2), alpha bits [2 P2, 2 P2 + P) (P2 = P rounded up
+    // to even: the alpha run starts 16-byte aligned for the bulk copy)
+    const int P2 = (P + 1) & ~1, staged_words = 2 * P2 + P;
+    int32_t *hist = a.hist_g ? a.hist_g : sh + (a.staged ? staged_words : 0);
     // per bin: first sorted position and first shrink tile of its segment
     int32_t *bin_first = hist + nw * cap, *bin_tile = bin_first + cap;
     // sorted token and source pair per position (with sorted_smem)
-    int32_t *s_stok = (a.hist_g ? sh + (a.staged ? 3 * P : 0) : bin_tile + cap), *s_ssrc = s_stok + P;
+    int32_t *s_stok = (a.hist_g ? sh + (a.staged ? staged_words : 0) : bin_tile + cap), *s_ssrc = s_stok + P;
     if (!a.hist_g)
         for (int i = tid; i < nw * cap; i += nthr)
             hist[i] = 0;
@@ -237,9 +241,27 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_sort(const SortArgs a)
     if (s_skip)
         return;  // this build is sorted already
     if (a.staged) {
-        stage_words(sh, pcw, 2 * P, alb, P, alb, 0);
+        // two bulk copies (the 16-byte multiples of pc and alpha) by one
+        // thread, the few words beyond them by others, in one round trip
+        const uint32_t pc_bytes = 8u * (uint32_t)(P & ~1), al_bytes = 4u * (uint32_t)(P & ~3);
+        if (tid == 0) {
+            mbar_init(&s_bar, 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&s_bar, pc_bytes + al_bytes);
+            if (pc_bytes)
+                bulk_g2s(sh, pcw, pc_bytes, &s_bar);
+            if (al_bytes)
+                bulk_g2s(sh + 2 * P2, alb, al_bytes, &s_bar);
+        }
+        if (tid < 2 && (P & 1))
+            sh[2 * (P - 1) + tid] = pcw[2 * (P - 1) + tid];
+        if (tid >= 2 && tid < 2 + (P & 3))
+            sh[2 * P2 + (P & ~3) + tid - 2] = alb[(P & ~3) + tid - 2];
+        __syncthreads();  // the barrier is initialised before anyone waits on it
+        if (!mbar_wait_bounded(&s_bar, 0, m.hdr + HDR_STATUS))
+            return;  // status flagged (a copy that never lands)
         pcw = sh;
-        alb = sh + 2 * P;
+        alb = sh + 2 * P2;
     }
     if (a.hist_g)
         for (int i = tid; i < nw * cap; i += nthr)
@@ -438,7 +460,7 @@ cudaError_t launch_map_csr(const MapDev &m, const int32_t *offsets, const int32_
 cudaError_t launch_map_sort(const MapDev &m, int T, int P, int capacity, cudaStream_t st)
 {
     const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
-    const long long staged_words = 3LL * P;       // pc (two words per pair) and alpha
+    const long long staged_words = 2LL * ((P + 1) & ~1) + P;  // pc (two words per pair, even count) and alpha
     // short batches over small pools: one CTA of 256 threads (cheaper
     // block-wide phases, the bins still one scan round); otherwise 1024
     const int threads = (P <= 512 && capacity <= 256) ? 256 : MAP_THREADS;
