@@ -651,3 +651,39 @@ def test_no_pairs_leaves_y():
                        alpha_lists=[[], []])
     y, st = run_gpu(wl)
     np.testing.assert_array_equal(y, wl.y)
+
+
+def _large_batch():
+    """12000 tokens with 1-4 pairs each (about 30000 pairs), ranks 1..16 over
+    a pool of 64: more than the mapping stages stage in shared memory, so the
+    CSR stage and the sort run their global-memory forms."""
+    rng = np.random.default_rng(41)
+    T, cap = 12000, 64
+    counts = rng.integers(1, 5, size=T)
+    lists = [[int(v) for v in rng.choice(cap, size=int(c), replace=False)] for c in counts]
+    alphas = [list(rng.random(len(l)).astype(np.float32)) for l in lists]
+    ranks = rng.integers(1, 17, size=cap).astype(np.int32)
+    return W.make_custom(rng, d_in=256, d_out=256, r_max=16, capacity=cap, id_lists=lists, alpha_lists=alphas,
+                         ranks=ranks, y_sigma=0.0, name="large_batch")
+
+
+def test_large_batch_mapping_bit_exact():
+    wl = _large_batch()
+    assert (wl.offsets.size - 1) + 1 + 2 * wl.ids.size > 51200  # beyond the staged CSR form
+    dw = DeviceWorkload(wl)
+    try:
+        got = dw.mapping.export()
+    finally:
+        dw.close()
+    compare_mapping(got, oracle.build_mapping(wl.offsets, wl.ids, wl.alpha, capacity=wl.capacity))
+
+
+@pytest.mark.parametrize("path", [PATH_AUTO, PATH_MMA, PATH_SPLIT, PATH_DECODE])
+def test_large_batch_every_token(path):
+    """Every token of the large batch against the fp64 oracle (y = 0, so the
+    delta-only bound applies)."""
+    wl = _large_batch()
+    y, st = run_gpu(wl, path=path)
+    assert st == 0
+    _, acc, _ = oracle.apply_workload(wl, threads=0)
+    delta_gate(y, acc)
