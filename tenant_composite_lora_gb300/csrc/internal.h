@@ -53,10 +53,12 @@ constexpr int RANK_TAB_MAX = 2048;
 // was built, and its CTAs that have exited in the current launch.
 // HDR_BUILD: builds of this mapping (advanced by the CSR stage); HDR_SORTED:
 // the build whose tuples the sort stage last produced.  HDR_U, HDR_PVALID,
-// HDR_NTILES and HDR_NMTILES belong to the sort stage.
+// HDR_NTILES and HDR_NMTILES belong to the sort stage.  HDR_CSR_DONE,
+// HDR_CSR_FLAGS: the several-CTA CSR stage's finished CTAs and their status
+// bits, zero between builds (its last CTA writes the status and clears them).
 enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_BAR = 5, HDR_BAR_BASE = 6,
        HDR_EXIT = 7, HDR_NMTILES = 8, HDR_EPOCH = 9, HDR_DEXIT = 10, HDR_BUILD = 11, HDR_SORTED = 12,
-       HDR_WORDS = 13 };
+       HDR_CSR_DONE = 13, HDR_CSR_FLAGS = 14, HDR_WORDS = 15 };
 
 // Tensor-core (tcgen05) prefill path: tiles of MMA_TM rows (pairs of one
 // segment for the shrink, consecutive tokens for the expand).

@@ -6,9 +6,10 @@
 // processes the tokens of one adapter back to back and each adapter's A and
 // B are read once.
 //
-// Two kernels, each a single CTA:
+// Two stages:
 //
-// k_map_csr (every build) copies the batch into the mapping in CSR order:
+// k_map_csr (every build; one CTA, or from 1024 tokens k_map_csr_wide, a CTA
+// per 256 tokens) copies the batch into the mapping in CSR order:
 //   the offsets (toff), and per pair {token, adapter} (pc; adapter -1 when
 //   the pair is left out) and alpha (calpha).  It checks the offsets (all
 //   pairs are left out when they are malformed), flags ids outside
@@ -16,7 +17,7 @@
 //   and advances the build epoch.  The decode kernels read nothing else:
 //   they index pairs in CSR order.
 //
-// k_map_sort (launched by the paths that read the sorted tuples, before
+// k_map_sort (one CTA, launched by the paths that read the sorted tuples, before
 // their own kernels; it returns at once when the current build is already
 // sorted) performs a stable counting sort on the adapter id over the CSR
 // copy (the key range is the pool capacity):
@@ -199,6 +200,112 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_csr(const CsrArgs a)
     }
     if (bad_id)
         atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_ID);
+}
+
+// The CSR stage of a long batch over several CTAs, a thread per token.
+// Before the dependency wait each thread reads its token's offsets and the
+// ids and alpha of its first CSR_WIDE_PR pairs (inputs no kernel of the
+// library writes); after it, it writes its token's records.  A CTA that
+// finds its tokens' offsets malformed writes no records and flags it; so do
+// ids outside the pool.  The CTA that finishes last (a counter in the
+// header) writes the status word from the flags of all CTAs, clears both
+// words, and -- when some offsets were malformed -- leaves every pair out,
+// over the records the other CTAs wrote.
+constexpr int CSR_WIDE_TOKENS = 256;  // tokens per CTA, one per thread
+constexpr int CSR_WIDE_PR = 8;        // pairs per token read before the wait
+
+__global__ void __launch_bounds__(CSR_WIDE_TOKENS) k_map_csr_wide(const CsrArgs a)
+{
+    __shared__ int s_last, s_flags;
+    const int tid = threadIdx.x;
+    const int T = a.T, P = a.P, cap = a.cap, G = gridDim.x, b = blockIdx.x;
+    const int32_t *alb = reinterpret_cast<const int32_t *>(a.alpha);
+    const MapDev &m = a.m;
+    pdl_launch_dependents();  // the dependents wait for this grid
+    const int t = b * CSR_WIDE_TOKENS + tid;
+    int e0 = 0, e1 = 0;
+    if (t < T) {
+        e0 = __ldg(a.off + t);
+        e1 = __ldg(a.off + t + 1);
+    }
+    // this CTA's share of the check: its tokens' ranges non-decreasing and
+    // inside [0, P]; off[0] = 0 and off[T] = P at the ends
+    int bad = e1 < e0 || e0 < 0 || e1 > P;
+    if (t == 0)
+        bad |= e0 != 0;
+    if (t == T - 1)
+        bad |= e1 != P;
+    bad = __syncthreads_or(bad);
+    int idv[CSR_WIDE_PR], alv[CSR_WIDE_PR];
+#pragma unroll
+    for (int i = 0; i < CSR_WIDE_PR; ++i) {
+        const bool in = !bad && e0 + i < e1;
+        idv[i] = in ? __ldg(a.ids + e0 + i) : 0;
+        alv[i] = in ? __ldg(alb + e0 + i) : 0;
+    }
+    pdl_wait();  // the previous kernel (which may still read this mapping) is done
+    if (b == 0 && tid == 0) {
+        m.hdr[HDR_BAR] = 0;  // fused-kernel counters start over with every mapping
+        m.hdr[HDR_BAR_BASE] = 0;
+        m.hdr[HDR_EXIT] = 0;
+        m.hdr[HDR_EPOCH] = 0;
+        m.hdr[HDR_DEXIT] = 0;
+        m.hdr[HDR_T] = T;
+        atomicAdd(&m.hdr[HDR_BUILD], 1);  // the sorted tuples are stale from here on
+    }
+    const int q0 = (int)((long long)b * P / G), q1 = (int)((long long)(b + 1) * P / G);
+    for (int p = q0 + tid; p < q1; p += CSR_WIDE_TOKENS)
+        m.zcnt[p] = 0;
+    int bad_id = 0;
+    if (!bad && t < T) {
+        m.toff[t] = e0;
+        if (t == T - 1)
+            m.toff[T] = P;
+#pragma unroll
+        for (int i = 0; i < CSR_WIDE_PR; ++i)
+            if (e0 + i < e1) {
+                const bool ok = idv[i] >= 0 && idv[i] < cap;
+                bad_id |= !ok;
+                m.pc[e0 + i] = make_int2(t, ok ? idv[i] : -1);
+                m.calpha[e0 + i] = __int_as_float(alv[i]);
+            }
+        for (int e = e0 + CSR_WIDE_PR; e < e1; ++e) {
+            const int id = __ldg(a.ids + e);
+            const bool ok = id >= 0 && id < cap;
+            bad_id |= !ok;
+            m.pc[e] = make_int2(t, ok ? id : -1);
+            m.calpha[e] = __int_as_float(__ldg(alb + e));
+        }
+    }
+    __threadfence();  // every thread's records before this CTA's count
+    bad_id = __syncthreads_or(bad_id);
+    if (tid == 0) {
+        const int mine = (bad ? LORA_DEV_BAD_OFFSETS : 0) | (bad_id ? LORA_DEV_BAD_ID : 0);
+        if (mine)
+            atomicOr(&m.hdr[HDR_CSR_FLAGS], mine);
+        __threadfence();  // the flags before the count
+        const int last = atomicAdd(&m.hdr[HDR_CSR_DONE], 1) == G - 1;
+        int flags = 0;
+        if (last) {
+            __threadfence();
+            flags = atomicExch(&m.hdr[HDR_CSR_FLAGS], 0);
+            m.hdr[HDR_CSR_DONE] = 0;
+            // malformed offsets anywhere: the batch's status is that alone
+            m.hdr[HDR_STATUS] = (flags & LORA_DEV_BAD_OFFSETS) ? LORA_DEV_BAD_OFFSETS : flags;
+        }
+        s_last = last;
+        s_flags = flags;
+    }
+    __syncthreads();
+    if (s_last && (s_flags & LORA_DEV_BAD_OFFSETS)) {
+        // every pair left out: empty pair ranges, no adapter
+        for (int u = tid; u <= T; u += CSR_WIDE_TOKENS)
+            m.toff[u] = 0;
+        for (int p = tid; p < P; p += CSR_WIDE_TOKENS) {
+            m.pc[p] = make_int2(-1, -1);
+            m.calpha[p] = 0.f;
+        }
+    }
 }
 
 struct SortArgs {
@@ -399,10 +506,11 @@ cudaError_t map_attrs(K kernel, int &done)
 }
 
 template <class Args>
-cudaError_t map_launch(void (*kernel)(Args), const Args &a, int threads, size_t smem, cudaStream_t st)
+cudaError_t map_launch(void (*kernel)(Args), const Args &a, int threads, size_t smem, cudaStream_t st,
+                       unsigned grid = 1)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(1, 1, 1);
+    cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -445,6 +553,16 @@ cudaError_t launch_map_csr(const MapDev &m, const int32_t *offsets, const int32_
                            int P, int capacity, cudaStream_t st)
 {
     const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
+    if (T >= 4 * CSR_WIDE_TOKENS) {
+        // long batches: a CTA per CSR_WIDE_TOKENS tokens, no shared memory
+        static thread_local int wide_done = -1;  // per host thread
+        const cudaError_t e = map_attrs(k_map_csr_wide, wide_done);
+        if (e != cudaSuccess)
+            return e;
+        const CsrArgs a{m, offsets, ids, alpha, T, P, capacity, 0};
+        return map_launch(k_map_csr_wide, a, CSR_WIDE_TOKENS, 0, st,
+                          (unsigned)((T + CSR_WIDE_TOKENS - 1) / CSR_WIDE_TOKENS));
+    }
     const long long words = (long long)(T + 1) + 2LL * P;
     const int staged = words <= budget ? 1 : 0;
     // a short batch is one staging round of 256 threads (cheaper block-wide steps)

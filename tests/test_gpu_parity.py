@@ -128,6 +128,33 @@ def test_mapping_bad_offsets_and_degenerate():
                     oracle.build_mapping(offsets, ids, np.ones(cap, np.float32), capacity=cap))
 
 
+@pytest.mark.parametrize("form", ["step_down", "first", "last", "beyond_p", "valid"])
+def test_mapping_long_batch_offsets(form):
+    """3000 tokens: the CSR stage runs over several CTAs, each checking its own
+    tokens' offsets; malformed offsets anywhere (inside one CTA's range, at
+    either end, beyond P) leave every pair out, as the oracle does, and some
+    ids outside the pool are among them."""
+    rng = np.random.default_rng(23)
+    n_tok, cap = 3000, 50
+    counts = rng.integers(0, 4, size=n_tok)
+    offsets = np.zeros(n_tok + 1, np.int32)
+    offsets[1:] = np.cumsum(counts)
+    P = int(offsets[-1])
+    ids = rng.integers(-2, cap + 2, size=P).astype(np.int32)
+    alpha = rng.standard_normal(P).astype(np.float32)
+    if form == "step_down":
+        offsets[1700] = offsets[1701] + 1
+    elif form == "first":
+        offsets[0] = 1
+    elif form == "last":
+        offsets[-1] = P - 1
+    elif form == "beyond_p":
+        offsets[900] = P + 5
+    got = _map_raw(offsets, ids, alpha, cap)
+    compare_mapping(got, oracle.build_mapping(offsets, ids, alpha, capacity=cap))
+    assert bool(got["status"] & 2) == (form != "valid")
+
+
 @pytest.mark.parametrize("cap", [20000, 49152])
 def test_mapping_large_pools(cap):
     """Pools too large for the shared-memory histograms (up to the library's
