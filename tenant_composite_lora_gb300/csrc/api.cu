@@ -307,7 +307,7 @@ void free_mapping(lora_mapping *m)
     MapDev &d = m->dev;
     void *ptrs[] = {d.tok,  d.adapter, d.src, d.pos,     d.alpha, d.seg_adapter, d.seg_start,
                     d.tile, d.tile_tok, d.hdr, d.mtile, d.toff,     d.pc, d.calpha, d.zcnt, d.z,
-                    d.partial, d.ghist, m->sx, m->sy, m->soff, m->sids, m->salpha};
+                    d.partial, d.ghist, d.gsort, m->sx, m->sy, m->soff, m->sids, m->salpha};
     for (void *p : ptrs)
         if (p)
             cudaFree(p);
@@ -608,6 +608,8 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
     if (e == cudaSuccess) e = dalloc(&d.partial, (size_t)d.partial_ctas * EXP_TILE_ELEMS);
     if (e == cudaSuccess && map_global_hist_words(capacity) > 0)
         e = dalloc(&d.ghist, (size_t)map_global_hist_words(capacity));
+    if (e == cudaSuccess && map_wide_sort_words(capacity) > 0)
+        e = dalloc(&d.gsort, (size_t)map_wide_sort_words(capacity));
     if (e == cudaSuccess) e = cudaMemset(d.hdr, 0, HDR_WORDS * sizeof(int32_t));
     if (e == cudaSuccess) e = cudaMemset(d.seg_start, 0, sizeof(int32_t));
     if (e == cudaSuccess) e = cudaDeviceSynchronize();

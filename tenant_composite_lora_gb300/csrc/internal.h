@@ -41,6 +41,8 @@ constexpr int MAP_SMEM_BYTES = 200 * 1024;
 constexpr int MAP_GHIST_WARPS = 8;
 // Words of global histogram scratch a mapping over `capacity` ids needs (0: none).
 int map_global_hist_words(int capacity);
+// Scratch words of the several-CTA sort of long batches (0: pools too large for it).
+int map_wide_sort_words(int capacity);
 
 // Ranks of pools up to this capacity are staged in shared memory by the
 // apply kernels (one coalesced read instead of a dependent lookup).
@@ -56,9 +58,14 @@ constexpr int RANK_TAB_MAX = 2048;
 // HDR_NTILES and HDR_NMTILES belong to the sort stage.  HDR_CSR_DONE,
 // HDR_CSR_FLAGS: the several-CTA CSR stage's finished CTAs and their status
 // bits, zero between builds (its last CTA writes the status and clears them).
+// HDR_SORT_DONE: the several-CTA sort's counting CTAs that have finished,
+// zero between sorts (its last CTA clears it); HDR_SORT_GO: 1 when its
+// counting kernel prepared this launch's scatter, 0 when it found the build
+// sorted already (the scatter's own decision, which its first CTA's update
+// of HDR_SORTED cannot change under its other CTAs).
 enum { HDR_U = 0, HDR_PVALID = 1, HDR_STATUS = 2, HDR_NTILES = 3, HDR_T = 4, HDR_BAR = 5, HDR_BAR_BASE = 6,
        HDR_EXIT = 7, HDR_NMTILES = 8, HDR_EPOCH = 9, HDR_DEXIT = 10, HDR_BUILD = 11, HDR_SORTED = 12,
-       HDR_CSR_DONE = 13, HDR_CSR_FLAGS = 14, HDR_WORDS = 15 };
+       HDR_CSR_DONE = 13, HDR_CSR_FLAGS = 14, HDR_SORT_DONE = 15, HDR_SORT_GO = 16, HDR_WORDS = 17 };
 
 // Tensor-core (tcgen05) prefill path: tiles of MMA_TM rows (pairs of one
 // segment for the shrink, consecutive tokens for the expand).
@@ -104,6 +111,8 @@ struct MapDev {
     int partial_ctas;
     int32_t *ghist;                      // [map_global_hist_words(capacity)] or null: mapping
                                          // histograms of pools too large for shared memory
+    int32_t *gsort;                      // [map_wide_sort_words(capacity)] or null: the
+                                         // several-CTA sort's per-CTA bin counts and per-bin arrays
 };
 
 // Launchers (each returns cudaGetLastError()).

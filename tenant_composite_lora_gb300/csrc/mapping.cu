@@ -17,7 +17,8 @@
 //   and advances the build epoch.  The decode kernels read nothing else:
 //   they index pairs in CSR order.
 //
-// k_map_sort (one CTA, launched by the paths that read the sorted tuples, before
+// k_map_sort (one CTA; k_sort_count + k_sort_scatter for long batches over
+// small pools, below; launched by the paths that read the sorted tuples, before
 // their own kernels; it returns at once when the current build is already
 // sorted) performs a stable counting sort on the adapter id over the CSR
 // copy (the key range is the pool capacity):
@@ -489,6 +490,153 @@ __global__ void __launch_bounds__(MAP_THREADS, 1) k_map_sort(const SortArgs a)
         m.hdr[HDR_SORTED] = s_build;
 }
 
+// The sort of a long batch over several CTAs, in two kernels (the second a
+// programmatic dependent of the first); the same tuples, bit for bit, as the
+// one-CTA sort.  k_sort_count: a CTA per SW_CHUNK pairs (a thread each)
+// counts its pairs per adapter and writes the counts; the CTA that finishes
+// last (a counter in the header) scans the bins -- segments, shrink tiles,
+// tensor-core tiles, the header's counts -- and turns the per-CTA counts into
+// every CTA's first sorted position per adapter.  k_sort_scatter: each CTA
+// places its pairs -- rank among equal adapters = earlier warps' counts +
+// earlier lanes of its own warp (match) + the CTA's first position -- so
+// ties keep CSR order.  Both return at once when the build is sorted.
+constexpr int SW_CHUNK = 512;     // pairs (threads) per CTA
+constexpr int SW_MAX_CTAS = 64;   // up to SW_CHUNK * SW_MAX_CTAS pairs
+constexpr int SW_MAX_CAP = 1024;  // pools up to this size
+
+struct SortWideArgs {
+    MapDev m;
+    int32_t *cnt;             // [G][cap]: per-CTA counts, then per-CTA first positions
+    int32_t *bfirst, *btile;  // [cap] each: a bin's first position and first shrink tile
+    int P, cap, tile_bound, mtile_bound;
+};
+
+__global__ void __launch_bounds__(SW_CHUNK) k_sort_count(const SortWideArgs a)
+{
+    __shared__ int hist[SW_MAX_CAP];
+    __shared__ int s_scan[4 * 32 + 4];
+    __shared__ int s_skip, s_last;
+    const int tid = threadIdx.x, b = blockIdx.x, G = gridDim.x, cap = a.cap, P = a.P;
+    const MapDev &m = a.m;
+    pdl_launch_dependents();  // the scatter waits for this grid
+    for (int i = tid; i < cap; i += SW_CHUNK)
+        hist[i] = 0;
+    pdl_wait();  // the CSR copy is complete, and no earlier kernel reads the sorted tuples any more
+    if (tid == 0)
+        s_skip = m.hdr[HDR_SORTED] == m.hdr[HDR_BUILD];  // no kernel writes either while this grid runs
+    __syncthreads();
+    if (s_skip) {
+        if (b == 0 && tid == 0)
+            m.hdr[HDR_SORT_GO] = 0;  // the scatter returns at once
+        return;  // this build is sorted already (uniform over the grid)
+    }
+    const int p = b * SW_CHUNK + tid;
+    const int id = p < P ? m.pc[p].y : -1;
+    if (id >= 0)
+        atomicAdd(&hist[id], 1);
+    __syncthreads();
+    for (int i = tid; i < cap; i += SW_CHUNK)
+        a.cnt[b * cap + i] = hist[i];
+    __threadfence();  // the counts before the CTA's arrival
+    __syncthreads();
+    if (tid == 0)
+        s_last = atomicAdd(&m.hdr[HDR_SORT_DONE], 1) == G - 1;
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    // the last CTA: a scan over bins, a CTA's worth of bins per round, bin-ascending
+    Scan4 carry = {0, 0, 0, 0};
+    for (int base = 0; base < cap; base += SW_CHUNK) {
+        const int bin = base + tid;
+        int c = 0;
+        if (bin < cap)
+            for (int g = 0; g < G; ++g)
+                c += __ldcg(a.cnt + g * cap + bin);
+        const Scan4 mine = {c, c > 0 ? 1 : 0, (c + SHRINK_TT - 1) / SHRINK_TT, (c + MMA_TM - 1) / MMA_TM};
+        Scan4 tot;
+        const Scan4 ex = block_exclusive_scan4(mine, tot, s_scan);
+        if (c > 0) {
+            int run = carry.a + ex.a;
+            const int sidx = carry.b + ex.b, tix = carry.c + ex.c;
+            m.seg_adapter[sidx] = bin;
+            m.seg_start[sidx] = run;
+            a.bfirst[bin] = run;
+            a.btile[bin] = tix;
+            for (int i = 0; i < mine.c; ++i)
+                m.tile[tix + i] = make_int4(bin, run + i * SHRINK_TT, min(SHRINK_TT, c - i * SHRINK_TT), sidx);
+            for (int i = 0, mix = carry.d + ex.d; i < mine.d; ++i)
+                m.mtile[mix + i] = make_int4(bin, run + i * MMA_TM, min(MMA_TM, c - i * MMA_TM), sidx);
+            for (int g = 0; g < G; ++g) {
+                const int v = __ldcg(a.cnt + g * cap + bin);
+                a.cnt[g * cap + bin] = run;
+                run += v;
+            }
+        }
+        carry.a += tot.a;
+        carry.b += tot.b;
+        carry.c += tot.c;
+        carry.d += tot.d;
+    }
+    for (int i = carry.c + tid; i < a.tile_bound; i += SW_CHUNK)
+        m.tile[i] = make_int4(0, 0, 0, -1);  // empty slots up to the host-known bound
+    for (int i = carry.d + tid; i < a.mtile_bound; i += SW_CHUNK)
+        m.mtile[i] = make_int4(0, 0, 0, -1);
+    if (tid == 0) {
+        m.hdr[HDR_U] = carry.b;
+        m.hdr[HDR_PVALID] = carry.a;
+        m.hdr[HDR_NTILES] = carry.c;
+        m.hdr[HDR_NMTILES] = carry.d;
+        m.seg_start[carry.b] = carry.a;
+        m.hdr[HDR_SORT_DONE] = 0;
+        m.hdr[HDR_SORT_GO] = 1;
+    }
+}
+
+__global__ void __launch_bounds__(SW_CHUNK) k_sort_scatter(const SortWideArgs a)
+{
+    extern __shared__ __align__(16) int32_t wh[];  // [SW_CHUNK / 32][cap]: each warp's count per adapter
+    __shared__ int s_build, s_skip;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, b = blockIdx.x, cap = a.cap, P = a.P;
+    const MapDev &m = a.m;
+    pdl_launch_dependents();  // the dependents wait for this grid
+    for (int i = tid; i < (SW_CHUNK / 32) * cap; i += SW_CHUNK)
+        wh[i] = 0;
+    pdl_wait();  // the counting grid, its last CTA included, is complete
+    if (tid == 0) {
+        s_build = m.hdr[HDR_BUILD];
+        s_skip = m.hdr[HDR_SORT_GO] == 0;  // set by the counting grid, which is complete
+    }
+    __syncthreads();
+    if (s_skip)
+        return;
+    const int p = b * SW_CHUNK + tid;
+    const bool valid = p < P;
+    const int2 pc = valid ? m.pc[p] : make_int2(0, -1);
+    const int id = pc.y;
+    const bool ok = id >= 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? id : -1 - lane);
+    if (ok && lane == __ffs(peers) - 1)
+        wh[warp * cap + id] = __popc(peers);
+    __syncthreads();
+    if (ok) {
+        int dst = __ldcg(a.cnt + b * cap + id) + __popc(peers & ((1u << lane) - 1u));
+        for (int w = 0; w < warp; ++w)
+            dst += wh[w * cap + id];
+        m.tok[dst] = pc.x;
+        m.adapter[dst] = id;
+        reinterpret_cast<int32_t *>(m.alpha)[dst] = reinterpret_cast<const int32_t *>(m.calpha)[p];
+        m.src[dst] = p;
+        m.pos[p] = dst;
+        const int r = dst - __ldcg(a.bfirst + id);
+        m.tile_tok[(__ldcg(a.btile + id) + r / SHRINK_TT) * SHRINK_TT + r % SHRINK_TT] = pc.x;
+    } else if (valid) {
+        m.pos[p] = -1;
+    }
+    if (b == 0 && tid == 0)
+        m.hdr[HDR_SORTED] = s_build;  // read by later launches only: this grid decided by HDR_SORT_GO
+}
+
 template <class K>
 cudaError_t map_attrs(K kernel, int &done)
 {
@@ -540,6 +688,11 @@ int mma_tile_bound(int P, int capacity)
     return (int)(b < P ? b : P);
 }
 
+int map_wide_sort_words(int capacity)
+{
+    return capacity <= SW_MAX_CAP ? (SW_MAX_CTAS + 2) * capacity : 0;
+}
+
 int map_global_hist_words(int capacity)
 {
     // shared memory holds one warp's histogram and the two per-bin arrays
@@ -577,6 +730,23 @@ cudaError_t launch_map_csr(const MapDev &m, const int32_t *offsets, const int32_
 
 cudaError_t launch_map_sort(const MapDev &m, int T, int P, int capacity, cudaStream_t st)
 {
+    if (m.gsort && P >= 4 * SW_CHUNK && (long long)P <= (long long)SW_CHUNK * SW_MAX_CTAS &&
+        capacity <= SW_MAX_CAP) {
+        // long batches over small pools: the several-CTA sort
+        static thread_local int count_done = -1, scatter_done = -1;  // per host thread
+        cudaError_t e = map_attrs(k_sort_count, count_done);
+        if (e == cudaSuccess)
+            e = map_attrs(k_sort_scatter, scatter_done);
+        if (e != cudaSuccess)
+            return e;
+        const unsigned G = (unsigned)((P + SW_CHUNK - 1) / SW_CHUNK);
+        const SortWideArgs a{m, m.gsort, m.gsort + SW_MAX_CTAS * capacity, m.gsort + (SW_MAX_CTAS + 1) * capacity,
+                             P, capacity, shrink_tile_bound(P, capacity), mma_tile_bound(P, capacity)};
+        e = map_launch(k_sort_count, a, SW_CHUNK, 0, st, G);
+        if (e == cudaSuccess)
+            e = map_launch(k_sort_scatter, a, SW_CHUNK, (size_t)(SW_CHUNK / 32) * capacity * 4, st, G);
+        return e;
+    }
     const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
     const long long staged_words = 2LL * ((P + 1) & ~1) + P;  // pc (two words per pair, even count) and alpha
     // short batches over small pools: one CTA of 256 threads (cheaper
