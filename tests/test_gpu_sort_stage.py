@@ -32,6 +32,20 @@ def built():
     build.build()
 
 
+def make_case(name):
+    """A workload by name; "long" is a batch of 2500 tokens with two pairs
+    each over a pool of 32 (5000 pairs): the sort of long batches, in two
+    kernels, instead of the one-CTA sort."""
+    if name != "long":
+        return W.make(name, y_zero=True)
+    rng = np.random.default_rng(77)
+    T, cap = 2500, 32
+    lists = [[int(v) for v in rng.choice(cap, size=2, replace=False)] for _ in range(T)]
+    alphas = [list(rng.random(2).astype(np.float32)) for _ in range(T)]
+    return W.make_custom(rng, d_in=256, d_out=256, r_max=16, capacity=cap, id_lists=lists, alpha_lists=alphas,
+                         y_sigma=0.0, name="long_batch")
+
+
 def delta_gate(y_bits, acc):
     y = bf16_bits_to_f32(y_bits).astype(np.float64)
     rms = float(np.sqrt(np.mean(acc ** 2)))
@@ -62,13 +76,13 @@ def device_lists(b):
 
 
 @pytest.mark.parametrize("path", [PATH_SPLIT, PATH_MMA, PATH_FUSED])
-@pytest.mark.parametrize("name", ["zipf", "sweep8"])
+@pytest.mark.parametrize("name", ["zipf", "sweep8", "long"])
 def test_decode_apply_then_sorted_path_each_build(name, path):
     """build, decode apply (CSR only), then an apply on a sorted path, batch
     after batch on one stream without a break: the sorted path must sort the
     current build, not reuse the previous one."""
     import tenant_composite_lora_gb300 as tcl
-    wl = W.make(name, y_zero=True)
+    wl = make_case(name)
     batches = [wl] + [other_batch(wl, 200 + i) for i in range(3)]
     dw = DeviceWorkload(wl, build=False)
     s = torch.cuda.Stream()
@@ -111,13 +125,14 @@ def test_export_after_decode_only_use():
         dw.close()
 
 
+@pytest.mark.parametrize("name", ["zipf", "long"])
 @pytest.mark.parametrize("path", [PATH_SPLIT, PATH_MMA])
-def test_graph_of_apply_sorts_each_new_build(path):
+def test_graph_of_apply_sorts_each_new_build(path, name):
     """A CUDA graph holding only the apply (sort stage included), replayed
     after eager builds of different batches: every replay applies the batch
     built last."""
     from tenant_composite_lora_gb300 import native
-    wl = W.make("zipf", y_zero=True)
+    wl = make_case(name)
     batches = [wl, other_batch(wl, 31), other_batch(wl, 32)]
     dw = DeviceWorkload(wl)
     s = torch.cuda.Stream()
@@ -148,12 +163,13 @@ def test_graph_of_apply_sorts_each_new_build(path):
         delta_gate(yb, acc)
 
 
+@pytest.mark.parametrize("name", ["sweep64", "long"])
 @pytest.mark.parametrize("path", [PATH_SPLIT, PATH_MMA])
-def test_second_apply_skips_the_sort_and_agrees(path):
+def test_second_apply_skips_the_sort_and_agrees(path, name):
     """Two applies of one build from the same y: the second finds the tuples
     sorted (its sort stage returns at once) and gives the same bits."""
     import tenant_composite_lora_gb300 as tcl
-    wl = W.make("sweep64", y_zero=True)
+    wl = make_case(name)
     dw = DeviceWorkload(wl)
     try:
         y1, y2 = dw.y0.clone(), dw.y0.clone()
