@@ -513,6 +513,7 @@ struct SortWideArgs {
 
 __global__ void __launch_bounds__(SW_CHUNK) k_sort_count(const SortWideArgs a)
 {
+    extern __shared__ __align__(16) int32_t sc[];  // [G][cap]: the last CTA's copy of every CTA's counts
     __shared__ int hist[SW_MAX_CAP];
     __shared__ int s_scan[4 * 32 + 4];
     __shared__ int s_skip, s_last;
@@ -545,14 +546,18 @@ __global__ void __launch_bounds__(SW_CHUNK) k_sort_count(const SortWideArgs a)
     if (!s_last)
         return;
     __threadfence();
-    // the last CTA: a scan over bins, a CTA's worth of bins per round, bin-ascending
+    // the last CTA: every CTA's counts into shared memory in one round trip,
+    // then a scan over bins, a CTA's worth of bins per round, bin-ascending
+    for (int i = tid; i < G * cap; i += SW_CHUNK)
+        sc[i] = __ldcg(a.cnt + i);
+    __syncthreads();
     Scan4 carry = {0, 0, 0, 0};
     for (int base = 0; base < cap; base += SW_CHUNK) {
         const int bin = base + tid;
         int c = 0;
         if (bin < cap)
             for (int g = 0; g < G; ++g)
-                c += __ldcg(a.cnt + g * cap + bin);
+                c += sc[g * cap + bin];
         const Scan4 mine = {c, c > 0 ? 1 : 0, (c + SHRINK_TT - 1) / SHRINK_TT, (c + MMA_TM - 1) / MMA_TM};
         Scan4 tot;
         const Scan4 ex = block_exclusive_scan4(mine, tot, s_scan);
@@ -568,8 +573,8 @@ __global__ void __launch_bounds__(SW_CHUNK) k_sort_count(const SortWideArgs a)
             for (int i = 0, mix = carry.d + ex.d; i < mine.d; ++i)
                 m.mtile[mix + i] = make_int4(bin, run + i * MMA_TM, min(MMA_TM, c - i * MMA_TM), sidx);
             for (int g = 0; g < G; ++g) {
-                const int v = __ldcg(a.cnt + g * cap + bin);
-                a.cnt[g * cap + bin] = run;
+                const int v = sc[g * cap + bin];
+                sc[g * cap + bin] = run;
                 run += v;
             }
         }
@@ -578,6 +583,9 @@ __global__ void __launch_bounds__(SW_CHUNK) k_sort_count(const SortWideArgs a)
         carry.c += tot.c;
         carry.d += tot.d;
     }
+    __syncthreads();
+    for (int i = tid; i < G * cap; i += SW_CHUNK)
+        a.cnt[i] = sc[i];  // every CTA's first position per adapter
     for (int i = carry.c + tid; i < a.tile_bound; i += SW_CHUNK)
         m.tile[i] = make_int4(0, 0, 0, -1);  // empty slots up to the host-known bound
     for (int i = carry.d + tid; i < a.mtile_bound; i += SW_CHUNK)
@@ -730,8 +738,9 @@ cudaError_t launch_map_csr(const MapDev &m, const int32_t *offsets, const int32_
 
 cudaError_t launch_map_sort(const MapDev &m, int T, int P, int capacity, cudaStream_t st)
 {
-    if (m.gsort && P >= 4 * SW_CHUNK && (long long)P <= (long long)SW_CHUNK * SW_MAX_CTAS &&
-        capacity <= SW_MAX_CAP) {
+    const long long sw_ctas = (P + SW_CHUNK - 1) / SW_CHUNK;
+    if (m.gsort && P >= 4 * SW_CHUNK && sw_ctas <= SW_MAX_CTAS && capacity <= SW_MAX_CAP &&
+        sw_ctas * capacity * 4 <= MAP_SMEM_BYTES) {
         // long batches over small pools: the several-CTA sort
         static thread_local int count_done = -1, scatter_done = -1;  // per host thread
         cudaError_t e = map_attrs(k_sort_count, count_done);
@@ -742,7 +751,7 @@ cudaError_t launch_map_sort(const MapDev &m, int T, int P, int capacity, cudaStr
         const unsigned G = (unsigned)((P + SW_CHUNK - 1) / SW_CHUNK);
         const SortWideArgs a{m, m.gsort, m.gsort + SW_MAX_CTAS * capacity, m.gsort + (SW_MAX_CTAS + 1) * capacity,
                              P, capacity, shrink_tile_bound(P, capacity), mma_tile_bound(P, capacity)};
-        e = map_launch(k_sort_count, a, SW_CHUNK, 0, st, G);
+        e = map_launch(k_sort_count, a, SW_CHUNK, (size_t)G * capacity * 4, st, G);
         if (e == cudaSuccess)
             e = map_launch(k_sort_scatter, a, SW_CHUNK, (size_t)(SW_CHUNK / 32) * capacity * 4, st, G);
         return e;
