@@ -50,11 +50,20 @@ PATH_NAMES = {0: "auto", 1: "split", 2: "fused", 3: "mma", 4: "decode"}
 # launch per step; the paths that read the adapter-sorted tuples launch the
 # sort stage first, which returns at once when the build is sorted already)
 PATH_KERNELS = {
-    "split": (3, "k_map_sort + k_shrink + k_expand (PDL)"),
+    "split": (2, "sort stage + k_shrink + k_expand (PDL)"),
     "fused": (1, "k_dec_fused (cooperative, one launch)"),
-    "mma": (3, "k_map_sort + k_mma_shrink + k_mma_expand (tcgen05, PDL)"),
+    "mma": (2, "sort stage + k_mma_shrink + k_mma_expand (tcgen05, PDL)"),
     "decode": (2, "k_dec_shrink + k_dec_expand (PDL)"),
 }
+SORTED_PATHS = ("split", "mma")
+
+
+def sort_stage_kernels(P: int, capacity: int) -> int:
+    """Kernels of the mapping's sort stage: two (count, scatter) for batches
+    of 2048..32768 pairs over pools of at most 1024 slots whose per-CTA
+    counts fit in shared memory, else one (the one-CTA sort)."""
+    ctas = (P + 511) // 512
+    return 2 if P >= 2048 and ctas <= 64 and capacity <= 1024 and ctas * capacity * 4 <= 200 * 1024 else 1
 
 
 def peaks():
@@ -429,6 +438,8 @@ def bench_ours(args, rank, world, dist):
     path_taken = args.path if args.path_id != 0 else PATH_NAMES[
         native.lora_dispatch_choose(wl.T, wl.P, wl.r_max, wl.d_in, wl.d_out)]
     n_apply_kernels, kernel_desc = PATH_KERNELS[path_taken]
+    if path_taken in SORTED_PATHS:
+        n_apply_kernels += sort_stage_kernels(wl.P, wl.capacity)
     achieved = ab["total"] / (ms_apply * 1e-3) / 1e9
     value = world * wl.T / (ms_per_step * 1e-3)
     line = {
@@ -464,7 +475,7 @@ def bench_ours(args, rank, world, dist):
         "e2e": {"value": round(world * wl.T / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 6),
                 "api": "lora_delta_apply_host", "host_us_per_call": round(host_us, 3)},
-        "gpu_launches": (1 + n_apply_kernels) * steps_done,
+        "gpu_launches": (1 + n_apply_kernels) * steps_done,  # the CSR stage is one launch
         "clocks": clocks,
         "step_us_spread": spread_step,
     }
