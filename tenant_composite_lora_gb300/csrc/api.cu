@@ -55,6 +55,12 @@ struct lora_mapping {
     int max_tokens, max_pairs, capacity, device;
     int T, P;
     bool built;
+    // host-side record of the sort stage: builds so far, and the build and
+    // stream (by its unique id: a handle may be reused after destruction) of
+    // the last sort enqueued eagerly (not into a graph)
+    long long builds, sorted_builds;
+    unsigned long long sorted_stream;
+    bool sorted_valid;
     tcl::MapDev dev;
     // staging of lora_delta_apply_host
     void *sx, *sy;
@@ -385,9 +391,34 @@ ExpandPlan choose_expand_plan(int T, int d_out)
 
 // The adapter-sorted tuples of the mapping's current build (the sort stage
 // returns at once when they are there already).
-cudaError_t sort_mapping(const lora_mapping *m, cudaStream_t st)
+// The sort stage before a path that reads the adapter-sorted tuples.  Its
+// kernel checks on the device whether the current build is sorted (so
+// graphs and other streams stay correct); on the host, a sort enqueued
+// eagerly on this same stream since the last build is already ahead of this
+// call in stream order, and the launch is left out.
+cudaError_t sort_mapping(const lora_mapping *cm, cudaStream_t st)
 {
-    return launch_map_sort(m->dev, m->T, m->P, m->capacity, st);
+    lora_mapping *m = const_cast<lora_mapping *>(cm);  // host-side bookkeeping only
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        cs = cudaStreamCaptureStatusActive;  // unknown: launch, record nothing
+    }
+    unsigned long long sid = 0;
+    bool eager = cs == cudaStreamCaptureStatusNone;
+    if (eager && cudaStreamGetId(st, &sid) != cudaSuccess) {
+        cudaGetLastError();
+        eager = false;  // no id: launch, record nothing
+    }
+    if (eager && m->sorted_valid && m->sorted_stream == sid && m->sorted_builds == m->builds)
+        return cudaSuccess;
+    const cudaError_t e = launch_map_sort(m->dev, m->T, m->P, m->capacity, st);
+    if (e == cudaSuccess && eager) {
+        m->sorted_valid = true;
+        m->sorted_stream = sid;
+        m->sorted_builds = m->builds;
+    }
+    return e;
 }
 
 lora_status run_fused(const void *x, void *y, const lora_pool *pool, const int32_t *ranks, const lora_mapping *m,
@@ -637,6 +668,7 @@ lora_status lora_build_mapping(lora_mapping *m, const int32_t *offsets_dev, cons
     m->T = T;
     m->P = P;
     m->built = true;
+    ++m->builds;  // a later sorted path sorts this build
     return LORA_OK;
 }
 
@@ -941,6 +973,7 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
             m->T = T;  // the host-side state lora_build_mapping would leave
             m->P = P;
             m->built = true;
+            ++m->builds;
             return from_cuda(cudaGraphLaunch(m->exec, st));
         }
         cudaGraphExecDestroy(m->exec);

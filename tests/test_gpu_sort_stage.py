@@ -183,3 +183,40 @@ def test_second_apply_skips_the_sort_and_agrees(path, name):
     np.testing.assert_array_equal(a, b)
     _, acc, _ = oracle.apply_workload(wl, threads=0)
     delta_gate(a, acc)
+
+
+@pytest.mark.parametrize("name", ["zipf", "long"])
+def test_sorted_path_across_streams_and_builds(name):
+    """The host leaves out the sort launch only after an eager sort of the
+    same build on the same stream: applies alternating between two streams
+    (ordered by events) over two builds each give the oracle's delta."""
+    import tenant_composite_lora_gb300 as tcl
+    wl = make_case(name)
+    b2 = other_batch(wl, 91)
+    dw = DeviceWorkload(wl)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    try:
+        ys = [dw.y0.clone() for _ in range(4)]
+        torch.cuda.synchronize()
+        ev = torch.cuda.Event()
+        with torch.cuda.stream(sa):
+            tcl.delta_apply(dw.x, ys[0], dw.pool, dw.mapping, path=PATH_MMA, stream=sa)
+            tcl.delta_apply(dw.x, ys[1], dw.pool, dw.mapping, path=PATH_SPLIT, stream=sa)
+            ev.record(sa)
+        sb.wait_event(ev)
+        with torch.cuda.stream(sb):
+            dw.mapping.build(*device_lists(b2), sb)
+            tcl.delta_apply(dw.x, ys[2], dw.pool, dw.mapping, path=PATH_MMA, stream=sb)
+            ev.record(sb)
+        sa.wait_event(ev)
+        with torch.cuda.stream(sa):
+            tcl.delta_apply(dw.x, ys[3], dw.pool, dw.mapping, path=PATH_SPLIT, stream=sa)
+        torch.cuda.synchronize()
+        got = [bf16_to_numpy_bits(y) for y in ys]
+        mapping_matches(dw.mapping.export(), b2)
+    finally:
+        dw.close()
+    _, acc1, _ = oracle.apply_workload(wl, threads=0)
+    _, acc2, _ = oracle.apply_workload(b2, threads=0)
+    for g, acc in zip(got, (acc1, acc1, acc2, acc2)):
+        delta_gate(g, acc)
