@@ -251,8 +251,11 @@ __device__ __forceinline__ void dec_rows(float (&acc)[8], const __nv_bfloat16 *b
 }
 
 // One expand item: token t, 256-column chunk c, on one warp.  wait_pair(q)
-// is called before the first read of pair q's z (the shrink's output).
-template <int PP, int R, class WaitPair>
+// is called before the first read of pair q's z (the shrink's output).  NX:
+// pairs after the PP prefetched ones whose adapter and rank are also read
+// before the wait (then one round trip each after it, for B, instead of
+// three) -- for the one-prefetched-pair instance, whose tokens have more.
+template <int PP, int R, int NX, class WaitPair>
 __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, int c, WaitPair wait_pair)
 {
     const int lane = threadIdx.x & 31;
@@ -265,12 +268,18 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
     const int p0 = a.m.toff[t], p1 = a.m.toff[t + 1];
     if (p1 <= p0)
         return;  // no pair: y stays as it is (every token when the offsets were malformed)
-    // round trip 2: the adapters of the first pairs
-    int pa[PP];
+    // round trip 2: the adapters of the first pairs (and of the NX after them)
+    int pa[PP], px[NX > 0 ? NX : 1], kx[NX > 0 ? NX : 1];
 #pragma unroll
     for (int i = 0; i < PP; ++i)
         pa[i] = p0 + i < p1 ? a.m.pc[p0 + i].y : -1;
+#pragma unroll
+    for (int i = 0; i < NX; ++i)
+        px[i] = p0 + PP + i < p1 ? a.m.pc[p0 + PP + i].y : -1;
     // round trip 3: their first B rows (whatever the rank turns out to be) and ranks
+#pragma unroll
+    for (int i = 0; i < NX; ++i)
+        kx[i] = px[i] >= 0 ? dec_rank(a.pool, a.ranks, px[i]) : 0;
     uint4 bpre[PP][DE_PR];
     int kk[PP];
 #pragma unroll
@@ -301,7 +310,16 @@ __device__ __forceinline__ void dec_expand_item(const DecExpandArgs &a, int t, i
                 dec_rows<R>(acc, a.pool.B + (size_t)pa[i] * r_max * d_out + col, zr, DE_PR, k, d_out, on);
         }
     }
-    for (int p = p0 + PP; p < p1; ++p) {
+#pragma unroll
+    for (int i = 0; i < NX; ++i) {
+        const int p = p0 + PP + i;
+        if (p < p1 && kx[i] > 0) {
+            wait_pair(p);
+            dec_rows<R>(acc, a.pool.B + (size_t)px[i] * r_max * d_out + col, a.z + (size_t)p * a.zs, 0, kx[i], d_out,
+                        on);
+        }
+    }
+    for (int p = p0 + PP + NX; p < p1; ++p) {
         const int ad = a.m.pc[p].y;
         if (ad < 0)
             continue;
@@ -335,7 +353,7 @@ __global__ void __launch_bounds__(256, MINB) k_dec_expand(const DecExpandArgs a)
     // consecutive warps: consecutive tokens on one column chunk, so the B rows
     // of an adapter several of them use come from L1 after the first
     bool waited = false;
-    dec_expand_item<PP, RF>(a, g % a.T, g / a.T, [&](int) {
+    dec_expand_item<PP, RF, PP == 1 ? 3 : 0>(a, g % a.T, g / a.T, [&](int) {
         if (!waited) {
             pdl_wait();  // z of the shrink
             waited = true;
@@ -489,7 +507,7 @@ __global__ void __launch_bounds__(256, 1) k_dec_fused(const DecFusedArgs a)
     const int nw = blockDim.x >> 5;
     bool ok = true;
     for (int wi = blockIdx.x * nw + (threadIdx.x >> 5); wi < a.e.T * a.e.nc; wi += G * nw)
-        dec_expand_item<DE_PP, 8>(a.e, wi % a.e.T, wi / a.e.T, [&](int q) {
+        dec_expand_item<DE_PP, 8, 0>(a.e, wi % a.e.T, wi / a.e.T, [&](int q) {
             if (ok)
                 ok = wait_count(m.zcnt + q, target, status);
         });
@@ -538,7 +556,7 @@ __global__ void __launch_bounds__(256, MINB) k_dec_expand_multi(const MultiDecAr
     const DecExpandArgs ea{pj.y, pj.pool, pj.ranks, a.m, a.T, Z_ROW_FLOATS, pj.nc, a.m.z + pj.zoff};
     const int gl = g - a.wpre[j];
     bool waited = false;
-    dec_expand_item<PP, 8>(ea, gl % a.T, gl / a.T, [&](int) {
+    dec_expand_item<PP, 8, 0>(ea, gl % a.T, gl / a.T, [&](int) {
         if (!waited) {
             pdl_wait();  // z of the shrink
             waited = true;
