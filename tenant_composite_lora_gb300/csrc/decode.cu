@@ -27,8 +27,9 @@
 //    sum_pairs sum_j z[q][j] * B_a[j][cols] in fp32, 8 or 16 rows in flight
 //    at a time, and rounds once to bf16.  The launch picks the instance that
 //    keeps the batch's warps in one wave where it can (fewer registers, more
-//    CTAs per SM, for long batches) and a CTA of 8 warps per (token, 256
-//    columns) for few tokens at large ranks.
+//    CTAs per SM, for long batches; that instance prefetches one pair's rows
+//    and reads the next pairs' adapters and ranks before the wait) and a CTA
+//    of 8 warps per (token, 256 columns) for few tokens at large ranks.
 //
 // Both kernels order their loads so that each waits on as few dependent
 // round trips to memory as possible: a decode batch moves little data, and
