@@ -8,8 +8,8 @@
 //
 // Two stages:
 //
-// k_map_csr (every build; one CTA, or from 1024 tokens k_map_csr_wide, a CTA
-// per 256 tokens) copies the batch into the mapping in CSR order:
+// k_map_csr (every build; a CTA per 256 tokens) copies the batch into the
+// mapping in CSR order:
 //   the offsets (toff), and per pair {token, adapter} (pc; adapter -1 when
 //   the pair is left out) and alpha (calpha).  It checks the offsets (all
 //   pairs are left out when they are malformed), flags ids outside
@@ -97,125 +97,27 @@ __device__ Scan4 block_exclusive_scan4(Scan4 v, Scan4 &total, int *sh /* [4 * 32
     return {r[0], r[1], r[2], r[3]};
 }
 
-constexpr int MAP_STAGE_U = 8;  // staged words per thread per round (loads in flight)
-
-// Stages words in shared memory: n_a words from src_a, then n_b from src_b,
-// then n_c from src_c, one index space.  MAP_STAGE_U loads in flight per
-// thread before any store.
-__device__ __forceinline__ void stage_words(int32_t *dst, const int32_t *src_a, int n_a, const int32_t *src_b,
-                                            int n_b, const int32_t *src_c, int n_c)
-{
-    const int tid = threadIdx.x, nthr = blockDim.x, n_ab = n_a + n_b, n_all = n_ab + n_c;
-    for (int base = 0; base < n_all; base += MAP_STAGE_U * nthr) {
-        int32_t v[MAP_STAGE_U];
-#pragma unroll
-        for (int u = 0; u < MAP_STAGE_U; ++u) {
-            const int i = base + u * nthr + tid;
-            v[u] = 0;
-            if (i < n_a)
-                v[u] = __ldg(src_a + i);
-            else if (i < n_ab)
-                v[u] = __ldg(src_b + (i - n_a));
-            else if (i < n_all)
-                v[u] = __ldg(src_c + (i - n_ab));
-        }
-#pragma unroll
-        for (int u = 0; u < MAP_STAGE_U; ++u) {
-            const int i = base + u * nthr + tid;
-            if (i < n_all)
-                dst[i] = v[u];
-        }
-    }
-}
-
 struct CsrArgs {
     MapDev m;
     const int32_t *off, *ids;
     const float *alpha;
-    int T, P, cap, staged;
+    int T, P, cap;
 };
 
-__global__ void __launch_bounds__(MAP_THREADS, 1) k_map_csr(const CsrArgs a)
-{
-    extern __shared__ __align__(16) int32_t sh[];
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    const int T = a.T, P = a.P, cap = a.cap;
-    const MapDev &m = a.m;
-    // Launched as a programmatic dependent of the previous kernel in the
-    // stream: the CTA starts and stages the batch's inputs (which no kernel of
-    // the library writes) while that kernel finishes, and waits for it before
-    // writing anything.  Its own dependents may launch at once: they wait too.
-    pdl_launch_dependents();
-    const int32_t *off = a.off, *ids = a.ids, *alb = reinterpret_cast<const int32_t *>(a.alpha);
-    if (a.staged) {
-        // offsets, ids and alpha bits consecutive in shared memory
-        stage_words(sh, a.off, T + 1, a.ids, P, alb, P);
-        off = sh;
-        ids = sh + T + 1;
-        alb = ids + P;
-        __syncthreads();  // every thread reads words that others staged
-    }
-    pdl_wait();  // the previous kernel (which may still read this mapping) is done
-    if (tid == 0) {
-        m.hdr[HDR_STATUS] = 0;
-        m.hdr[HDR_BAR] = 0;  // fused-kernel counters start over with every mapping
-        m.hdr[HDR_BAR_BASE] = 0;
-        m.hdr[HDR_EXIT] = 0;
-        m.hdr[HDR_EPOCH] = 0;
-        m.hdr[HDR_DEXIT] = 0;
-        m.hdr[HDR_T] = T;
-        atomicAdd(&m.hdr[HDR_BUILD], 1);  // the sorted tuples are stale from here on (no round trip)
-    }
-    for (int p = tid; p < P; p += nthr)
-        m.zcnt[p] = 0;
-    // the offsets: off[0] = 0, off[T] = P, non-decreasing
-    int bad = (tid == 0) && (off[0] != 0 || off[T] != P);
-    for (int t = tid; t < T; t += nthr)
-        bad |= off[t + 1] < off[t];
-    if (__syncthreads_or(bad)) {
-        // every pair left out: empty pair ranges, no adapter
-        for (int t = tid; t <= T; t += nthr)
-            m.toff[t] = 0;
-        for (int p = tid; p < P; p += nthr) {
-            m.pc[p] = make_int2(-1, -1);
-            m.calpha[p] = 0.f;
-        }
-        if (tid == 0)
-            atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_OFFSETS);
-        return;
-    }
-    // a thread per token writes its pairs: {token, adapter} and alpha
-    bool bad_id = false;
-    for (int t = tid; t <= T; t += nthr) {
-        m.toff[t] = off[t];
-        if (t == T)
-            continue;
-        const int p0 = off[t], p1 = off[t + 1];
-        for (int p = p0; p < p1; ++p) {
-            const int id = ids[p];
-            const bool ok = id >= 0 && id < cap;
-            bad_id |= !ok;
-            m.pc[p] = make_int2(t, ok ? id : -1);
-            m.calpha[p] = __int_as_float(alb[p]);
-        }
-    }
-    if (bad_id)
-        atomicOr(&m.hdr[HDR_STATUS], LORA_DEV_BAD_ID);
-}
-
-// The CSR stage of a long batch over several CTAs, a thread per token.
+// The CSR stage over a CTA per CSR_TOKENS tokens, a thread per token.
 // Before the dependency wait each thread reads its token's offsets and the
-// ids and alpha of its first CSR_WIDE_PR pairs (inputs no kernel of the
+// ids and alpha of its first CSR_PR pairs (inputs no kernel of the
 // library writes); after it, it writes its token's records.  A CTA that
 // finds its tokens' offsets malformed writes no records and flags it; so do
 // ids outside the pool.  The CTA that finishes last (a counter in the
 // header) writes the status word from the flags of all CTAs, clears both
 // words, and -- when some offsets were malformed -- leaves every pair out,
-// over the records the other CTAs wrote.
-constexpr int CSR_WIDE_TOKENS = 256;  // tokens per CTA, one per thread
-constexpr int CSR_WIDE_PR = 8;        // pairs per token read before the wait
+// over the records the other CTAs wrote; a grid of one CTA does all of that
+// itself, without the counter.
+constexpr int CSR_TOKENS = 256;  // tokens per CTA, one per thread
+constexpr int CSR_PR = 8;        // pairs per token read before the wait
 
-__global__ void __launch_bounds__(CSR_WIDE_TOKENS) k_map_csr_wide(const CsrArgs a)
+__global__ void __launch_bounds__(CSR_TOKENS) k_map_csr(const CsrArgs a)
 {
     __shared__ int s_last, s_flags;
     const int tid = threadIdx.x;
@@ -223,7 +125,7 @@ __global__ void __launch_bounds__(CSR_WIDE_TOKENS) k_map_csr_wide(const CsrArgs 
     const int32_t *alb = reinterpret_cast<const int32_t *>(a.alpha);
     const MapDev &m = a.m;
     pdl_launch_dependents();  // the dependents wait for this grid
-    const int t = b * CSR_WIDE_TOKENS + tid;
+    const int t = b * CSR_TOKENS + tid;
     int e0 = 0, e1 = 0;
     if (t < T) {
         e0 = __ldg(a.off + t);
@@ -236,10 +138,12 @@ __global__ void __launch_bounds__(CSR_WIDE_TOKENS) k_map_csr_wide(const CsrArgs 
         bad |= e0 != 0;
     if (t == T - 1)
         bad |= e1 != P;
+    if (T == 0 && t == 0)  // no token: the offsets are {0} and there is no pair
+        bad |= __ldg(a.off) != 0 || P != 0;
     bad = __syncthreads_or(bad);
-    int idv[CSR_WIDE_PR], alv[CSR_WIDE_PR];
+    int idv[CSR_PR], alv[CSR_PR];
 #pragma unroll
-    for (int i = 0; i < CSR_WIDE_PR; ++i) {
+    for (int i = 0; i < CSR_PR; ++i) {
         const bool in = !bad && e0 + i < e1;
         idv[i] = in ? __ldg(a.ids + e0 + i) : 0;
         alv[i] = in ? __ldg(alb + e0 + i) : 0;
@@ -255,28 +159,46 @@ __global__ void __launch_bounds__(CSR_WIDE_TOKENS) k_map_csr_wide(const CsrArgs 
         atomicAdd(&m.hdr[HDR_BUILD], 1);  // the sorted tuples are stale from here on
     }
     const int q0 = (int)((long long)b * P / G), q1 = (int)((long long)(b + 1) * P / G);
-    for (int p = q0 + tid; p < q1; p += CSR_WIDE_TOKENS)
+    for (int p = q0 + tid; p < q1; p += CSR_TOKENS)
         m.zcnt[p] = 0;
     int bad_id = 0;
+    if (!bad && T == 0 && t == 0)
+        m.toff[0] = 0;
     if (!bad && t < T) {
         m.toff[t] = e0;
         if (t == T - 1)
             m.toff[T] = P;
 #pragma unroll
-        for (int i = 0; i < CSR_WIDE_PR; ++i)
+        for (int i = 0; i < CSR_PR; ++i)
             if (e0 + i < e1) {
                 const bool ok = idv[i] >= 0 && idv[i] < cap;
                 bad_id |= !ok;
                 m.pc[e0 + i] = make_int2(t, ok ? idv[i] : -1);
                 m.calpha[e0 + i] = __int_as_float(alv[i]);
             }
-        for (int e = e0 + CSR_WIDE_PR; e < e1; ++e) {
+        for (int e = e0 + CSR_PR; e < e1; ++e) {
             const int id = __ldg(a.ids + e);
             const bool ok = id >= 0 && id < cap;
             bad_id |= !ok;
             m.pc[e] = make_int2(t, ok ? id : -1);
             m.calpha[e] = __int_as_float(__ldg(alb + e));
         }
+    }
+    if (G == 1) {
+        // one CTA: it is the last; the status in one store, and on malformed
+        // offsets every pair left out (it wrote no records)
+        bad_id = __syncthreads_or(bad_id);
+        if (tid == 0)
+            m.hdr[HDR_STATUS] = bad ? LORA_DEV_BAD_OFFSETS : (bad_id ? LORA_DEV_BAD_ID : 0);
+        if (bad) {
+            for (int u = tid; u <= T; u += CSR_TOKENS)
+                m.toff[u] = 0;
+            for (int p = tid; p < P; p += CSR_TOKENS) {
+                m.pc[p] = make_int2(-1, -1);
+                m.calpha[p] = 0.f;
+            }
+        }
+        return;
     }
     __threadfence();  // every thread's records before this CTA's count
     bad_id = __syncthreads_or(bad_id);
@@ -300,9 +222,9 @@ __global__ void __launch_bounds__(CSR_WIDE_TOKENS) k_map_csr_wide(const CsrArgs 
     __syncthreads();
     if (s_last && (s_flags & LORA_DEV_BAD_OFFSETS)) {
         // every pair left out: empty pair ranges, no adapter
-        for (int u = tid; u <= T; u += CSR_WIDE_TOKENS)
+        for (int u = tid; u <= T; u += CSR_TOKENS)
             m.toff[u] = 0;
-        for (int p = tid; p < P; p += CSR_WIDE_TOKENS) {
+        for (int p = tid; p < P; p += CSR_TOKENS) {
             m.pc[p] = make_int2(-1, -1);
             m.calpha[p] = 0.f;
         }
@@ -713,27 +635,12 @@ int map_global_hist_words(int capacity)
 cudaError_t launch_map_csr(const MapDev &m, const int32_t *offsets, const int32_t *ids, const float *alpha, int T,
                            int P, int capacity, cudaStream_t st)
 {
-    const long long budget = MAP_SMEM_BYTES / 4;  // int32 words
-    if (T >= 4 * CSR_WIDE_TOKENS) {
-        // long batches: a CTA per CSR_WIDE_TOKENS tokens, no shared memory
-        static thread_local int wide_done = -1;  // per host thread
-        const cudaError_t e = map_attrs(k_map_csr_wide, wide_done);
-        if (e != cudaSuccess)
-            return e;
-        const CsrArgs a{m, offsets, ids, alpha, T, P, capacity, 0};
-        return map_launch(k_map_csr_wide, a, CSR_WIDE_TOKENS, 0, st,
-                          (unsigned)((T + CSR_WIDE_TOKENS - 1) / CSR_WIDE_TOKENS));
-    }
-    const long long words = (long long)(T + 1) + 2LL * P;
-    const int staged = words <= budget ? 1 : 0;
-    // a short batch is one staging round of 256 threads (cheaper block-wide steps)
-    const int threads = (T + 1 + 2LL * P <= 256LL * MAP_STAGE_U) ? 256 : MAP_THREADS;
     static thread_local int attr_done = -1;  // per host thread
     const cudaError_t e = map_attrs(k_map_csr, attr_done);
     if (e != cudaSuccess)
         return e;
-    const CsrArgs a{m, offsets, ids, alpha, T, P, capacity, staged};
-    return map_launch(k_map_csr, a, threads, staged ? 4 * (size_t)words : 0, st);
+    const CsrArgs a{m, offsets, ids, alpha, T, P, capacity};
+    return map_launch(k_map_csr, a, CSR_TOKENS, 0, st, T > 0 ? (unsigned)((T + CSR_TOKENS - 1) / CSR_TOKENS) : 1u);
 }
 
 cudaError_t launch_map_sort(const MapDev &m, int T, int P, int capacity, cudaStream_t st)

@@ -121,6 +121,13 @@ def test_mapping_bad_offsets_and_degenerate():
     # no pairs at all, and one token with every adapter of a large pool
     compare_mapping(_map_raw([0, 0, 0], [], [], 5), oracle.build_mapping(
         np.zeros(3, np.int32), np.zeros(0, np.int32), np.zeros(0, np.float32), capacity=5))
+    # no token: offsets {0} and no pair; offsets {2} with two pairs is malformed
+    compare_mapping(_map_raw([0], [], [], 5), oracle.build_mapping(
+        np.zeros(1, np.int32), np.zeros(0, np.int32), np.zeros(0, np.float32), capacity=5))
+    got = _map_raw([2], [0, 1], np.ones(2), 5)
+    compare_mapping(got, oracle.build_mapping(np.array([2], np.int32), np.array([0, 1], np.int32),
+                                              np.ones(2, np.float32), capacity=5))
+    assert got["status"] & 2
     cap = 3000
     ids = np.random.default_rng(3).permutation(cap).astype(np.int32)
     offsets = np.array([0, cap], np.int32)
