@@ -142,13 +142,22 @@ __global__ void __launch_bounds__(CSR_TOKENS) k_map_csr(const CsrArgs a)
         bad |= __ldg(a.off) != 0 || P != 0;
     bad = __syncthreads_or(bad);
     int idv[CSR_PR], alv[CSR_PR];
+    int pre_bad_id = 0;
 #pragma unroll
     for (int i = 0; i < CSR_PR; ++i) {
         const bool in = !bad && e0 + i < e1;
         idv[i] = in ? __ldg(a.ids + e0 + i) : 0;
         alv[i] = in ? __ldg(alb + e0 + i) : 0;
+        pre_bad_id |= in && (idv[i] < 0 || idv[i] >= cap);
     }
+    // a one-CTA grid whose tokens hold at most CSR_PR pairs each knows its
+    // status before the wait (no barrier after it)
+    const bool one_pass = G == 1 && !__syncthreads_or(!bad && e1 - e0 > CSR_PR);
+    const int pre_status =
+        one_pass ? (bad ? LORA_DEV_BAD_OFFSETS : (__syncthreads_or(pre_bad_id) ? LORA_DEV_BAD_ID : 0)) : 0;
     pdl_wait();  // the previous kernel (which may still read this mapping) is done
+    if (one_pass && tid == 0)
+        m.hdr[HDR_STATUS] = pre_status;
     if (b == 0 && tid == 0) {
         m.hdr[HDR_BAR] = 0;  // fused-kernel counters start over with every mapping
         m.hdr[HDR_BAR_BASE] = 0;
@@ -185,11 +194,14 @@ __global__ void __launch_bounds__(CSR_TOKENS) k_map_csr(const CsrArgs a)
         }
     }
     if (G == 1) {
-        // one CTA: it is the last; the status in one store, and on malformed
-        // offsets every pair left out (it wrote no records)
-        bad_id = __syncthreads_or(bad_id);
-        if (tid == 0)
-            m.hdr[HDR_STATUS] = bad ? LORA_DEV_BAD_OFFSETS : (bad_id ? LORA_DEV_BAD_ID : 0);
+        // one CTA: it is the last; the status in one store (written above when
+        // it was known before the wait), and on malformed offsets every pair
+        // left out (it wrote no records)
+        if (!one_pass) {
+            bad_id = __syncthreads_or(bad_id);
+            if (tid == 0)
+                m.hdr[HDR_STATUS] = bad ? LORA_DEV_BAD_OFFSETS : (bad_id ? LORA_DEV_BAD_ID : 0);
+        }
         if (bad) {
             for (int u = tid; u <= T; u += CSR_TOKENS)
                 m.toff[u] = 0;
