@@ -13,7 +13,8 @@
 //    decode batches; DyMerge-LoRA page, "Core idea": the weight alpha folded
 //    in).  A CTA owns one pair q and 4 or 8 consecutive rank rows (long
 //    batches at large ranks: several such row groups of its pair in turn);
-//    its x row is staged once in shared memory and each warp streams one row
+//    its x row is staged once in shared memory (or, in CTAs of 8 rows, read
+//    by each warp into registers) and each warp streams one row
 //    of A_a (stored transposed, contiguous along d_in) against it, reducing
 //    with warp shuffles:  z[q][j] = alpha_q * sum_d x[tok_q][d] * A_a[d][j].
 //
@@ -77,7 +78,7 @@ __device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc)
 // the x row staged once).  Every thread of the CTA calls it; it returns once
 // the CTA's copies have landed.  report: set the status bit of an unusable
 // adapter (one item per pair does).
-template <bool GROUPS>
+template <bool GROUPS, bool XREG = false>
 __device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *xs, int q, int j0, int ngrp,
                                                 bool report)
 {
@@ -103,6 +104,40 @@ __device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *x
     }
     const bool row = j < k_early;
     const int d_in = a.pool.d_in, nv = d_in / 8;  // 16-byte vectors per row
+    if (XREG && nv <= 32 * 16) {
+        // (the 8-row CTAs of ranks above 8) each warp reads the x row itself
+        // into registers (from L2 after the first warp) beside its A row, so
+        // that no block barrier waits for the slowest of the 8 warps' copies
+        const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)tk * d_in);
+        const uint4 *ar = reinterpret_cast<const uint4 *>(a.pool.At + ((size_t)ad * r_max + (row ? j : 0)) * d_in);
+        uint4 av[16], xv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int i = u * 32 + lane;
+            const bool in = row && i < nv;
+            av[u] = in ? __ldcs(&ar[i]) : make_uint4(0u, 0u, 0u, 0u);
+            xv[u] = in ? __ldg(&xr[i]) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int k = effective_rank(a.pool, a.ranks, ad);
+        if (k <= 0 || j0 >= k) {
+            if (k < 0 && report && threadIdx.x == 0)
+                atomicOr(a.m.hdr + HDR_STATUS, k == -1 ? LORA_DEV_UNREGISTERED : LORA_DEV_BAD_RANK);
+            return;
+        }
+        if (j >= k)
+            return;  // this warp's row is at or past the rank (uniform over the warp)
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (u * 32 + lane < nv)
+                acc = dot8(av[u], xv[u], acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0)
+            a.z[(size_t)q * a.zs + j] = al * acc;
+        return;
+    }
     // second round trip: x row (to shared memory), the A row, the rank
     const uint4 *xr = reinterpret_cast<const uint4 *>(a.x + (size_t)tk * d_in);
     for (int i = threadIdx.x; i < nv; i += blockDim.x)
@@ -167,6 +202,9 @@ __device__ __forceinline__ void dec_shrink_item(const DecShrinkArgs &a, uint4 *x
     }
 }
 
+// XREG: CTAs of 8 rank rows take the x row into each warp's registers
+// (measured faster there; slower for the 4-row CTAs of ranks up to 8).
+template <bool XREG>
 __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a)
 {
     extern __shared__ __align__(16) uint4 xs[];  // the pair's x row
@@ -178,7 +216,7 @@ __global__ void __launch_bounds__(DS_THREADS) k_dec_shrink(const DecShrinkArgs a
     // included -- must have completed.  Its prologue still overlaps the work
     // below.
     pdl_launch_dependents();
-    dec_shrink_item<false>(a, xs, blockIdx.x, blockIdx.y * (blockDim.x >> 5), 1, blockIdx.y == 0);
+    dec_shrink_item<false, XREG>(a, xs, blockIdx.x, blockIdx.y * (blockDim.x >> 5), 1, blockIdx.y == 0);
 }
 
 // The same over several row groups of its pair per CTA (long batches at large ranks).
@@ -582,7 +620,10 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     int dev = 0;
     cudaGetDevice(&dev);
     if (attr_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(k_dec_shrink, cudaFuncAttributeMaxDynamicSharedMemorySize, DS_SMEM_MAX);
+        cudaError_t e = cudaFuncSetAttribute(k_dec_shrink<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             DS_SMEM_MAX);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_dec_shrink<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, DS_SMEM_MAX);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k_dec_shrink_groups, cudaFuncAttributeMaxDynamicSharedMemorySize, DS_SMEM_MAX);
         if (e != cudaSuccess)
@@ -615,8 +656,9 @@ cudaError_t launch_decode(const __nv_bfloat16 *x, __nv_bfloat16 *y, const PoolDe
     scfg.stream = st;
     scfg.attrs = attr;
     scfg.numAttrs = 1;
-    cudaError_t e = sa.gpc > 1 ? cudaLaunchKernelEx(&scfg, k_dec_shrink_groups, sa)
-                               : cudaLaunchKernelEx(&scfg, k_dec_shrink, sa);
+    cudaError_t e = sa.gpc > 1   ? cudaLaunchKernelEx(&scfg, k_dec_shrink_groups, sa)
+                    : rpc == 8 ? cudaLaunchKernelEx(&scfg, k_dec_shrink<true>, sa)
+                               : cudaLaunchKernelEx(&scfg, k_dec_shrink<false>, sa);
     if (e != cudaSuccess)
         return e;
     const int nc = (pool.d_out + 255) / 256;
