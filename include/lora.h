@@ -163,7 +163,9 @@ lora_status lora_mapping_create(int max_tokens, int max_pairs, int capacity, lor
  * lora_mapping_export) enqueues before its own kernels; later calls on the
  * same build find them there (a device-side build counter decides, so this
  * also holds inside CUDA graphs; an eager call on the stream of an earlier
- * eager sort of the same build does not launch it at all).
+ * eager sort of the same build does not launch it at all, unless a build of
+ * this mapping was ever enqueued into a graph, whose replays the host does
+ * not see).
  * One mapping serves every lora_delta_apply on the same batch (all
  * projections and layers).  The input arrays need to stay valid only until
  * the stream reaches this call.

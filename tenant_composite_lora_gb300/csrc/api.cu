@@ -57,10 +57,14 @@ struct lora_mapping {
     bool built;
     // host-side record of the sort stage: builds so far, and the build and
     // stream (by its unique id: a handle may be reused after destruction) of
-    // the last sort enqueued eagerly (not into a graph)
+    // the last sort enqueued eagerly (not into a graph).  graph_builds: a
+    // build was enqueued into a caller's graph, whose replays the count
+    // cannot see -- the sort launch is then never left out.  self_capture:
+    // the host entry point is capturing its own step graph (its replays
+    // advance the count).
     long long builds, sorted_builds;
     unsigned long long sorted_stream;
-    bool sorted_valid;
+    bool sorted_valid, graph_builds, self_capture;
     tcl::MapDev dev;
     // staging of lora_delta_apply_host
     void *sx, *sy;
@@ -410,7 +414,7 @@ cudaError_t sort_mapping(const lora_mapping *cm, cudaStream_t st)
         cudaGetLastError();
         eager = false;  // no id: launch, record nothing
     }
-    if (eager && m->sorted_valid && m->sorted_stream == sid && m->sorted_builds == m->builds)
+    if (eager && !m->graph_builds && m->sorted_valid && m->sorted_stream == sid && m->sorted_builds == m->builds)
         return cudaSuccess;
     const cudaError_t e = launch_map_sort(m->dev, m->T, m->P, m->capacity, st);
     if (e == cudaSuccess && eager) {
@@ -659,10 +663,19 @@ lora_status lora_build_mapping(lora_mapping *m, const int32_t *offsets_dev, cons
         return LORA_ERR_INVALID_ARG;
     if (P > 0 && (!ids_dev || !alpha_dev))
         return LORA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (!m->self_capture) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            cs = cudaStreamCaptureStatusActive;  // unknown: as if captured
+        }
+        if (cs != cudaStreamCaptureStatusNone)
+            m->graph_builds = true;
+    }
     // the CSR stage only: the paths that read the adapter-sorted tuples sort
     // them first (once per build)
-    cudaError_t e = launch_map_csr(m->dev, offsets_dev, ids_dev, alpha_dev, T, P, m->capacity,
-                                   static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_map_csr(m->dev, offsets_dev, ids_dev, alpha_dev, T, P, m->capacity, st);
     if (e != cudaSuccess)
         return from_cuda(e);
     m->T = T;
@@ -990,7 +1003,9 @@ lora_status lora_delta_apply_host(const void *x_host, void *y_host, const int32_
         cudaGraphExec_t exec = nullptr;
         lora_status s = from_cuda(cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal));
         if (s == LORA_OK) {
+            m->self_capture = true;
             s = host_step(x_host, y_host, offsets_host, ids_host, alpha_host, T, P, pool, ranks_dev, m, stream, al);
+            m->self_capture = false;
             const cudaError_t e2 = cudaStreamEndCapture(st, &graph);
             if (s == LORA_OK && e2 == cudaSuccess && graph)
                 s = from_cuda(cudaGraphInstantiate(&exec, graph, 0));

@@ -220,3 +220,39 @@ def test_sorted_path_across_streams_and_builds(name):
     _, acc2, _ = oracle.apply_workload(b2, threads=0)
     for g, acc in zip(got, (acc1, acc1, acc2, acc2)):
         delta_gate(g, acc)
+
+
+@pytest.mark.parametrize("name", ["zipf", "long"])
+def test_eager_sorted_apply_after_replayed_graph_build(name):
+    """A build captured into a caller's graph and replayed rebuilds the
+    mapping without the host seeing it: an eager sorted-path apply on the
+    same stream afterwards must still sort the replayed build."""
+    import tenant_composite_lora_gb300 as tcl
+    wl = make_case(name)
+    b2 = other_batch(wl, 57)
+    dw = DeviceWorkload(wl, build=False)
+    s = torch.cuda.Stream()
+    try:
+        l1, l2 = device_lists(wl), device_lists(b2)
+        ys = [dw.y0.clone() for _ in range(3)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(s):
+            dw.mapping.build(*l1, s)
+            tcl.delta_apply(dw.x, ys[0], dw.pool, dw.mapping, path=PATH_SPLIT, stream=s)
+            s.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                dw.mapping.build(*l2, s)
+            # the capture ran nothing: the mapping still holds the first batch
+            tcl.delta_apply(dw.x, ys[1], dw.pool, dw.mapping, path=PATH_SPLIT, stream=s)
+            g.replay()
+            tcl.delta_apply(dw.x, ys[2], dw.pool, dw.mapping, path=PATH_SPLIT, stream=s)
+        s.synchronize()
+        got = [bf16_to_numpy_bits(y) for y in ys]
+        mapping_matches(dw.mapping.export(s), b2)
+    finally:
+        dw.close()
+    _, acc1, _ = oracle.apply_workload(wl, threads=0)
+    _, acc2, _ = oracle.apply_workload(b2, threads=0)
+    for gy, acc in zip(got, (acc1, acc1, acc2)):
+        delta_gate(gy, acc)
