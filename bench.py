@@ -527,6 +527,27 @@ class ColdTimer:
             b2 = self._mean_ms(self.g_flush, n)
         return max(0.0, ((a + a2) - (b + b2)) / 2 * 1e3)
 
+    def time_spread_us(self, fn, n=100, blocks=10):
+        """As time_us (2n replays of the work, 2n of the read alone), in
+        `blocks` alternating blocks: the mean and the spread of the blocks."""
+        g = self.capture(fn)
+        per = max(1, (2 * n) // blocks)
+        with self.torch.cuda.stream(self.stream):
+            return cold_blocks_us(lambda: self._mean_ms(g, per), lambda: self._mean_ms(self.g_flush, per), blocks)
+
+
+def cold_blocks_us(work_ms, flush_ms, blocks: int):
+    """Alternate `blocks` times a block of [read, work] replays (work_ms():
+    its mean ms per replay) with a block of the read alone (flush_ms()); the
+    work's own time per block is the difference.  Returns the mean over the
+    blocks (microseconds, at least 0) and their median, p10 and p90."""
+    diffs = []
+    for _ in range(blocks):
+        a = work_ms()
+        b = flush_ms()
+        diffs.append((a - b) * 1e3)
+    return max(0.0, float(np.mean(diffs))), spread(diffs)
+
 
 def per_config_lines(args, peak, torch, stream, dev):
     """Every workload of the metric: the apply and the step (mapping +
@@ -554,8 +575,8 @@ def per_config_lines(args, peak, torch, stream, dev):
                     native.lora_build_mapping(m, dw.offsets, dw.ids, dw.alpha, wl.T, wl.P, stream)
                     native.lora_delta_apply(dw.x, y, pool, None, m, stream)
 
-                apply_us = timer.time_us(apply_)
-                step_us = timer.time_us(step_)
+                apply_us, apply_sp = timer.time_spread_us(apply_)
+                step_us, step_sp = timer.time_spread_us(step_)
             finally:
                 dw.close()
         path = PATH_NAMES[native.lora_dispatch_choose(wl.T, wl.P, wl.r_max, wl.d_in, wl.d_out)]
@@ -565,10 +586,13 @@ def per_config_lines(args, peak, torch, stream, dev):
             "tokens_per_s": round(wl.T / (step_us * 1e-6), 1) if step_us > 0 else None,
             "algorithmic_bytes": ab["total"], "achieved_gbs": round(achieved, 1) if achieved else None,
             "frac": round(achieved / peak, 4) if achieved else None, "traffic": ncu_traffic(name, path),
+            "apply_us_blocks": apply_sp, "step_us_blocks": step_sp,
             "setup_s": round(time.perf_counter() - t0, 2),
         }
     return {"protocol": "cold L2: a 256 MB read before every timed replay, its own time subtracted; "
-                        "mean over 200 replays; path = the dispatch table's", "configs": out}
+                        "mean over 200 replays in 10 blocks of 20, alternating with blocks of the read "
+                        "alone (*_blocks: median, p10, p90 of the blocks); path = the dispatch table's",
+            "configs": out}
 
 
 def ablation_lines(torch, stream, dev):

@@ -91,3 +91,17 @@ def test_pass_times_and_spread():
     sp = bench.spread([m * 1e3 / 4 for m in ms])  # 4 steps per pass, microseconds
     assert sp["median"] == 750.0 and sp["samples"] == 5
     assert sp["p10"] == 350.0 and sp["p90"] == 1150.0
+
+
+def test_cold_blocks_subtract_the_read_per_block():
+    """Each block's work time is its [read, work] mean less the next block of
+    the read alone; the mean and the percentiles are over the blocks."""
+    work = iter([0.050, 0.052, 0.051, 0.060])
+    flush = iter([0.040, 0.041, 0.040, 0.040])
+    mean, sp = bench.cold_blocks_us(lambda: next(work), lambda: next(flush), 4)
+    diffs = [10.0, 11.0, 11.0, 20.0]
+    assert abs(mean - sum(diffs) / 4) < 1e-9
+    assert sp["samples"] == 4 and abs(sp["median"] - 11.0) < 1e-9
+    assert sp["p10"] <= sp["median"] <= sp["p90"]
+    neg, _ = bench.cold_blocks_us(lambda: 0.039, lambda: 0.040, 3)
+    assert neg == 0.0
