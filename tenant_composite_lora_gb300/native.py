@@ -226,6 +226,10 @@ def lora_mapping_create(max_tokens: int, max_pairs: int, capacity: int) -> int:
 
 
 def lora_build_mapping(m: int, offsets, ids, alpha, T: int, P: int, stream=None):
+    fn = "lora_build_mapping"
+    _need(fn, "offsets", offsets, T + 1)
+    _need(fn, "ids", ids, P)
+    _need(fn, "alpha", alpha, P)
     _check("lora_build_mapping",
            load().lora_build_mapping(m, _dptr(offsets, "offsets", "int32"), _dptr(ids, "ids", "int32"),
                                      _dptr(alpha, "alpha", "float32"), T, P, _stream(stream)))
@@ -258,6 +262,7 @@ def lora_delta_apply_ablation(x, y, pool: int, ranks, m: int, variant: int, work
     ws = workspace if workspace is None or isinstance(workspace, int) else workspace.data_ptr()
     if workspace is not None and not isinstance(workspace, int) and not workspace.is_cuda:
         raise ValueError("workspace: a CUDA tensor is expected")
+    _need_bytes("lora_delta_apply_ablation", workspace, workspace_bytes)
     _check("lora_delta_apply_ablation",
            load().lora_delta_apply_ablation(_dptr(x, "x", "bf16"), _dptr(y, "y", "bf16"), pool,
                                             _dptr(ranks, "ranks", "int32"), m, variant, ws, workspace_bytes,
@@ -265,12 +270,25 @@ def lora_delta_apply_ablation(x, y, pool: int, ranks, m: int, variant: int, work
 
 
 def lora_gate_logits(x, wg, req, T: int, E: int, d_in: int, logits, stream=None):
+    fn = "lora_gate_logits"
+    if T > 0 and E > 0 and d_in > 0:
+        _need(fn, "x", x, T * d_in)
+        _need(fn, "wg", wg, E * d_in)
+        _need(fn, "req", req, T)
+        _need(fn, "logits", logits, T * E)
     _check("lora_gate_logits",
            load().lora_gate_logits(_dptr(x, "x", "bf16"), _dptr(wg, "wg", "bf16"), _dptr(req, "req", "int32"), T, E,
                                    d_in, _dptr(logits, "logits", "float32"), _stream(stream)))
 
 
 def lora_gate_topk(logits, cand, T: int, E: int, top_k: int, offsets, ids, alpha, stream=None):
+    fn = "lora_gate_topk"
+    if T > 0 and 1 <= top_k <= min(E, 8) and E <= 64:  # (other values: the library refuses them)
+        _need(fn, "logits", logits, T * E)
+        _need(fn, "cand", cand, T * E)
+        _need(fn, "offsets", offsets, T + 1)
+        _need(fn, "ids", ids, T * top_k)
+        _need(fn, "alpha", alpha, T * top_k)
     _check("lora_gate_topk",
            load().lora_gate_topk(_dptr(logits, "logits", "float32"), _dptr(cand, "cand", "int32"), T, E, top_k,
                                  _dptr(offsets, "offsets", "int32"), _dptr(ids, "ids", "int32"),
@@ -288,6 +306,14 @@ def lora_recompress(A, B, M: int, d_in: int, d_out: int, r: int, F, T, sigma, wo
     buffer of lora_recompress_workspace_bytes(M, d_in, r)."""
     if workspace is not None and not isinstance(workspace, int) and not workspace.is_cuda:
         raise ValueError("workspace: a CUDA tensor is expected")
+    fn = "lora_recompress"
+    if M > 0 and d_in > 0 and d_out > 0 and r > 0:
+        _need(fn, "A", A, M * d_in * r)
+        _need(fn, "B", B, M * r * d_out)
+        _need(fn, "F", F, M * d_in * r)
+        _need(fn, "T", T, M * r * d_out)
+        _need(fn, "sigma", sigma, M * r)
+    _need_bytes(fn, workspace, workspace_bytes)
     ws = workspace if workspace is None or isinstance(workspace, int) else workspace.data_ptr()
     _check("lora_recompress",
            load().lora_recompress(_dptr(A, "A", "bf16"), _dptr(B, "B", "bf16"), M, d_in, d_out, r,
@@ -302,6 +328,8 @@ def lora_rank_allocate(sigma, rank, cost, policy: int, d: int, floor_k: int = 1)
     rank = np.ascontiguousarray(rank, np.int32)
     cost = np.ascontiguousarray(cost, np.int32)
     M, r = sigma.shape
+    _need("lora_rank_allocate", "rank", rank, M)
+    _need("lora_rank_allocate", "cost", cost, M)
     k = np.zeros(M, np.int32)
     _check("lora_rank_allocate",
            load().lora_rank_allocate(sigma.ctypes.data, M, r, rank.ctypes.data, cost.ctypes.data, policy, d, floor_k,
@@ -321,6 +349,14 @@ def lora_dispatch_choose(T: int, P: int, r_max: int, d_in: int, d_out: int) -> i
 
 def lora_delta_apply_host(x_host, y_host, offsets_host, ids_host, alpha_host, T: int, P: int,
                           pool: int, ranks, m: int, stream=None):
+    fn = "lora_delta_apply_host"
+    _need(fn, "offsets_host", offsets_host, T + 1)
+    _need(fn, "ids_host", ids_host, P)
+    _need(fn, "alpha_host", alpha_host, P)
+    for name, t in (("x_host", x_host), ("y_host", y_host)):
+        rc = _rows_cols(t)
+        if rc is not None and rc[0] < T:
+            raise ValueError(f"{fn}: {name} has {rc[0]} rows, at least T = {T} needed")
     _check("lora_delta_apply_host",
            load().lora_delta_apply_host(_hptr(x_host, "x_host", "bf16"), _hptr(y_host, "y_host", "bf16"),
                                         _hptr(offsets_host, "offsets_host", "int32"),
@@ -334,6 +370,23 @@ def _numel(t) -> int | None:
     if t is None or isinstance(t, int):
         return None
     return int(t.size) if isinstance(t, np.ndarray) else int(t.numel())
+
+
+def _need(fn: str, name: str, t, want: int):
+    """Refuse a tensor or array of fewer than `want` elements: the library
+    would read or write past it (raw addresses and None are not checked)."""
+    n = _numel(t)
+    if n is not None and want > 0 and n < want:
+        raise ValueError(f"{fn}: {name} holds {n} entries, at least {want} needed")
+
+
+def _need_bytes(fn: str, t, want: int):
+    """The same for a workspace given as a tensor, in bytes."""
+    if t is None or isinstance(t, int):
+        return
+    n = int(t.numel()) * int(t.element_size())
+    if want > 0 and n < want:
+        raise ValueError(f"{fn}: the workspace holds {n} bytes, {want} passed as its size")
 
 
 def _rows_cols(t):
@@ -417,6 +470,7 @@ def lora_mapping_destroy(m: int):
 
 def lora_diag_wait_expiry(kind: int, limit_ns: int, words, stream=None):
     """words: device int32 [4] (words[1] = 0 for kind 1)."""
+    _need("lora_diag_wait_expiry", "words", words, 4)
     _check("lora_diag_wait_expiry",
            load().lora_diag_wait_expiry(kind, limit_ns, _dptr(words, "words", "int32"), _stream(stream)))
 

@@ -299,3 +299,78 @@ def test_rank_allocate_matches_the_oracle(lib):
             got = native.lora_rank_allocate(sig, rank, cost, pol, d, fl)
             want = RC.rank_allocate(list(sig.astype(np.float64)), cost, rank, key, d, fl)
             assert got.tolist() == want, (trial, key)
+
+
+def test_binding_checks_array_sizes_before_the_library():
+    """The other entry points taking arrays refuse one with fewer elements
+    than their sizes imply (the kernels would read or write past it), before
+    any library call (CPU tensors: the size checks come before the memory
+    checks); calls whose parameters the library refuses itself reach it."""
+    import numpy as np
+    import torch
+    from tenant_composite_lora_gb300 import native
+
+    fake = 1  # never dereferenced: every call below raises before the library
+    i32 = lambda n: torch.zeros(n, dtype=torch.int32)
+    f32 = lambda *s: torch.zeros(*s, dtype=torch.float32)
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    T, P = 4, 6
+    with pytest.raises(ValueError, match="lora_build_mapping: offsets holds 4 entries, at least 5"):
+        native.lora_build_mapping(fake, i32(4), i32(P), f32(P), T, P, 0)
+    with pytest.raises(ValueError, match="lora_build_mapping: ids holds 5 entries, at least 6"):
+        native.lora_build_mapping(fake, i32(T + 1), i32(5), f32(P), T, P, 0)
+    with pytest.raises(ValueError, match="lora_build_mapping: alpha holds 5 entries, at least 6"):
+        native.lora_build_mapping(fake, i32(T + 1), i32(P), f32(5), T, P, 0)
+    # larger buffers than the batch are fine (the memory check is what fails here)
+    with pytest.raises(ValueError, match="offsets: a CUDA tensor is expected"):
+        native.lora_build_mapping(fake, i32(64), i32(64), f32(64), T, P, 0)
+
+    x, y = bf(T, 64).view(torch.int16), bf(T, 64).view(torch.int16)
+    with pytest.raises(ValueError, match="lora_delta_apply_host: offsets_host holds 4 entries"):
+        native.lora_delta_apply_host(x, y, i32(4), i32(P), f32(P), T, P, fake, None, fake, 0)
+    with pytest.raises(ValueError, match="lora_delta_apply_host: ids_host holds 5 entries"):
+        native.lora_delta_apply_host(x, y, i32(T + 1), i32(5), f32(P), T, P, fake, None, fake, 0)
+    with pytest.raises(ValueError, match="lora_delta_apply_host: alpha_host holds 5 entries"):
+        native.lora_delta_apply_host(x, y, i32(T + 1), i32(P), f32(5), T, P, fake, None, fake, 0)
+    with pytest.raises(ValueError, match="lora_delta_apply_host: x_host has 3 rows"):
+        native.lora_delta_apply_host(x[:3], y, i32(T + 1), i32(P), f32(P), T, P, fake, None, fake, 0)
+    with pytest.raises(ValueError, match="lora_delta_apply_host: y_host has 3 rows"):
+        native.lora_delta_apply_host(x, y[:3], i32(T + 1), i32(P), f32(P), T, P, fake, None, fake, 0)
+
+    E, d_in = 8, 64
+    with pytest.raises(ValueError, match="lora_gate_logits: x holds"):
+        native.lora_gate_logits(bf(T - 1, d_in), bf(E, d_in), i32(T), T, E, d_in, f32(T, E))
+    with pytest.raises(ValueError, match="lora_gate_logits: wg holds"):
+        native.lora_gate_logits(bf(T, d_in), bf(E - 1, d_in), i32(T), T, E, d_in, f32(T, E))
+    with pytest.raises(ValueError, match="lora_gate_logits: req holds"):
+        native.lora_gate_logits(bf(T, d_in), bf(E, d_in), i32(T - 1), T, E, d_in, f32(T, E))
+    with pytest.raises(ValueError, match="lora_gate_logits: logits holds"):
+        native.lora_gate_logits(bf(T, d_in), bf(E, d_in), i32(T), T, E, d_in, f32(T, E - 1))
+    k = 2
+    good = dict(logits=f32(T * E), cand=i32(T * E), offsets=i32(T + 1), ids=i32(T * k), alpha=f32(T * k))
+    for name, short in (("logits", f32(T * E - 1)), ("cand", i32(T * E - 1)), ("offsets", i32(T)),
+                        ("ids", i32(T * k - 1)), ("alpha", f32(T * k - 1))):
+        a = dict(good, **{name: short})
+        with pytest.raises(ValueError, match=f"lora_gate_topk: {name} holds"):
+            native.lora_gate_topk(a["logits"], a["cand"], T, E, k, a["offsets"], a["ids"], a["alpha"])
+
+    M, r, d_out = 2, 4, 32
+    good = dict(A=bf(M, d_in, r), B=bf(M, r, d_out), F=f32(M, d_in, r), T=f32(M, r, d_out), sigma=f32(M, r))
+    for name, short in (("A", bf(M, d_in, r - 1)), ("B", bf(M, r, d_out - 1)), ("F", f32(1, d_in, r)),
+                        ("T", f32(M, r - 1, d_out)), ("sigma", f32(M, r - 1))):
+        a = dict(good, **{name: short})
+        with pytest.raises(ValueError, match=f"lora_recompress: {name} holds"):
+            native.lora_recompress(a["A"], a["B"], M, d_in, d_out, r, a["F"], a["T"], a["sigma"], None, 0)
+
+    with pytest.raises(ValueError, match="lora_rank_allocate: rank holds 2 entries, at least 3"):
+        native.lora_rank_allocate(np.ones((3, 4), np.float32), [4, 4], [8, 8, 8], native.LORA_RANK_UNIFORM, 2)
+    with pytest.raises(ValueError, match="lora_rank_allocate: cost holds 2 entries, at least 3"):
+        native.lora_rank_allocate(np.ones((3, 4), np.float32), [4, 4, 4], [8, 8], native.LORA_RANK_UNIFORM, 2)
+    with pytest.raises(ValueError, match="lora_diag_wait_expiry: words holds 3 entries, at least 4"):
+        native.lora_diag_wait_expiry(0, 10_000, i32(3))
+    # parameters the library refuses itself (top_k above 8, E above 64) skip
+    # the size checks, so that the library's own status comes back
+    with pytest.raises(ValueError, match="logits: a CUDA tensor is expected"):
+        native.lora_gate_topk(f32(16), i32(16), 2, 8, 9, i32(16), i32(16), f32(16))
+    with pytest.raises(ValueError, match="logits: a CUDA tensor is expected"):
+        native.lora_gate_topk(f32(16), i32(16), 2, 65, 2, i32(16), i32(16), f32(16))
