@@ -354,9 +354,9 @@ def lora_delta_apply_host(x_host, y_host, offsets_host, ids_host, alpha_host, T:
     _need(fn, "ids_host", ids_host, P)
     _need(fn, "alpha_host", alpha_host, P)
     for name, t in (("x_host", x_host), ("y_host", y_host)):
-        rc = _rows_cols(t)
-        if rc is not None and rc[0] < T:
-            raise ValueError(f"{fn}: {name} has {rc[0]} rows, at least T = {T} needed")
+        shape = getattr(t, "shape", None)
+        if shape is not None and len(shape) == 2 and shape[0] < T:
+            raise ValueError(f"{fn}: {name} has {shape[0]} rows, at least T = {T} needed")
     _check("lora_delta_apply_host",
            load().lora_delta_apply_host(_hptr(x_host, "x_host", "bf16"), _hptr(y_host, "y_host", "bf16"),
                                         _hptr(offsets_host, "offsets_host", "int32"),
@@ -375,9 +375,10 @@ def _numel(t) -> int | None:
 def _need(fn: str, name: str, t, want: int):
     """Refuse a tensor or array of fewer than `want` elements: the library
     would read or write past it (raw addresses and None are not checked)."""
-    n = _numel(t)
-    if n is not None and want > 0 and n < want:
-        raise ValueError(f"{fn}: {name} holds {n} entries, at least {want} needed")
+    if want > 0 and t is not None and not isinstance(t, int):
+        n = t.size if isinstance(t, np.ndarray) else t.numel()
+        if n < want:
+            raise ValueError(f"{fn}: {name} holds {n} entries, at least {want} needed")
 
 
 def _need_bytes(fn: str, t, want: int):
